@@ -1,0 +1,86 @@
+"""Parsers for the hand-derived text fixtures under tests/golden/."""
+import os
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+def fval(v):
+    """A decimal number, or an exact fp32 bit pattern written h<hex>."""
+    import numpy as np
+    if v.startswith("h"):
+        return float(np.array([int(v[1:], 16)], np.uint32).view(np.float32)[0])
+    return float(v)
+
+
+def _kv(text, conv):
+    out = {}
+    for tok in text.split():
+        k, v = tok.split("=")
+        out[int(k)] = conv(v)
+    return out
+
+
+def quantize_cases():
+    cases, cur = [], None
+    for line in _lines("quantize_ties.txt"):
+        key, _, rest = line.partition(":") if not line.startswith("row ") else ("row", None, line[4:])
+        if key == "row":
+            cur = {"name": rest.strip()}
+            cases.append(cur)
+        elif key == "x":
+            cur["x"] = _kv(rest, fval)
+        elif key == "s":
+            cur["s"] = fval(rest.strip())
+        elif key == "q":
+            cur["q"] = _kv(rest, int)
+        elif key == "bsum":
+            cur["bsum"] = _kv(rest, int)
+    return cases
+
+
+def gemm_cases():
+    cases, cur = [], None
+    for line in _lines("gemm_q8_0_small.txt"):
+        if line.startswith("case "):
+            cur = {"name": line[5:].strip(), "w": {}, "y": {}, "bf16": {}}
+            cases.append(cur)
+            continue
+        key, _, rest = line.partition(":")
+        rest = rest.strip()
+        if key == "K":
+            cur["K"] = int(rest)
+        elif key == "x":
+            cur["x"] = _kv(rest, float)
+        elif key.startswith("w"):
+            dpart, qpart = rest.split(" q=")
+            d = [int(h, 16) for h in dpart[2:].split(",")]
+            cur["w"][int(key[1:])] = (d, _kv(qpart, int))
+        elif key.startswith("y"):
+            cur["y"][int(key[1:])] = float(rest)
+        elif key.startswith("bf16_"):
+            cur["bf16"][int(key[5:])] = int(rest, 16)
+    return cases
+
+
+def q4k_case():
+    c = {}
+    for line in _lines("q4k_superblock.txt"):
+        key, _, rest = line.partition(":")
+        rest = rest.strip()
+        if key in ("header", "scales", "nibbles8"):
+            c[key] = [int(h, 16) for h in rest.split()]
+        elif key in ("d", "dmin"):
+            c[key] = float(rest)
+        elif key in ("sc", "m"):
+            c[key] = [int(v) for v in rest.split()]
+        elif key == "w":
+            c["w"] = _kv(rest, float)
+    return c

@@ -1,0 +1,355 @@
+"""Pins for the CPU oracle (no GPU): every check here compares the oracle with
+something other than itself -- hand-derived fixtures, library routines for the
+special cases they reduce to (numpy float16, torch bf16 rounding, int64
+matrix products), fp64 brute force within the matching bound, and invariants
+the method fixes (exact int32 sums, batch invariance, sign and power-of-two
+symmetry)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_quantized_gemm_gb300 import synth
+import golden_io
+
+
+def f16_bits(v):
+    return int(np.array([v], np.float16).view(np.uint16)[0])
+
+
+# ----------------------------------------------------------------- conversions
+def test_f16_decode_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    L = oracle.lib()
+    got = np.array([L.orc_f16_to_f32(int(b)) for b in bits], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_bf16_rounding_matches_torch_rne():
+    rng = np.random.default_rng(7)
+    u = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    # add exact ties (low 16 bits 0x8000) on both parities and the overflow edge
+    ties = (rng.integers(0, 2**16, size=5000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    edge = np.array([0x7F7FFFFF, 0x7F7F8000, 0xFF7FFFFF, 0x00008000, 0x00018000, 0x3F808000], np.uint32)
+    u = np.concatenate([u, ties, edge])
+    f = u.view(np.float32)
+    f = f[~np.isnan(f)]
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    L = oracle.lib()
+    got = np.array([L.orc_f32_to_bf16(float(v)) for v in f], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ----------------------------------------------------------------- quantizer
+@pytest.mark.parametrize("case", golden_io.quantize_cases(), ids=lambda c: c["name"])
+def test_quantize_golden(case):
+    K = 32
+    x = np.zeros((1, K), np.float32)
+    for k, v in case["x"].items():
+        x[0, k] = v
+    q, s, bs = oracle.quantize_act(x, bsum=True)
+    assert s[0] == np.float32(case["s"])
+    exp = np.zeros(K, np.int8)
+    for k, v in case["q"].items():
+        exp[k] = v
+    assert np.array_equal(q[0], exp)
+    assert bs[0, 0] == case["bsum"][0]
+
+
+def test_quantize_one_hot_closed_form():
+    for c in (3.0, -3.0, 1e-20, 7.5e4):
+        x = np.zeros((1, 64), np.float32)
+        x[0, 5] = c
+        q, s = oracle.quantize_act(x)
+        assert s[0] == np.float32(abs(c)) / np.float32(127.0)
+        exp = np.zeros(64, np.int8)
+        exp[5] = 127 if c > 0 else -127
+        assert np.array_equal(q[0], exp)
+
+
+def _quant_invariants(x, q, s):
+    x64 = x.astype(np.float64)
+    s64 = s.astype(np.float64)[:, None]
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    nz = s != 0
+    # the absmax element maps to +-127
+    assert np.all(np.abs(q[nz]).max(axis=1) == 127)
+    # |x/s - q| <= 1/2 up to the fp32 division's rounding
+    r = np.where(nz[:, None], x64 / np.where(s64 == 0, 1, s64), 0.0)
+    assert np.all(np.abs(r - q) <= 0.5 + 1e-5)
+    assert np.all((np.sign(q) == np.sign(x)) | (q == 0))
+    # s is the correctly rounded absmax/127
+    am = np.abs(x).max(axis=1)
+    assert np.array_equal(s, (am / np.float32(127)).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_quantize_invariants_random(dtype):
+    x, bits = synth.activations(11, 37, 320, dtype=dtype, outlier_frac=0.01, seq_slots=8, min_len=2)
+    src = bits if dtype == "bf16" else x
+    q, s, bs = oracle.quantize_act(src, bsum=True)
+    _quant_invariants(x, q, s)
+    assert np.array_equal(bs, q.astype(np.int64).reshape(37, 10, 32).sum(axis=2))
+    # sign symmetry and power-of-two scaling: same q (negated), exactly scaled s
+    qn, sn = oracle.quantize_act(-x)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    q4, s4 = oracle.quantize_act(x * np.float32(4.0))
+    assert np.array_equal(q4, q) and np.array_equal(s4, s * np.float32(4.0))
+    # rows are independent
+    perm = np.random.default_rng(3).permutation(37)
+    qp, sp = oracle.quantize_act(x[perm])
+    assert np.array_equal(qp, q[perm]) and np.array_equal(sp, s[perm])
+
+
+# ----------------------------------------------------------------- Q8_0 GEMM
+def _decode_q8_0(blocks):
+    N, B, _ = blocks.shape
+    d = blocks[:, :, 0:2].copy().view(np.float16).reshape(N, B).astype(np.float64)
+    qw = blocks[:, :, 2:].copy().view(np.int8).astype(np.int64)
+    return d, qw
+
+
+def _brute_q8_0(qa, sa, blocks):
+    """fp64 sum of every term q_a*q_w*d*s_a and the sum of magnitudes."""
+    d, qw = _decode_q8_0(blocks)
+    N, B, _ = blocks.shape
+    M = qa.shape[0]
+    qa_b = qa.astype(np.int64).reshape(M, B, 32)
+    isum = np.einsum("mbk,nbk->mnb", qa_b, qw)              # exact int64
+    terms = isum.astype(np.float64) * d[None, :, :]
+    exact = terms.sum(axis=2) * sa.astype(np.float64)[:, None]
+    mag = np.abs(terms).sum(axis=2) * np.abs(sa.astype(np.float64))[:, None]
+    return exact, mag, isum
+
+
+def _blocks_from_golden(case):
+    K = case["K"]
+    B = K // 32
+    N = len(case["w"])
+    blocks = np.zeros((N, B, 34), np.uint8)
+    for n, (d, q) in case["w"].items():
+        for b in range(B):
+            blocks[n, b, 0] = d[b] & 0xFF
+            blocks[n, b, 1] = d[b] >> 8
+        qq = np.zeros(K, np.int8)
+        for k, v in q.items():
+            qq[k] = v
+        blocks[n, :, 2:] = qq.view(np.uint8).reshape(B, 32)
+    return blocks
+
+
+@pytest.mark.parametrize("case", golden_io.gemm_cases(), ids=lambda c: c["name"])
+def test_gemm_q8_0_golden(case):
+    K = case["K"]
+    x = np.zeros((1, K), np.float32)
+    for k, v in case["x"].items():
+        x[0, k] = v
+    qa, sa = oracle.quantize_act(x)
+    blocks = _blocks_from_golden(case)
+    y, out = oracle.gemm_w8a8_q8_0(qa, sa, blocks)
+    for n, v in case["y"].items():
+        assert y[0, n] == np.float32(v), (n, y[0, n], v)
+        assert out[0, n] == case["bf16"][n]
+
+
+@pytest.mark.parametrize("M,K,N,seed", [(4, 256, 128, 0), (3, 512, 17, 1), (1, 32, 5, 2), (7, 96, 33, 3)])
+def test_gemm_q8_0_bruteforce(M, K, N, seed):
+    if (M, K, N) == (4, 256, 128):
+        x, _ = synth.config_activations("tiny_w8a8", M, K)
+        blocks = synth.config_weights("tiny_w8a8", N, K)
+    else:
+        x, _ = synth.activations(seed, M, K, dtype="bf16", outlier_frac=0.05)
+        blocks = synth.q8_0_weights(seed + 100, N, K)
+    qa, sa = oracle.quantize_act(x)
+    y, out = oracle.gemm_w8a8_q8_0(qa, sa, blocks)
+    exact, mag, isum = _brute_q8_0(qa, sa, blocks)
+    assert np.all(np.abs(y.astype(np.float64) - exact) <= 1e-5 * mag + 1e-30)
+    ref_bf16 = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out, ref_bf16)
+    assert np.array_equal(oracle.block_sums_q8_0(qa, blocks), isum.astype(np.int32))
+
+
+def test_block_sum_extremes_are_exact():
+    # |isum| reaches 32*127*127 = 516128; int32 holds it exactly
+    M, K, N = 2, 64, 3
+    qa = np.full((M, K), 127, np.int8)
+    qa[1] = -127
+    blocks = np.zeros((N, 2, 34), np.uint8)
+    blocks[:, :, 0:2] = np.array([f16_bits(1.0)], np.uint16).view(np.uint8)
+    blocks[0, :, 2:] = np.full(32, 127, np.int8).view(np.uint8)
+    blocks[1, :, 2:] = np.full(32, -127, np.int8).view(np.uint8)
+    alt = np.array([127, -127] * 16, np.int8)
+    blocks[2, :, 2:] = alt.view(np.uint8)
+    isum = oracle.block_sums_q8_0(qa, blocks)
+    assert isum[0, 0, 0] == 516128 and isum[0, 1, 0] == -516128 and isum[1, 0, 0] == -516128
+    assert isum[0, 2, 0] == 0
+    y, _ = oracle.gemm_w8a8_q8_0(qa, np.ones(M, np.float32), blocks)
+    assert y[0, 0] == np.float32(2 * 516128) and y[1, 1] == np.float32(2 * 516128)
+
+
+def test_gemm_q8_0_special_cases():
+    M, K, N = 3, 128, 9
+    x, _ = synth.activations(5, M, K, dtype="f32")
+    x[1] = 0.0                                     # all-zero row
+    blocks = synth.q8_0_weights(105, N, K)
+    blocks[4, :, 0:2] = 0                          # d = 0 for every block of row 4
+    qa, sa = oracle.quantize_act(x)
+    y, out = oracle.gemm_w8a8_q8_0(qa, sa, blocks)
+    assert np.all(y[1].view(np.uint32) == 0) and np.all(out[1] == 0)   # +0.0
+    assert np.all(y[:, 4] == 0)
+    # one-hot activation: y = fl(fl(127*q_w[n,k0]*d) * s), one rounding each
+    x1 = np.zeros((1, K), np.float32)
+    x1[0, 40] = 2.75
+    q1, s1 = oracle.quantize_act(x1)
+    y1, _ = oracle.gemm_w8a8_q8_0(q1, s1, blocks)
+    d, qw = _decode_q8_0(blocks)
+    for n in range(N):
+        acc = np.float32(127 * qw[n, 1, 8]) * np.float32(d[n, 1])
+        assert y1[0, n] == np.float32(acc * s1[0])
+
+
+def test_gemm_q8_0_invariants():
+    M, K, N = 6, 192, 40
+    x, _ = synth.activations(9, M, K, dtype="bf16", outlier_frac=0.02)
+    blocks = synth.q8_0_weights(109, N, K)
+    qa, sa = oracle.quantize_act(x)
+    y, out = oracle.gemm_w8a8_q8_0(qa, sa, blocks)
+    # sign symmetry
+    qn, sn = oracle.quantize_act(-x)
+    yn, _ = oracle.gemm_w8a8_q8_0(qn, sn, blocks)
+    assert np.array_equal(yn, -y)
+    # power-of-two scaling of the activations scales the outputs exactly
+    q8, s8 = oracle.quantize_act(x * np.float32(8.0))
+    y8, _ = oracle.gemm_w8a8_q8_0(q8, s8, blocks)
+    assert np.array_equal(y8, y * np.float32(8.0))
+    # row permutation and batch invariance: each row alone gives the same bits
+    perm = np.random.default_rng(1).permutation(M)
+    yp, _ = oracle.gemm_w8a8_q8_0(qa[perm], sa[perm], blocks)
+    assert np.array_equal(yp, y[perm])
+    for m in range(M):
+        ym, _ = oracle.gemm_w8a8_q8_0(qa[m:m + 1], sa[m:m + 1], blocks)
+        assert np.array_equal(ym[0].view(np.uint32), y[m].view(np.uint32))
+
+
+def test_q8_0_encoder_round_trip():
+    w = synth.normal_weights(3, 16, 256)
+    blocks = synth.encode_q8_0(w)
+    d, qw = _decode_q8_0(blocks)
+    wd = (qw * d[:, :, None]).reshape(16, 256)
+    am = np.abs(w.reshape(16, 8, 32)).max(axis=2)
+    assert np.array_equal(d.astype(np.float16), (am / np.float32(127)).astype(np.float16))
+    assert np.all(np.abs(wd - w) <= 0.5 * np.repeat(d, 32, axis=1) * 1.0001 + 1e-12)
+
+
+# ----------------------------------------------------------------- Q4_K
+def test_q4k_golden_superblock():
+    c = golden_io.q4k_case()
+    sb = np.array(c["header"] + c["scales"] + c["nibbles8"] * 16, np.uint8)
+    assert sb.shape == (144,)
+    dec = oracle.q4k_decode(sb)
+    assert dec["d"] == c["d"] and dec["dmin"] == c["dmin"]
+    assert list(dec["sc"]) == c["sc"] and list(dec["m"]) == c["m"]
+    assert np.array_equal(dec["q"], np.arange(256) % 16)
+    for j, v in c["w"].items():
+        assert dec["w"][j] == v, (j, dec["w"][j], v)
+    # the generator's packer writes the same bytes from the same fields
+    packed = synth.pack_q4k_fields(np.array([[0.5]], np.float16), np.array([[0.25]], np.float16),
+                                   np.array([[c["sc"]]], np.uint8), np.array([[c["m"]]], np.uint8),
+                                   (np.arange(256) % 16).astype(np.uint8)[None, None, :])
+    assert np.array_equal(packed[0, 0], sb)
+
+
+def _decode_q4k_all(sblocks):
+    N, J, _ = sblocks.shape
+    ds = np.zeros((N, J * 8))
+    dm = np.zeros((N, J * 8))
+    q = np.zeros((N, J * 256), np.int64)
+    w = np.zeros((N, J * 256))
+    for n in range(N):
+        for j in range(J):
+            dec = oracle.q4k_decode(sblocks[n, j])
+            ds[n, j * 8:(j + 1) * 8] = np.float64(dec["d"]) * dec["sc"]
+            dm[n, j * 8:(j + 1) * 8] = np.float64(dec["dmin"]) * dec["m"]
+            q[n, j * 256:(j + 1) * 256] = dec["q"]
+            w[n, j * 256:(j + 1) * 256] = dec["w"]
+    return ds, dm, q, w
+
+
+def test_q4k_encoder_round_trip_bound():
+    w = synth.normal_weights(8, 6, 512)
+    sblocks = synth.encode_q4k(w)
+    ds, dm, q, wd = _decode_q4k_all(sblocks)
+    d = np.array([[oracle.q4k_decode(sblocks[n, j])["d"] for j in range(2)] for n in range(6)])
+    dmin = np.array([[oracle.q4k_decode(sblocks[n, j])["dmin"] for j in range(2)] for n in range(6)])
+    bound = (0.5 * np.repeat(ds, 32, axis=1) + 7.5 * np.repeat(d, 256, axis=1)
+             + 0.5 * np.repeat(dmin, 256, axis=1)) * 1.001
+    assert np.all(np.abs(wd - w) <= bound)
+    assert np.all(q <= 15)
+
+
+@pytest.mark.parametrize("M,K,N,seed", [(3, 256, 12, 0), (2, 512, 7, 1), (5, 768, 4, 2)])
+def test_gemm_q4k_bruteforce(M, K, N, seed):
+    x, bits = synth.activations(seed, M, K, dtype="bf16", outlier_frac=0.02)
+    sblocks = synth.q4k_weights(seed + 100, N, K)
+    qa, sa, bs = oracle.quantize_act(bits, bsum=True)
+    y, out = oracle.gemm_w4a8_q4k(qa, sa, sblocks)
+    ds, dm, q, w = _decode_q4k_all(sblocks)
+    B = K // 32
+    qa_b = qa.astype(np.int64).reshape(M, B, 32)
+    isum = np.einsum("mbk,nbk->mnb", qa_b, q.reshape(N, B, 32))
+    asum = qa_b.sum(axis=2)
+    t1 = isum * ds[None]
+    t2 = -asum[:, None, :] * dm[None]
+    exact = (t1 + t2).sum(axis=2) * sa.astype(np.float64)[:, None]
+    mag = (np.abs(t1) + np.abs(t2)).sum(axis=2) * sa.astype(np.float64)[:, None]
+    assert np.all(np.abs(y - exact) <= 1e-5 * mag + 1e-30)
+    # the same value from the decoded fp64 weights (no use of the decomposition)
+    direct = (qa.astype(np.float64) @ w.T) * sa.astype(np.float64)[:, None]
+    assert np.all(np.abs(y - direct) <= 1e-5 * mag + 1e-30)
+    gi, ga = oracle.block_sums_q4k(qa, sblocks)
+    assert np.array_equal(gi, isum.astype(np.int32)) and np.array_equal(ga, asum.astype(np.int32))
+    assert np.array_equal(ga, bs)
+    ref_bf16 = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out, ref_bf16)
+
+
+def test_gemm_q4k_special_cases():
+    M, K, N = 2, 256, 3
+    x, _ = synth.activations(4, M, K, dtype="f32")
+    qa, sa = oracle.quantize_act(x)
+    f = lambda v: np.array([[v]], np.float16)
+    zero_q = np.zeros((1, 1, 256), np.uint8)
+    # sc = m = 0 -> 0
+    sb0 = synth.pack_q4k_fields(f(0.5), f(0.25), np.zeros((1, 1, 8), np.uint8),
+                                np.zeros((1, 1, 8), np.uint8), (np.arange(256) % 16).astype(np.uint8)[None, None])
+    # q = 0, m_i = 2 everywhere: y = s * chain of fmaf(-asum_i, dmin*2, acc)
+    sb1 = synth.pack_q4k_fields(f(0.5), f(0.25), np.ones((1, 1, 8), np.uint8),
+                                np.full((1, 1, 8), 2, np.uint8), zero_q)
+    sb2 = synth.pack_q4k_fields(f(0.0), f(0.0), np.full((1, 1, 8), 63, np.uint8),
+                                np.full((1, 1, 8), 63, np.uint8), zero_q + 15)
+    sblocks = np.concatenate([sb0, sb1, sb2], axis=0)
+    y, _ = oracle.gemm_w4a8_q4k(qa, sa, sblocks)
+    assert np.all(y[:, 0] == 0) and np.all(y[:, 2] == 0)
+    asum = qa.astype(np.int64).reshape(M, 8, 32).sum(axis=2)
+    for m in range(M):
+        acc = np.float32(0)
+        for b in range(8):   # -asum*0.5 is exact, so each step is one exact-input rounding
+            acc = np.float32(np.float64(acc) - np.float64(asum[m, b]) * 0.5)
+        assert y[m, 1] == np.float32(acc * sa[m])
+
+
+def test_gemm_q4k_batch_invariance():
+    M, K, N = 5, 512, 9
+    x, bits = synth.activations(21, M, K, dtype="bf16", outlier_frac=0.02)
+    sblocks = synth.q4k_weights(121, N, K)
+    qa, sa = oracle.quantize_act(bits)
+    y, _ = oracle.gemm_w4a8_q4k(qa, sa, sblocks)
+    for m in range(M):
+        ym, _ = oracle.gemm_w4a8_q4k(qa[m:m + 1], sa[m:m + 1], sblocks)
+        assert np.array_equal(ym[0].view(np.uint32), y[m].view(np.uint32))
+    qn, sn = oracle.quantize_act(-x)
+    yn, _ = oracle.gemm_w4a8_q4k(qn, sn, sblocks)
+    assert np.array_equal(yn, -y)
