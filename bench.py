@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the exact int8 (W8A8) / W4A8 quantized linear layer on GB300.
+
+One step = the whole hot path over one batch of the 4B-class prefill
+workload: per-token int8 quantization of the activations, then the W8A8
+(Q8_0) GEMM, for both projections of that workload (gate/up: M=2048, K=2560,
+N=9728; down: M=2048, K=9728, N=2560). Inputs are seeded synthetic (bf16
+N(0,1) activations with 1% outlier channels x20 and right-padded rows;
+weights N(0,0.02) encoded as Q8_0), resident in HBM when the timed region
+starts; L2 is flushed (a 512 MiB write) between timed steps, outside the
+per-step CUDA events.
+
+`value` = int8 GEMM tera-operations per second (2*M*N*K per GEMM, both
+projections, quantization time included). The `rows` object adds the other
+workloads of the layer, each timed per launch with an L2 flush in between:
+decode (M = 1, 8, 64) as weight-streaming GB/s, the 27B-class prefill and
+the W4A8 (Q4_K) shapes. `--impl reference` times the CPU oracle on a bounded
+sample of the same step instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_quantized_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "int8 GEMM TOPS (large M) & weight HBM GB/s (M<=64), % of GB300 roofline"
+WORKLOAD = "prefill_4b_w8a8"
+STEP_SHAPES = [(2048, 2560, 9728), (2048, 9728, 2560)]  # (M, K, N): gate/up, down
+L2_FLUSH_BYTES = 512 << 20
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get(
+            "bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_step_inputs(dev):
+    """Seeded inputs of the 4B-class prefill step (x bf16, packed Q8_0 weights)."""
+    import bit_quantized_gemm_gb300 as qg
+    layers = []
+    for i, (M, K, N) in enumerate(STEP_SHAPES):
+        x, bits = synth.config_activations(WORKLOAD, M, K, seed_offset=i)
+        blocks = synth.config_weights(WORKLOAD, N, K, seed_offset=i)
+        xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        packed = qg.pack_q8_0(torch.from_numpy(blocks).to(dev), N, K)
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+        h = torch.empty((M, K), dtype=torch.float16, device=dev)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        layers.append(dict(M=M, K=K, N=N, x=xd, bits=bits, blocks=blocks, packed=packed, q=q,
+                           s=s, h=h, out=out))
+    torch.cuda.synchronize()
+    return layers
+
+
+def step_ops():
+    return sum(2.0 * M * N * K for (M, K, N) in STEP_SHAPES)
+
+
+def run_step(layers, ev=None):
+    """quantize + GEMM for each layer; ev: optional list of (start, end) event pairs per GEMM."""
+    import bit_quantized_gemm_gb300 as qg
+    for i, L in enumerate(layers):
+        qg.quantize_act(L["x"], q16=True, out=(L["q"], L["s"], None, L["h"]))
+        if ev is not None:
+            ev[i][0].record()
+        qg.gemm_w8a8_q8_0(L["q"], L["h"], L["s"], L["packed"], L["N"], out=L["out"])
+        if ev is not None:
+            ev[i][1].record()
+
+
+def timed_launches(fn, reps, flush):
+    """Median/mean device time (ms) of fn() over reps, with an L2 flush before each."""
+    times = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def bench_rows(dev, flush, hbm, tf_burst, quick):
+    """The other workloads of the layer, per launch (GEMM kernel only)."""
+    import bit_quantized_gemm_gb300 as qg
+    rows = {}
+    reps = 5 if quick else 10
+
+    def w8a8_rows(name, shapes):
+        by_kn = {}
+        for (M, K, N) in shapes:
+            if (K, N) not in by_kn:
+                blocks = synth.config_weights(name, N, K)
+                by_kn[(K, N)] = qg.pack_q8_0(torch.from_numpy(blocks).to(dev), N, K)
+                del blocks
+            packed = by_kn[(K, N)]
+            x, bits = synth.config_activations(name, M, K)
+            xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+            q, s, _, h = qg.quantize_act(xd, q16=True)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: qg.gemm_w8a8_q8_0(q, h, s, packed, N, out=out)
+            fn()
+            t = statistics.median(timed_launches(fn, reps, flush))
+            ops = 2.0 * M * N * K
+            key = "%s_M%d_K%d_N%d" % (name, M, K, N)
+            r = {"ms": round(t, 5), "tops": round(ops / t / 1e9, 2)}
+            if M <= 64:
+                wbytes = N * K + N * (K // 32) * 2
+                algo = wbytes + M * K + 4 * M + 2 * M * N
+                gbs = algo / t / 1e6
+                r.update({"gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / hbm, 4)})
+            else:
+                r.update({"bound": "tensor", "frac": round(ops / t / 1e9 / tf_burst, 4)})
+            rows[key] = r
+        by_kn.clear()
+
+    w8a8_rows("decode_w8a8", synth.CONFIGS["decode_w8a8"]["shapes"])
+    torch.cuda.empty_cache()
+    w8a8_rows("prefill_27b_w8a8", synth.CONFIGS["prefill_27b_w8a8"]["shapes"])
+    torch.cuda.empty_cache()
+    # W4A8
+    name = "w4a8_q4k"
+    shapes = synth.CONFIGS[name]["shapes"]
+    M0, K, N = shapes[0]
+    sblocks = synth.config_weights(name, N, K)
+    packed = qg.pack_q4k(torch.from_numpy(sblocks).to(dev), N, K)
+    for (M, K, N) in shapes:
+        x, bits = synth.config_activations(name, M, K)
+        xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        q, s, bs, h = qg.quantize_act(xd, block_sums=True, q16=True)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: qg.gemm_w4a8_q4k(q, h, s, bs, packed, N, out=out)
+        fn()
+        t = statistics.median(timed_launches(fn, reps, flush))
+        ops = 2.0 * M * N * K
+        r = {"ms": round(t, 5), "tops": round(ops / t / 1e9, 2)}
+        if M <= 64:
+            algo = N * K // 256 * 144 + M * K + 4 * M + 4 * M * (K // 32) + 2 * M * N
+            gbs = algo / t / 1e6
+            r.update({"gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / hbm, 4)})
+        else:
+            r.update({"bound": "tensor", "frac": round(ops / t / 1e9 / tf_burst, 4)})
+        rows["%s_M%d_K%d_N%d" % (name, M, K, N)] = r
+    return rows
+
+
+def oracle_step_data(rows_sample):
+    """Seeded inputs for a `rows_sample`-row slice of the step (the same
+    generators as the GPU arm; rows are independent, so a slice is a fair sample)."""
+    data = []
+    for i, (M, K, N) in enumerate(STEP_SHAPES):
+        x, bits = synth.config_activations(WORKLOAD, M, K, seed_offset=i)
+        blocks = synth.config_weights(WORKLOAD, N, K, seed_offset=i)
+        data.append((np.ascontiguousarray(bits[:rows_sample]), blocks, N, K))
+    return data
+
+
+def oracle_step(data):
+    import oracle
+    for bits, blocks, N, K in data:
+        q, s = oracle.quantize_act(bits)
+        oracle.gemm_w8a8_q8_0(q, s, blocks)
+
+
+def cpu_baseline(rows_sample=1024):
+    """The oracle, as it stands, timed on a bounded sample of the step:
+    `rows_sample` of the 2048 rows of both projections (quantize + GEMM), on
+    all host cores (input generation excluded)."""
+    import oracle
+    oracle.build()
+    data = oracle_step_data(rows_sample)
+    t0 = time.perf_counter()
+    oracle_step(data)
+    dt = time.perf_counter() - t0
+    ops = sum(2.0 * rows_sample * N * K for (_, _, N, K) in data)
+    return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "%d of 2048 rows of both projections (quantize + W8A8 GEMM)" % rows_sample}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-workload rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    rank, world, local = env_rank()
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # The CPU oracle on a bounded sample of the same step (64 rows per step).
+        import oracle
+        oracle.build()
+        rows_sample = 64
+        data = oracle_step_data(rows_sample)
+
+        def ref_step():
+            oracle_step(data)
+        for _ in range(args.warmup):
+            ref_step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            ref_step()
+        dt = (time.perf_counter() - t0) / args.steps
+        ops = sum(2.0 * rows_sample * N * K for (_, _, N, K) in data)
+        v = ops / dt / 1e12
+        line = {"metric": METRIC, "value": round(v, 6), "unit": "TOPS", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int8", "data": "synthetic", "impl": "reference",
+                "config": {"workload": WORKLOAD, "shapes": STEP_SHAPES, "sample_rows": rows_sample},
+                "cpu_baseline": {"value": round(v, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+                                 "kind": "oracle",
+                                 "sample": "%d of 2048 rows of both projections per step" % rows_sample},
+                "e2e": {"value": round(v, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        sys.exit(1)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import bit_quantized_gemm_gb300 as qg
+    qg.load()
+
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    layers = make_step_inputs(dev)
+    for _ in range(max(args.warmup, 3)):
+        run_step(layers)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    step_ms, gemm_ms = [], []
+    barrier()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in layers]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run_step(layers, ev)
+            b.record()
+            b.synchronize()
+            step_ms.append(a.elapsed_time(b))
+            gemm_ms.append([e0.elapsed_time(e1) for e0, e1 in ev])
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    clocks = clk.summary()
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ops = step_ops()
+    value = world * ops / (ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the prefill GEMM; both shapes of the step)
+    gemm_tot = sum(sum(g) for g in gemm_ms) / len(gemm_ms)
+    achieved = ops / (gemm_tot * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_burst,
+                "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4), "traffic": None,
+                "peak_source": "%s bf16 dense burst (same rate as the fp16 kind the kernel uses)"
+                               % peak_src,
+                "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands)",
+                "gemm_ms_per_step": round(gemm_tot, 4)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hx = [L["x"].cpu().pin_memory() for L in layers]
+        hout = [torch.empty(L["out"].shape, dtype=torch.bfloat16).pin_memory() for L in layers]
+        h2d = sum(t.numel() * 2 for t in hx)
+        d2h = sum(t.numel() * 2 for t in hout)
+
+        def e2e_step():
+            import bit_quantized_gemm_gb300 as qg
+            for L, hxi, ho in zip(layers, hx, hout):
+                L["x"].copy_(hxi, non_blocking=True)
+                qg.quantize_act(L["x"], q16=True, out=(L["q"], L["s"], None, L["h"]))
+                qg.gemm_w8a8_q8_0(L["q"], L["h"], L["s"], L["packed"], L["N"], out=L["out"])
+                ho.copy_(L["out"], non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        et = []
+        for _ in range(max(3, args.steps // 2)):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            e2e_step()
+            b.record()
+            b.synchronize()
+            et.append(a.elapsed_time(b))
+        e2e_ms = sum(et) / len(et)
+        e2e = {"value": round(world * ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    rows = None
+    if not args.no_rows:
+        del layers
+        torch.cuda.empty_cache()
+        rows = bench_rows(dev, flush, hbm, tf_burst, quick=True)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int8", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "shapes_MKN": STEP_SHAPES,
+                           "parallelism": "replicas" if world > 1 else "single",
+                           "l2": "flushed between timed steps (512 MiB write, outside events)",
+                           "wall_s": round(t_wall, 3)},
+                "gpu_launches": 2 * len(STEP_SHAPES) * args.steps,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "rows": rows}
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,12 @@
+"""Exact int8 (W8A8) / W4A8 quantized linear layer for NVIDIA GB300 (sm_103a).
+
+The compute path is the C-ABI library libqgemm.so (include/qgemm.h), built by
+``bit_quantized_gemm_gb300.build``; this package binds it through ctypes.
+"""
+from ._lib import (QGError, check_device_error, debug_block_sums, declared_symbols,
+                   gemm_w4a8_q4k, gemm_w8a8_q8_0, load, pack_q4k, pack_q8_0, q4k_packed_bytes,
+                   q8_0_packed_bytes, quantize_act, small_m_max)
+
+__all__ = ["QGError", "check_device_error", "debug_block_sums", "declared_symbols",
+           "gemm_w4a8_q4k", "gemm_w8a8_q8_0", "load", "pack_q4k", "pack_q8_0",
+           "q4k_packed_bytes", "q8_0_packed_bytes", "quantize_act", "small_m_max"]

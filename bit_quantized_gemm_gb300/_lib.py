@@ -1,0 +1,180 @@
+"""ctypes binding of libqgemm.so (the C ABI declared in include/qgemm.h).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels. PyTorch tensors provide device memory and the current stream.
+If the shared library is missing this module raises -- there is no fallback.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SO_PATH = os.path.join(HERE, "libqgemm.so")
+HEADER = os.path.join(HERE, "..", "include", "qgemm.h")
+
+QG_OK, QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA, QG_ETIMEOUT = range(6)
+QG_BF16, QG_F32 = 0, 1
+QG_PATH_AUTO, QG_PATH_SMALL, QG_PATH_LARGE = 0, 1, 2
+PATHS = {"auto": QG_PATH_AUTO, "small": QG_PATH_SMALL, "large": QG_PATH_LARGE}
+
+_lib = None
+
+
+class QGError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s (%s)" % (msg, status))
+        self.status = status
+
+
+def load():
+    """Load libqgemm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(SO_PATH):
+        raise RuntimeError("libqgemm.so is not built: run `python -m bit_quantized_gemm_gb300.build` "
+                           "(or __graft_entry__.build()); there is no CPU fallback")
+    L = ctypes.CDLL(SO_PATH)
+    P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sigs = {
+        "qg_status_string": ([I], ctypes.c_char_p),
+        "qg_last_error": ([], ctypes.c_char_p),
+        "qg_version": ([], I),
+        "qg_small_m_max": ([], I64),
+        "qg_check_device_error": ([P], I),
+        "qg_quantize_act": ([P, I, I64, I64, I64, P, P, P, P, P], I),
+        "qg_q8_0_packed_bytes": ([I64, I64], SZ),
+        "qg_pack_q8_0": ([P, I64, I64, P, P], I),
+        "qg_gemm_w8a8_q8_0": ([P, P, P, I64, I64, P, I64, P, I, I64, P], I),
+        "qg_gemm_w8a8_q8_0_ex": ([P, P, P, I64, I64, P, I64, P, I, I64, I, P], I),
+        "qg_q4k_packed_bytes": ([I64, I64], SZ),
+        "qg_pack_q4k": ([P, I64, I64, P, P], I),
+        "qg_gemm_w4a8_q4k": ([P, P, P, P, I64, I64, P, I64, P, I, I64, P], I),
+        "qg_gemm_w4a8_q4k_ex": ([P, P, P, P, I64, I64, P, I64, P, I, I64, I, P], I),
+        "qg_debug_block_sums_q8_0": ([P, P, I64, I64, P, I64, P, I, P], I),
+        "qg_debug_block_sums_q4k": ([P, P, I64, I64, P, I64, P, I, P], I),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+def declared_symbols():
+    """Names of the functions include/qgemm.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qg_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status):
+    if status != QG_OK:
+        L = load()
+        raise QGError(status, L.qg_last_error().decode() or L.qg_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return QG_BF16
+    if dt == torch.float32:
+        return QG_F32
+    raise ValueError("dtype must be torch.bfloat16 or torch.float32")
+
+
+# ----------------------------------------------------------------------- API
+def quantize_act(x, block_sums=False, q16=False, out=None, stream=None):
+    """x: cuda [M, K] bf16/fp32 (rows may be strided) ->
+    (q int8 [M,K], scale fp32 [M], block_sums int32 [M,K/32] or None, q16 fp16 [M,K] or None).
+    `out` may supply preallocated (q, scale, block_sums, q16)."""
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        dev = x.device
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+        bs = torch.empty((M, K // 32), dtype=torch.int32, device=dev) if block_sums else None
+        h = torch.empty((M, K), dtype=torch.float16, device=dev) if q16 else None
+    else:
+        q, s, bs, h = out
+    _check(load().qg_quantize_act(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(q),
+                                  _ptr(s), _ptr(bs), _ptr(h), _stream(stream)))
+    return q, s, bs, h
+
+
+def q8_0_packed_bytes(N, K):
+    return int(load().qg_q8_0_packed_bytes(N, K))
+
+
+def q4k_packed_bytes(N, K):
+    return int(load().qg_q4k_packed_bytes(N, K))
+
+
+def pack_q8_0(blocks, N, K, stream=None):
+    """blocks: cuda uint8 tensor holding N*K/32 Q8_0 blocks of 34 bytes -> packed uint8 tensor."""
+    nbytes = q8_0_packed_bytes(N, K)
+    if nbytes == 0:
+        raise QGError(QG_EINVAL, "bad N/K for Q8_0")
+    packed = torch.empty((nbytes,), dtype=torch.uint8, device=blocks.device)
+    _check(load().qg_pack_q8_0(_ptr(blocks), N, K, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def pack_q4k(superblocks, N, K, stream=None):
+    nbytes = q4k_packed_bytes(N, K)
+    if nbytes == 0:
+        raise QGError(QG_EINVAL, "bad N/K for Q4_K")
+    packed = torch.empty((nbytes,), dtype=torch.uint8, device=superblocks.device)
+    _check(load().qg_pack_q4k(_ptr(superblocks), N, K, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def gemm_w8a8_q8_0(q, q16, scale, packed, N, out=None, out_dtype=torch.bfloat16, path="auto",
+                   stream=None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=q.device)
+    _check(load().qg_gemm_w8a8_q8_0_ex(_ptr(q), _ptr(q16), _ptr(scale), M, K, _ptr(packed), N,
+                                       _ptr(out), _dtype_code(out.dtype), out.stride(0),
+                                       PATHS[path], _stream(stream)))
+    return out
+
+
+def gemm_w4a8_q4k(q, q16, scale, block_sums, packed, N, out=None, out_dtype=torch.bfloat16,
+                  path="auto", stream=None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=q.device)
+    _check(load().qg_gemm_w4a8_q4k_ex(_ptr(q), _ptr(q16), _ptr(scale), _ptr(block_sums), M, K,
+                                      _ptr(packed), N, _ptr(out), _dtype_code(out.dtype),
+                                      out.stride(0), PATHS[path], _stream(stream)))
+    return out
+
+
+def debug_block_sums(kind, q, q16, packed, N, path, stream=None):
+    """Exact per-block integer sums isum[M][N][K/32] as the chosen kernel computes them."""
+    M, K = q.shape
+    isum = torch.empty((M, N, K // 32), dtype=torch.int32, device=q.device)
+    fn = load().qg_debug_block_sums_q8_0 if kind == "q8_0" else load().qg_debug_block_sums_q4k
+    _check(fn(_ptr(q), _ptr(q16), M, K, _ptr(packed), N, _ptr(isum), PATHS[path], _stream(stream)))
+    return isum
+
+
+def check_device_error(stream=None):
+    _check(load().qg_check_device_error(_stream(stream)))
+
+
+def small_m_max():
+    return int(load().qg_small_m_max())

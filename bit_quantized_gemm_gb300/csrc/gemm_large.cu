@@ -1,0 +1,415 @@
+// gemm_large.cu -- prefill (large-M) GEMMs on the 5th-generation tensor cores.
+//
+// Operation: the W8A8 (Q8_0) and W4A8 (Q4_K) products with exact int32 block
+// sums and a fixed ascending-block fp32 epilogue (StartLux-Prism README, "Why
+// StartLux-Prism": "Reproducible to the bit"; "How it works": int8 tensor
+// cores with exact int32 sums; the pages' own Hopper kernels used warpgroup
+// MMA with TMA, "Supported models and GPUs").
+//
+// sm_103a has no int8 kind for tcgen05.mma, so the exact integer product runs
+// as kind::f16 on integer-valued fp16 operands: int8 values (|q| <= 127) and
+// 4-bit values are exact in fp16, every product (<= 16129) is exact, and one
+// 32-wide block sum (|isum| <= 516128 < 2^20) is accumulated from zero in the
+// fp32 tensor accumulator, which holds it exactly. Each block gets its own
+// accumulator, so the tensor-memory value IS (float)isum and the epilogue is
+// one FMA per (row, token, block), in block order -- the same chain as the
+// decode kernel, so both paths give identical bits.
+//
+// Tile: 128 weight rows (MMA M, tensor-memory lanes) x 256 tokens (MMA N,
+// tensor-memory columns), K staged 64 at a time (two blocks) through a
+// 4-deep TMA ring with 128-byte swizzle. Two 256-column accumulators
+// alternate per block (512 columns, all of tensor memory), so the MMA of
+// block b+1 overlaps the epilogue of block b.
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (lane 0); for W4A8 the whole warp also converts
+//               the activation block sums of each block into a float ring
+//   warp 1      tensor-memory allocator and MMA issuer (lane 0)
+//   warps 2..9  epilogue: warp w reads lanes 32*(w%4).. of tensor memory and
+//               half (w-2)/4 of the 256 token columns; each thread keeps 128
+//               fp32 accumulators (one weight row x 128 tokens) in registers
+//               and applies acc = fma(isum, d, acc) with packed f32x2 FMAs.
+#include <cuda.h>
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+constexpr int kBN = 128;  // weight rows per tile
+constexpr int kBM = 256;  // tokens per tile
+constexpr int kBK = 64;   // K per stage
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kLThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
+constexpr uint32_t kStageBBytes = kBM * kBK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
+constexpr int kColsPerThread = kBM / (kEpiWarps / 4);  // 128
+
+struct LargeSmem {
+  uint8_t a[kStages][kStageABytes];
+  uint8_t b[kStages][kStageBBytes];
+  float asum[kAsumRing][kBM];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t afull[kAsumRing], aempty[kAsumRing];
+  uint32_t tmem_base;
+};
+constexpr size_t kLargeSmemBytes = sizeof(LargeSmem) + 1024;  // + alignment slack
+static_assert(kStageABytes % 1024 == 0 && kStageBBytes % 1024 == 0, "1024-B aligned stages");
+
+struct LargeArgs {
+  const float* d32;      // W8A8: [N][ldd] fp32 scales; W4A8: d*sc [N][ldd]
+  const float* dm32;     // W4A8: dmin*m [N][ldd]
+  const int32_t* bsum;   // W4A8: [M][B] activation block sums
+  const float* sa;       // [M]
+  void* out;
+  int64_t ldo;
+  int64_t ldd;
+  int M, N, K;
+  int out_f32;
+  int32_t* dbg;          // [M][N][B] isum export (debug) or null
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int MT, int NT, int& mt, int& nt) {
+  // groups of up to 8 token tiles; inside a group the token tile varies
+  // fastest so concurrently running CTAs share weight tiles in L2
+  constexpr int kGroup = 8;
+  const int per_group = kGroup * NT;
+  const int grp = tile / per_group;
+  const int first = grp * kGroup;
+  const int gm = min(kGroup, MT - first);
+  const int idx = tile - grp * per_group;
+  mt = first + idx % gm;
+  nt = idx / gm;
+}
+
+template <bool kQ4K, bool kDebug>
+__global__ void __launch_bounds__(kLThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const LargeArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  LargeSmem& S = *reinterpret_cast<LargeSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = args.M, N = args.N, K = args.K;
+  const int NB = K / kBlk;                  // blocks
+  const int NS = (NB + 1) / 2;              // stages per tile
+  const int MT = (M + kBM - 1) / kBM, NT = (N + kBN - 1) / kBN;
+  const int tiles = MT * NT;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.tfull[i], 1);
+      mbar_init(&S.tempty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kAsumRing; ++i) {
+      mbar_init(&S.afull[i], 32);
+      mbar_init(&S.aempty[i], kEpiWarps);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = S.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int aslot = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, MT, NT, mt, nt);
+      for (int s = 0; s < NS && ok; ++s) {
+        if (lane == 0) {
+          ok = mbar_wait(&S.empty[stage], phase ^ 1, args.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&S.full[stage], kStageABytes + kStageBBytes);
+            tma_load_2d(S.a[stage], &tmA, &S.full[stage], s * kBK, nt * kBN);
+            tma_load_2d(S.b[stage], &tmB, &S.full[stage], s * kBK, mt * kBM);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (kQ4K && ok) {
+          for (int j = 0; j < 2; ++j) {
+            const int blk = 2 * s + j;
+            if (blk >= NB) break;
+            ok = mbar_wait(&S.aempty[aslot], aphase ^ 1, args.err);
+            if (!ok) break;
+#pragma unroll
+            for (int i = 0; i < kBM / 32; ++i) {
+              const int m = mt * kBM + i * 32 + lane;
+              const int v = (m < M) ? __ldg(args.bsum + (int64_t)m * NB + blk) : 0;
+              S.asum[aslot][i * 32 + lane] = (float)v;  // exact: |v| <= 4064
+            }
+            mbar_arrive(&S.afull[aslot]);
+            if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
+          }
+        }
+      }
+    }
+    // Tail: wait until the MMA has released every stage, so that no commit
+    // arrival is still outstanding on this CTA's barriers when it exits.
+    if (lane == 0 && ok) {
+      for (int i = 0; i < kStages; ++i) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1, args.err)) break;
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kBN, kBM);
+      int stage = 0;
+      uint32_t phase = 0;
+      int tb = 0;
+      uint32_t tphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int s = 0; s < NS && ok; ++s) {
+          ok = mbar_wait(&S.full[stage], phase, args.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(S.a[stage]);
+          const uint32_t b_addr = smem_u32(S.b[stage]);
+          for (int j = 0; j < 2; ++j) {
+            if (2 * s + j >= NB) break;
+            ok = mbar_wait(&S.tempty[tb], tphase ^ 1, args.err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(tb * kBM);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t koff = (uint32_t)((j * 32 + kk * 16) * 2);  // bytes within row
+              mma_f16_ss(d_tmem, smem_desc_sw128(a_addr + koff), smem_desc_sw128(b_addr + koff),
+                         idesc, kk);
+            }
+            mma_commit(&S.tfull[tb]);
+            if (++tb == 2) { tb = 0; tphase ^= 1; }
+          }
+          mma_commit(&S.empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int tb = 0;
+    uint32_t tphase = 0;
+    int aslot = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, MT, NT, mt, nt);
+      const int n = nt * kBN + quarter * 32 + lane;
+      const bool nvalid = n < N;
+      const float* drow = args.d32 + (int64_t)(nvalid ? n : 0) * args.ldd;
+      const float* mrow = kQ4K ? args.dm32 + (int64_t)(nvalid ? n : 0) * args.ldd : nullptr;
+      float2 acc[kColsPerThread / 2];
+#pragma unroll
+      for (int i = 0; i < kColsPerThread / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+
+      for (int blk = 0; blk < NB && ok; ++blk) {
+        const float dw = nvalid ? __ldg(drow + blk) : 0.0f;
+        const float ndm = (kQ4K && nvalid) ? -__ldg(mrow + blk) : 0.0f;
+        ok = mbar_wait(&S.tfull[tb], tphase, args.err);
+        if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(tb * kBM + half * kColsPerThread);
+        const float2 dw2 = make_float2(dw, dw);
+        const float2 ndm2 = make_float2(ndm, ndm);
+        constexpr int kChunk = 16;  // columns per tensor-memory load
+#pragma unroll
+        for (int ch = 0; ch < kColsPerThread / kChunk; ++ch) {
+          uint32_t v[kChunk];
+          tmem_ld16(taddr + ch * kChunk, v);
+          tmem_wait_ld();
+          if (ch == kColsPerThread / kChunk - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.tempty[tb]);
+          }
+          if (kDebug) {
+            const int m0 = mt * kBM + half * kColsPerThread + ch * kChunk;
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+              const int m = m0 + i;
+              if (m < M && nvalid)
+                args.dbg[((int64_t)m * N + n) * NB + blk] = __float2int_rn(__uint_as_float(v[i]));
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kChunk / 2; ++i) {
+            const float2 x = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            float2& a2 = acc[ch * (kChunk / 2) + i];
+            a2 = __ffma2_rn(x, dw2, a2);
+            if (kQ4K) {
+              const float2 as = *reinterpret_cast<const float2*>(
+                  &S.asum[aslot][half * kColsPerThread + ch * kChunk + 2 * i]);
+              a2 = __ffma2_rn(as, ndm2, a2);
+            }
+          }
+        }
+        if (kQ4K) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.aempty[aslot]);
+          if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
+        }
+        if (++tb == 2) { tb = 0; tphase ^= 1; }
+      }
+      if (!ok || kDebug) continue;
+      // final scale by the activation scale and store out[m][n]
+      const int mbase = mt * kBM + half * kColsPerThread;
+#pragma unroll
+      for (int i = 0; i < kColsPerThread; ++i) {  // fully unrolled: acc stays in registers
+        const int m = mbase + i;
+        if (m < M && nvalid) {
+          const float a = (i & 1) ? acc[i / 2].y : acc[i / 2].x;
+          const float y = a * __ldg(args.sa + m);
+          if (args.out_f32)
+            reinterpret_cast<float*>(args.out)[(int64_t)m * args.ldo + n] = y;
+          else
+            reinterpret_cast<uint16_t*>(args.out)[(int64_t)m * args.ldo + n] = f32_to_bf16_rne(y);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// fp16 matrix [rows][K] row-major, box = 64 (K) x box_rows, 128-byte swizzle
+static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                      uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <bool kQ4K, bool kDebug>
+static cudaError_t launch_prefill_t(const CUtensorMap& ta, const CUtensorMap& tb,
+                                   const LargeArgs& a, cudaStream_t st) {
+  auto kern = prefill_gemm_kernel<kQ4K, kDebug>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kLargeSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)(ceil_div(a.M, kBM) * ceil_div(a.N, kBN));
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, kLThreads, kLargeSmemBytes, st>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+// returns cudaErrorNotSupported when the tensor-map encoder is unavailable
+cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
+                                const void* packed, int64_t N, void* out, bool out_f32,
+                                int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+  const Q8Layout L(N, K);
+  const auto* base = reinterpret_cast<const uint8_t*>(packed);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, kBM))
+    return cudaErrorNotSupported;
+  LargeArgs a{};
+  a.d32 = reinterpret_cast<const float*>(base + L.off_d32);
+  a.ldd = L.B4;
+  a.sa = sa;
+  a.out = out;
+  a.ldo = ldo;
+  a.M = (int)M; a.N = (int)N; a.K = (int)K;
+  a.out_f32 = out_f32 ? 1 : 0;
+  a.dbg = dbg;
+  a.err = err;
+  return dbg ? launch_prefill_t<false, true>(ta, tb, a, st)
+             : launch_prefill_t<false, false>(ta, tb, a, st);
+}
+
+cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
+                               int64_t M, int64_t K, const void* packed, int64_t N, void* out,
+                               bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err,
+                               cudaStream_t st) {
+  const Q4kLayout L(N, K);
+  const auto* base = reinterpret_cast<const uint8_t*>(packed);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, kBM))
+    return cudaErrorNotSupported;
+  LargeArgs a{};
+  a.d32 = reinterpret_cast<const float*>(base + L.off_ds32);
+  a.dm32 = reinterpret_cast<const float*>(base + L.off_dm32);
+  a.ldd = L.B;
+  a.bsum = bsum;
+  a.sa = sa;
+  a.out = out;
+  a.ldo = ldo;
+  a.M = (int)M; a.N = (int)N; a.K = (int)K;
+  a.out_f32 = out_f32 ? 1 : 0;
+  a.dbg = dbg;
+  a.err = err;
+  return dbg ? launch_prefill_t<true, true>(ta, tb, a, st)
+             : launch_prefill_t<true, false>(ta, tb, a, st);
+}
+
+}  // namespace qg

@@ -1,0 +1,297 @@
+// qg_common.cuh -- shared device helpers for the quantized linear layer
+// kernels: the packed-weight layout, bounded mbarrier waits, TMA, tcgen05
+// (tensor memory + 5th-generation MMA) and legacy int8 MMA wrappers.
+//
+// Everything here is hand-written inline PTX for sm_103a.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qgemm.h"
+
+namespace qg {
+
+// ---------------------------------------------------------------------------
+// Sizes fixed by the formats (StartLux-Prism README, "Why StartLux-Prism":
+// Q8_0 blocks of 32 int8 weights with one fp16 scale; Q4_K super-blocks of
+// 256 4-bit weights in 8 sub-blocks of 32).
+// ---------------------------------------------------------------------------
+constexpr int kBlk = 32;          // K per block / sub-block
+constexpr int kQ8Bytes = 34;      // {fp16 d; int8 q[32]}
+constexpr int kQ4kWeights = 256;  // weights per super-block
+constexpr int kQ4kBytes = 144;    // super-block bytes
+constexpr int kMaxK = 65536;
+
+// Error word codes (device-side, read by qg_check_device_error).
+constexpr uint32_t kErrTimeout = 1u;
+
+__host__ __device__ constexpr int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// Packed weight layout (opaque to callers; sized by qg_*_packed_bytes).
+//
+// Q8_0, for N rows, K columns, B = K/32 blocks, G = ceil(N/16) row groups:
+//  stream  G*B*512 B   int8 weights in the decode kernel's fragment order:
+//                       for group g, block b, lane t (r = t/4, c = t%4) the
+//                       16 bytes are q[16g+r][32b+8c .. +3],
+//                       q[16g+r+8][32b+8c .. +3], q[16g+r][32b+8c+4 .. +7],
+//                       q[16g+r+8][32b+8c+4 .. +7] -- exactly the A-operand
+//                       registers of one m16n8k32 int8 MMA (K permuted the
+//                       same way on both operands; integer sums do not
+//                       depend on the order).
+//  dsc     G*(B4/4)*128 B  fp16 scales for the decode kernel: for group g,
+//                       block quad p, row r (0..7): 16 bytes =
+//                       d[16g+r][4p .. 4p+3], d[16g+r+8][4p .. 4p+3].
+//  q16     N*K*2 B     the same int8 values as fp16, row-major [N][K]
+//                       (operand A of the prefill tensor-core kernel).
+//  d32     N*B4*4 B    scales as fp32, [N][B4] (B4 = B rounded up to 4).
+// Q4_K, with J = K/256 super-blocks per row:
+//  stream  G*B*256 B   nibbles in fragment order: for group g, block pair p,
+//                       lane t: 8 bytes for block 2p then 8 for block 2p+1;
+//                       for one block the 8 bytes are words w0, w1 with
+//                       byte j of w0 = q[16g+r][32b+8c+j] | q[16g+r+8][..] << 4
+//                       and w1 the same for k = 32b+8c+4+j.
+//  shdr    G*J*256 B   the first 16 bytes (d, dmin, 6-bit fields) of each
+//                       super-block, [G][J][16 rows][16 B].
+//  q16     N*K*2 B     q (0..15) as fp16, row-major [N][K].
+//  ds32    N*B*4 B     d*sc_b as fp32 (exact), [N][B].
+//  dm32    N*B*4 B     dmin*m_b as fp32 (exact), [N][B].
+// ---------------------------------------------------------------------------
+struct Q8Layout {
+  int64_t N, K, B, B4, G;
+  int64_t off_stream, off_dsc, off_q16, off_d32, total;
+  __host__ __device__ Q8Layout(int64_t n, int64_t k) : N(n), K(k) {
+    B = K / kBlk;
+    B4 = align_up(B, 4);
+    G = ceil_div(N, 16);
+    off_stream = 0;
+    off_dsc = align_up(off_stream + G * B * 512, 256);
+    off_q16 = align_up(off_dsc + G * (B4 / 4) * 128, 256);
+    off_d32 = align_up(off_q16 + N * K * 2, 256);
+    total = align_up(off_d32 + N * B4 * 4, 256);
+  }
+};
+
+struct Q4kLayout {
+  int64_t N, K, B, J, G;
+  int64_t off_stream, off_shdr, off_q16, off_ds32, off_dm32, total;
+  __host__ __device__ Q4kLayout(int64_t n, int64_t k) : N(n), K(k) {
+    B = K / kBlk;
+    J = K / kQ4kWeights;
+    G = ceil_div(N, 16);
+    off_stream = 0;
+    off_shdr = align_up(off_stream + G * B * 256, 256);
+    off_q16 = align_up(off_shdr + G * J * 256, 256);
+    off_ds32 = align_up(off_q16 + N * K * 2, 256);
+    off_dm32 = align_up(off_ds32 + N * B * 4, 256);
+    total = align_up(off_dm32 + N * B * 4, 256);
+  }
+};
+
+// Kernels that wait on barriers receive the address of the library's device
+// error word (one per device) and OR a code into it when a wait gives up.
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t code) {
+  if (err) atomicOr(err, code);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false (and records a timeout) after `limit` polls.
+// Each try_wait suspends the thread for a hardware-defined time slice, so the
+// default limit is on the order of seconds, far above any legitimate wait.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint32_t limit = (1u << 24)) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  set_error(err, kErrTimeout);
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor) -- 2D tiled load into shared memory, completion
+// signalled on an mbarrier as transaction bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory allocation, MMA, commit, loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has
+// completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
+// lane (taddr.lane + i), columns taddr.col .. +31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Bits: [0,14) start>>4, [16,30) leading offset>>4 (unused for swizzled
+// K-major), [32,46) stride offset>>4 (1024 B), [46,48) version 1,
+// [61,64) layout 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
+// M = m, N = n.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4)                       // D format: f32
+         | (0u << 7) | (0u << 10)        // A, B format: f16
+         | ((uint32_t)(n >> 3) << 17)    // N >> 3
+         | ((uint32_t)(m >> 4) << 24);   // M >> 4
+}
+
+// ---------------------------------------------------------------------------
+// Legacy warp-level int8 MMA (exact int32 accumulate): m16n8k32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const int (&a)[4], int b0, int b1,
+                                             const int (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(c[0]), "r"(c[1]),
+        "r"(c[2]), "r"(c[3]));
+}
+
+// (float)i for |i| < 2^22, exactly, from an int32 accumulator that started at
+// the bit pattern of 1.5*2^23: the integer add lands in the mantissa.
+constexpr int kMagicBits = 0x4B400000;
+constexpr float kMagicF = 12582912.0f;
+__device__ __forceinline__ float magic_to_float(int acc_bits) {
+  return __int_as_float(acc_bits) - kMagicF;
+}
+
+// Streaming 128-bit global load that bypasses L1 allocation.
+__device__ __forceinline__ int4 ldg_stream(const void* p) {
+  int4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+}  // namespace qg

@@ -1,0 +1,166 @@
+// quantize.cu -- per-token int8 activation quantization.
+//
+// Operation (StartLux-Prism README, "Supported models and GPUs": Q8_0 runs as
+// int8 W8A8; "How it works": int8 tensor cores with exact int32 sums): for
+// each row m, s = absmax/127 (correctly rounded fp32 division) and
+// q = clamp(rint(x/s), -127, 127) with the IEEE-rounded quotient and
+// ties-to-even; an all-zero row gives s = 0, q = 0. Optional outputs: the
+// per-32-block sums of q (the W4A8 min term needs them) and an fp16 copy of q
+// (the prefill tensor-core operand).
+//
+// One CTA per row, 256 threads, 16-byte vector loads of 8 values. The row is
+// held in registers between the absmax pass and the quantize pass when it
+// fits (K <= 256*8*kRegChunks), else re-read (second read hits L2).
+// HBM-bound: per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with q16)
+// written.
+#include "qg_common.cuh"
+
+namespace qg {
+
+constexpr int kQThreads = 256;
+constexpr int kRegChunks = 9;  // 9 * 256 * 8 = 18432 values per row in registers
+
+template <bool kBf16>
+__device__ __forceinline__ void load_chunk(const void* row, int64_t c, float (&v)[8]) {
+  if (kBf16) {
+    int4 raw = *reinterpret_cast<const int4*>(reinterpret_cast<const uint16_t*>(row) + c * 8);
+    const uint32_t w[4] = {(uint32_t)raw.x, (uint32_t)raw.y, (uint32_t)raw.z, (uint32_t)raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(row) + c * 8);
+    float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ int quant1(float x, float s, bool zero_row) {
+  if (zero_row) return 0;
+  int r = __float2int_rn(__fdiv_rn(x, s));  // IEEE quotient, then ties-to-even
+  return max(-127, min(127, r));
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
+    const void* __restrict__ x, int64_t ldx, int K, int8_t* __restrict__ q,
+    float* __restrict__ scale, int32_t* __restrict__ bsum, __half* __restrict__ q16) {
+  const int64_t m = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nchunks = K / 8;
+  const char* row = reinterpret_cast<const char*>(x) + m * ldx * (kBf16 ? 2 : 4);
+
+  float v[kRegChunks][8];
+  float amax = 0.0f;
+  const bool in_regs = nchunks <= kRegChunks * kQThreads;
+#pragma unroll
+  for (int i = 0; i < kRegChunks; ++i) {
+    const int c = tid + i * kQThreads;
+    if (c < nchunks) {
+      load_chunk<kBf16>(row, c, v[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
+    }
+  }
+  if (!in_regs) {
+    for (int c = tid + kRegChunks * kQThreads; c < nchunks; c += kQThreads) {
+      float t[8];
+      load_chunk<kBf16>(row, c, t);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(t[j]));
+    }
+  }
+  // block-wide max
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[kQThreads / 32];
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+
+  const float s = __fdiv_rn(amax, 127.0f);
+  const bool zero_row = (amax == 0.0f);
+  if (tid == 0) scale[m] = s;
+
+  int8_t* qrow = q + m * (int64_t)K;
+  __half* hrow = q16 ? q16 + m * (int64_t)K : nullptr;
+  int32_t* brow = bsum ? bsum + m * (int64_t)(K / kBlk) : nullptr;
+
+  // All lanes of a warp run every trip of the loops below (invalid chunks
+  // compute on zeros and store nothing), so the block-sum shuffles always
+  // see the full warp.
+  auto emit = [&](int c, bool valid, const float (&t)[8]) {
+    int qi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qi[j] = valid ? quant1(t[j], s, zero_row) : 0;
+    if (valid) {
+      uint32_t lo = (qi[0] & 0xFF) | ((qi[1] & 0xFF) << 8) | ((qi[2] & 0xFF) << 16) |
+                    ((uint32_t)(qi[3] & 0xFF) << 24);
+      uint32_t hi = (qi[4] & 0xFF) | ((qi[5] & 0xFF) << 8) | ((qi[6] & 0xFF) << 16) |
+                    ((uint32_t)(qi[7] & 0xFF) << 24);
+      *reinterpret_cast<uint2*>(qrow + (int64_t)c * 8) = make_uint2(lo, hi);
+      if (hrow) {
+        __half2 h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          h[j] = __halves2half2(__int2half_rn(qi[2 * j]), __int2half_rn(qi[2 * j + 1]));
+        *reinterpret_cast<uint4*>(hrow + (int64_t)c * 8) = *reinterpret_cast<uint4*>(h);
+      }
+    }
+    if (brow) {
+      // chunks 4j..4j+3 form block j; their owners are 4 consecutive lanes,
+      // all valid or all invalid (the chunk count is a multiple of 4)
+      int part = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part += qi[j];
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (valid && (c & 3) == 0) brow[c >> 2] = part;
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kRegChunks; ++i) {
+    const int c = tid + i * kQThreads;
+    const bool valid = c < nchunks;
+    if (in_regs) {
+      emit(c, valid, v[i]);
+    } else {
+      float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (valid) load_chunk<kBf16>(row, c, t);
+      emit(c, valid, t);
+    }
+  }
+  if (!in_regs) {
+    for (int base = kRegChunks * kQThreads; base < nchunks; base += kQThreads) {
+      const int c = base + tid;
+      const bool valid = c < nchunks;
+      float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (valid) load_chunk<kBf16>(row, c, t);
+      emit(c, valid, t);
+    }
+  }
+}
+
+cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
+                                int8_t* q, float* scale, int32_t* bsum, uint16_t* q16,
+                                cudaStream_t st) {
+  dim3 grid((unsigned)M), block(kQThreads);
+  if (bf16)
+    quantize_act_kernel<true><<<grid, block, 0, st>>>(x, ldx, (int)K, q, scale, bsum,
+                                                      reinterpret_cast<__half*>(q16));
+  else
+    quantize_act_kernel<false><<<grid, block, 0, st>>>(x, ldx, (int)K, q, scale, bsum,
+                                                       reinterpret_cast<__half*>(q16));
+  return cudaGetLastError();
+}
+
+}  // namespace qg

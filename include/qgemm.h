@@ -1,0 +1,179 @@
+/*
+ * qgemm.h -- C ABI of the exact int8 (W8A8) / W4A8 quantized linear layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the StartLux-Prism README describes:
+ *   - "Why StartLux-Prism", bullet "The released files as they are": Q8_0
+ *     weights run as int8 (W8A8), Q4_K_M weights on their own 4-bit values
+ *     (W4A8), with no conversion of the file's numbers;
+ *   - "Why StartLux-Prism", bullet "Reproducible to the bit", and "How it
+ *     works", bullet on int8 tensor cores: integer products are summed
+ *     exactly in int32, so a row's result does not depend on the other rows
+ *     of its batch.
+ * The pages print no formula or layout; this library fixes them as follows.
+ *
+ *   Activation quantization, per row m (token):
+ *     s[m] = absmax_k |x[m,k]| / 127            (fp32, correctly rounded)
+ *     q[m,k] = clamp(rint(x[m,k] / s[m]), -127, 127)   (IEEE division,
+ *                                                  ties to even)
+ *     an all-zero row gives s = 0 and q = 0.
+ *   W8A8 with Q8_0 weights (block b = 32 consecutive k, scale d[n,b]):
+ *     isum = sum_{k in b} q[m,k] * qw[n,k]          (exact int32)
+ *     acc  = fmaf((float)isum, d[n,b], acc)          for b = 0, 1, ... in order
+ *     y    = acc * s[m];  out = bf16(y) (round to nearest even) or y (fp32)
+ *   W4A8 with Q4_K weights (sub-block b = 32 k, super-block = 8 sub-blocks):
+ *     ds = d * sc_b, dm = dmin * m_b                 (exact fp32 products)
+ *     isum = sum q[m,k] * qw[n,k],  asum = sum q[m,k] (exact int32)
+ *     acc = fmaf((float)isum, ds, acc); acc = fmaf(-(float)asum, dm, acc)
+ *     y = acc * s[m];  out as above.
+ * Every path of this library produces these bits exactly, so results are
+ * identical whatever the batch size M, the rows' positions, or the path
+ * (decode or prefill kernel) chosen.
+ *
+ * Conventions for every call below.
+ *   - All data pointers are DEVICE pointers, allocated and owned by the
+ *     caller; the library allocates no memory and keeps no state between
+ *     calls. Sizes are element counts unless stated otherwise.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on that stream; no call
+ *     synchronizes.
+ *   - Arguments are validated on the host before any launch. A rejected call
+ *     launches nothing and returns QG_EINVAL / QG_EALIGN / QG_EUNSUPPORTED;
+ *     qg_last_error() then holds a one-line reason (thread-local).
+ *   - A failed launch returns QG_ECUDA. Device-side waits are bounded: a wait
+ *     that gives up records itself in a device error word, which
+ *     qg_check_device_error() reads (it synchronizes its stream).
+ *   - Nothing aborts and nothing prints.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QG_OK = 0,
+  QG_EINVAL = 1,        /* null pointer, non-positive or inconsistent size  */
+  QG_EALIGN = 2,        /* pointer or leading dimension not aligned         */
+  QG_EUNSUPPORTED = 3,  /* valid request that no kernel here implements     */
+  QG_ECUDA = 4,         /* CUDA runtime/launch error                        */
+  QG_ETIMEOUT = 5       /* a bounded device-side wait gave up               */
+} qg_status;
+
+typedef enum { QG_BF16 = 0, QG_F32 = 1 } qg_dtype;
+
+/* Kernel selection for the *_ex GEMM calls. AUTO picks the weight-streaming
+ * decode kernel for M <= qg_small_m_max() and the tensor-memory prefill
+ * kernel above it. Both give identical bits; forcing one is for tests and
+ * measurements. */
+typedef enum { QG_PATH_AUTO = 0, QG_PATH_SMALL = 1, QG_PATH_LARGE = 2 } qg_path;
+
+const char* qg_status_string(qg_status s);
+/* One-line reason for the last non-OK status returned on this thread. */
+const char* qg_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int qg_version(void);
+/* Largest M the AUTO path sends to the decode kernel. */
+int64_t qg_small_m_max(void);
+/* Synchronizes `stream`, then reads and clears the device error word of the
+ * current device: QG_OK, or QG_ETIMEOUT if a bounded wait gave up. */
+qg_status qg_check_device_error(void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Activation quantization (per token, dynamic absmax; see the definition    */
+/* above).                                                                   */
+/*   x          [M][ldx] of x_dtype (QG_BF16 or QG_F32), rows of K values;   */
+/*              16-byte aligned, ldx >= K, ldx*elem_size % 16 == 0.          */
+/*   q          [M][K] int8 out, 16-byte aligned.                            */
+/*   scale      [M] fp32 out.                                                */
+/*   block_sums [M][K/32] int32 out (sum of q over each 32-wide block, needed */
+/*              by the W4A8 GEMM), or NULL.                                   */
+/*   q16        [M][K] fp16 out holding the same integers as q (exact), the  */
+/*              operand of the prefill tensor-core kernel, or NULL. 16-byte   */
+/*              aligned.                                                     */
+/* K must be a positive multiple of 32 and at most 65536; M >= 1.             */
+/* ------------------------------------------------------------------------ */
+qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
+                          int8_t* q, float* scale, int32_t* block_sums, uint16_t* q16,
+                          void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Q8_0 weights (W8A8).                                                      */
+/* Input format: the weight matrix W [N][K] as N*K/32 blocks of 34 bytes,    */
+/* row-major over (n, b): {fp16 d (little endian); int8 q[32]}, weight =     */
+/* d*q. qg_pack_q8_0 rearranges them once into the library's opaque packed   */
+/* buffer (qg_q8_0_packed_bytes(N, K) bytes, 256-byte aligned, caller-owned), */
+/* which holds the int8 values in the decode kernel's fragment order, the     */
+/* scales, and an fp16 copy of the values for the prefill kernel. The values  */
+/* are never changed: d and q reach the arithmetic bit for bit.              */
+/*   blocks  device, [N][K/32][34] bytes (no alignment needed).              */
+/*   K % 32 == 0, 32 <= K <= 65536, 1 <= N <= 2^24.                          */
+/* ------------------------------------------------------------------------ */
+size_t qg_q8_0_packed_bytes(int64_t N, int64_t K);
+qg_status qg_pack_q8_0(const void* blocks, int64_t N, int64_t K, void* packed, void* stream);
+
+/* out[m][n] = the W8A8 result above for m < M, n < N.
+ *   q, scale  from qg_quantize_act ([M][K] int8, [M] fp32).
+ *   q16       the fp16 copy from qg_quantize_act; required when the prefill
+ *             kernel runs (M > qg_small_m_max() under AUTO), else may be NULL.
+ *   w_packed  from qg_pack_q8_0 with the same N, K.
+ *   out       [M][ldo] of out_dtype, 16-byte aligned, ldo >= N.
+ * Rows are independent: the bits of row m depend only on q[m], scale[m] and
+ * the weights. */
+qg_status qg_gemm_w8a8_q8_0(const int8_t* q, const uint16_t* q16, const float* scale,
+                            int64_t M, int64_t K, const void* w_packed, int64_t N,
+                            void* out, qg_dtype out_dtype, int64_t ldo, void* stream);
+qg_status qg_gemm_w8a8_q8_0_ex(const int8_t* q, const uint16_t* q16, const float* scale,
+                               int64_t M, int64_t K, const void* w_packed, int64_t N,
+                               void* out, qg_dtype out_dtype, int64_t ldo, qg_path path,
+                               void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Q4_K weights (W4A8).                                                      */
+/* Input format: W [N][K] as N*K/256 super-blocks of 144 bytes (this         */
+/* library's canonical packing; the pages give none):                        */
+/*   bytes 0-1 d, 2-3 dmin (fp16, little endian);                            */
+/*   bytes 4-15 a 96-bit little-endian string of sixteen 6-bit fields, field */
+/*     f at bits [6f, 6f+6): sc_0..sc_7 then m_0..m_7;                        */
+/*   bytes 16-143 4-bit q: weight j (0..255) is the low nibble of byte       */
+/*     16 + j/2 for even j, the high nibble for odd j.                       */
+/*   weight(j) = d*sc_i*q_j - dmin*m_i, i = j/32.                            */
+/*   K % 256 == 0, 256 <= K <= 65536, 1 <= N <= 2^24.                         */
+/* ------------------------------------------------------------------------ */
+size_t qg_q4k_packed_bytes(int64_t N, int64_t K);
+qg_status qg_pack_q4k(const void* superblocks, int64_t N, int64_t K, void* packed, void* stream);
+
+/* out[m][n] = the W4A8 result above.
+ *   block_sums  [M][K/32] int32 from qg_quantize_act (required).
+ *   Other arguments as for qg_gemm_w8a8_q8_0. */
+qg_status qg_gemm_w4a8_q4k(const int8_t* q, const uint16_t* q16, const float* scale,
+                           const int32_t* block_sums, int64_t M, int64_t K,
+                           const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                           int64_t ldo, void* stream);
+qg_status qg_gemm_w4a8_q4k_ex(const int8_t* q, const uint16_t* q16, const float* scale,
+                              const int32_t* block_sums, int64_t M, int64_t K,
+                              const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                              int64_t ldo, qg_path path, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Test support: the exact per-block integer sums as the chosen kernel sees   */
+/* them, isum[m][n][b] (int32, [M][N][K/32]), taken from the same kernels     */
+/* (decode: the int8 MMA accumulators; prefill: the tensor-memory block       */
+/* accumulators), for checking exactness. Small shapes only:                 */
+/* M*N*(K/32) <= 2^28. For Q4_K the same layout holds sum q_a*q (4-bit q).   */
+/* ------------------------------------------------------------------------ */
+qg_status qg_debug_block_sums_q8_0(const int8_t* q, const uint16_t* q16, int64_t M, int64_t K,
+                                   const void* w_packed, int64_t N, int32_t* isum,
+                                   qg_path path, void* stream);
+qg_status qg_debug_block_sums_q4k(const int8_t* q, const uint16_t* q16, int64_t M, int64_t K,
+                                  const void* w_packed, int64_t N, int32_t* isum,
+                                  qg_path path, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMM_H */

@@ -1,0 +1,99 @@
+"""Host-side checks of the C ABI (no GPU): the shared library loads, exports
+every function include/qgemm.h declares, and rejects bad arguments with the
+documented status before touching the GPU."""
+import ctypes
+import subprocess
+
+import pytest
+
+import bit_quantized_gemm_gb300 as qg
+from bit_quantized_gemm_gb300 import _lib
+from bit_quantized_gemm_gb300 import build as qbuild
+
+P = ctypes.c_void_p
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(L):
+    names = _lib.declared_symbols()
+    assert len(names) >= 16
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.SO_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(L, n)
+
+
+def test_status_strings_and_constants(L):
+    for s in range(6):
+        assert L.qg_status_string(s).decode().startswith("QG_")
+    assert L.qg_version() == 10000
+    assert L.qg_small_m_max() == 64
+
+
+def test_packed_sizes(L):
+    # sizes cover the int8 stream, the scales and the fp16 copy
+    for N, K in [(1, 32), (17, 96), (128, 256), (9728, 2560)]:
+        b = L.qg_q8_0_packed_bytes(N, K)
+        assert b % 256 == 0 and b >= N * K * 3 + N * (K // 32) * 6
+    for N, K in [(1, 256), (33, 512), (17408, 5120)]:
+        b = L.qg_q4k_packed_bytes(N, K)
+        assert b % 256 == 0 and b >= N * K * 2 + N * K // 2 + N * (K // 32) * 8
+    for N, K in [(0, 32), (4, 0), (4, 48), (4, 65536 + 32), (-1, 32)]:
+        assert L.qg_q8_0_packed_bytes(N, K) == 0
+    for N, K in [(4, 128), (4, 32), (0, 256)]:
+        assert L.qg_q4k_packed_bytes(N, K) == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _gemm(L, q=FAKE, q16=FAKE, s=FAKE, M=4, K=256, w=FAKE, N=16, out=FAKE, dt=0, ldo=16, path=0):
+    return L.qg_gemm_w8a8_q8_0_ex(P(q), P(q16), P(s), M, K, P(w), N, P(out), dt, ldo, path, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), _lib.QG_EINVAL), (dict(out=0), _lib.QG_EINVAL), (dict(w=0), _lib.QG_EINVAL),
+    (dict(M=0), _lib.QG_EINVAL), (dict(N=0), _lib.QG_EINVAL), (dict(K=48), _lib.QG_EINVAL),
+    (dict(K=0), _lib.QG_EINVAL), (dict(K=65536 + 32), _lib.QG_EINVAL),
+    (dict(ldo=8), _lib.QG_EINVAL), (dict(dt=7), _lib.QG_EINVAL), (dict(path=9), _lib.QG_EINVAL),
+    (dict(q=FAKE + 8), _lib.QG_EALIGN), (dict(out=FAKE + 2), _lib.QG_EALIGN),
+    (dict(w=FAKE + 16), _lib.QG_EALIGN), (dict(q16=FAKE + 4), _lib.QG_EALIGN),
+    (dict(M=65, q16=0), _lib.QG_EINVAL), (dict(M=4, q16=0, path=2), _lib.QG_EINVAL),
+])
+def test_gemm_argument_validation(L, kw, status):
+    assert _gemm(L, **kw) == status
+    assert L.qg_last_error().decode()
+
+
+def test_q4k_and_quantize_validation(L):
+    g = L.qg_gemm_w4a8_q4k_ex
+    assert g(P(FAKE), P(FAKE), P(FAKE), None, 4, 256, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EINVAL
+    assert g(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 4, 288, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EINVAL
+    assert g(P(FAKE), P(FAKE), P(FAKE), P(FAKE + 2), 4, 256, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EALIGN
+    qa = L.qg_quantize_act
+    assert qa(None, 0, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qa(P(FAKE), 0, 4, 40, 40, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qa(P(FAKE), 0, 4, 64, 32, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qa(P(FAKE), 0, 4, 64, 68, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EALIGN
+    assert qa(P(FAKE + 4), 1, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EALIGN
+    assert qa(P(FAKE), 5, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qa(P(FAKE), 0, 0, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    pk = L.qg_pack_q8_0
+    assert pk(P(FAKE), 4, 64, P(FAKE + 16), None) == _lib.QG_EALIGN
+    assert pk(None, 4, 64, P(FAKE), None) == _lib.QG_EINVAL
+    assert L.qg_pack_q4k(P(FAKE), 4, 128, P(FAKE), None) == _lib.QG_EINVAL
+    db = L.qg_debug_block_sums_q8_0
+    assert db(P(FAKE), P(FAKE), 4096, 4096, P(FAKE), 4096, P(FAKE), 0, None) == _lib.QG_EINVAL
+
+
+def test_binding_raises_without_gpu_work(L):
+    with pytest.raises(qg.QGError):
+        _lib._check(_lib.QG_EINVAL)

@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Matching rules (the layer's contract): quantized activations, scales and the
+per-block int32 sums are bit-exact; outputs are bit-exact too, because every
+kernel keeps the oracle's ascending-block, one-FMA-per-block fp32 chain (the
+tolerance rule |err| <= 1e-5 * sum|terms| would be the fallback, and is
+asserted as well where an fp32 output is compared).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_quantized_gemm_gb300 as qg
+from bit_quantized_gemm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from bit_quantized_gemm_gb300 import build
+    build.build()
+    oracle.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def bf16_dev(bits):
+    return to_dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def run_quant(x_vals, x_bits, want_bs=True):
+    """Quantize on the GPU; returns numpy (q, s, bs, q16) and the device tensors."""
+    xd = bf16_dev(x_bits) if x_bits is not None else to_dev(x_vals.astype(np.float32))
+    q, s, bs, h = qg.quantize_act(xd, block_sums=want_bs, q16=True)
+    torch.cuda.synchronize()
+    return (q, s, bs, h)
+
+
+def oracle_quant(x_vals, x_bits):
+    return oracle.quantize_act(x_bits if x_bits is not None else x_vals, bsum=True)
+
+
+def out_bits(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy().view(np.uint32)
+
+
+# --------------------------------------------------------------------- quantize
+@pytest.mark.parametrize("M,K,dtype,outl,seq", [
+    (4, 256, "f32", 0.0, None), (37, 320, "bf16", 0.01, 8), (3, 32, "bf16", 0.0, None),
+    (64, 5120, "bf16", 0.0, None), (9, 17408, "bf16", 0.01, None), (5, 24576, "f32", 0.01, None),
+    (130, 2560, "bf16", 0.01, 128),
+])
+def test_quantize_bit_exact(M, K, dtype, outl, seq):
+    x, bits = synth.activations(M * 7 + K, M, K, dtype=dtype, outlier_frac=outl, seq_slots=seq,
+                                min_len=1 if seq else None)
+    q, s, bs, h = run_quant(x, bits)
+    oq, os_, obs = oracle_quant(x, bits)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(bs.cpu().numpy(), obs)
+    assert np.array_equal(h.float().cpu().numpy(), oq.astype(np.float32))
+
+
+def test_quantize_golden_ties_and_strided_rows():
+    import golden_io
+    cases = golden_io.quantize_cases()
+    x = np.zeros((len(cases), 32), np.float32)
+    for i, c in enumerate(cases):
+        for k, v in c["x"].items():
+            x[i, k] = v
+    # strided rows: ldx = 64
+    wide = np.zeros((len(cases), 64), np.float32)
+    wide[:, :32] = x
+    xd = to_dev(wide)[:, :32]
+    q, s, bs, _ = qg.quantize_act(xd, block_sums=True)
+    for i, c in enumerate(cases):
+        assert s[i].item() == np.float32(c["s"])
+        exp = np.zeros(32, np.int8)
+        for k, v in c["q"].items():
+            exp[k] = v
+        assert np.array_equal(q[i].cpu().numpy(), exp)
+        assert bs[i, 0].item() == c["bsum"][0]
+
+
+# --------------------------------------------------------------------- W8A8
+def make_w8a8(M, K, N, seed, dtype="bf16", outl=0.0, seq=None):
+    x, bits = synth.activations(seed, M, K, dtype=dtype, outlier_frac=outl, seq_slots=seq,
+                                min_len=1 if seq else None)
+    blocks = synth.q8_0_weights(seed + 100, N, K)
+    return x, bits, blocks
+
+
+def gpu_w8a8(x, bits, blocks, N, path, out_dtype=torch.bfloat16):
+    K = x.shape[1]
+    q, s, _, h = run_quant(x, bits, want_bs=False)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    out = qg.gemm_w8a8_q8_0(q, h, s, packed, N, out_dtype=out_dtype, path=path)
+    torch.cuda.synchronize()
+    qg.check_device_error()
+    return out, (q, h, s, packed)
+
+
+SHAPES = [(1, 32, 16), (3, 96, 40), (8, 256, 128), (17, 512, 300), (64, 2560, 1000),
+          (65, 256, 129), (129, 1024, 257), (300, 640, 520), (513, 96, 130)]
+
+
+@pytest.mark.parametrize("M,K,N", SHAPES)
+@pytest.mark.parametrize("path", ["small", "large"])
+def test_w8a8_matches_oracle(M, K, N, path):
+    x, bits, blocks = make_w8a8(M, K, N, seed=M + K + N, outl=0.01)
+    out, _ = gpu_w8a8(x, bits, blocks, N, path)
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    got = out_bits(out)
+    bad = np.argwhere(got != ob)
+    assert bad.size == 0, "first mismatches %s" % bad[:5].tolist()
+    out32, _ = gpu_w8a8(x, bits, blocks, N, path, out_dtype=torch.float32)
+    assert np.array_equal(out_bits(out32), y.view(np.uint32))
+
+
+def test_w8a8_tiny_config_both_paths():
+    M, K, N = synth.CONFIGS["tiny_w8a8"]["shapes"][0]
+    x, _ = synth.config_activations("tiny_w8a8", M, K)
+    blocks = synth.config_weights("tiny_w8a8", N, K)
+    oq, os_ = oracle.quantize_act(x)
+    y, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    for path in ("auto", "small", "large"):
+        out, _ = gpu_w8a8(x, None, blocks, N, path)
+        assert np.array_equal(out_bits(out), ob)
+
+
+@pytest.mark.parametrize("path", ["small", "large"])
+def test_w8a8_block_sums_exact_adversarial(path):
+    """The tensor-core block accumulators must hold the exact integer sums,
+    including the extremes +-32*127*127 and full cancellation."""
+    M, K, N = 40, 256, 48
+    rng = np.random.default_rng(5)
+    qa = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    qa[0] = 127
+    qa[1] = -127
+    qa[2, ::2] = 127
+    qa[2, 1::2] = -127
+    qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    qw[0] = 127
+    qw[1] = -127
+    qw[2] = 127
+    blocks = np.zeros((N, K // 32, 34), np.uint8)
+    blocks[:, :, 0:2] = np.array([0x3C00], np.uint16).view(np.uint8)
+    blocks[:, :, 2:] = qw.view(np.uint8).reshape(N, K // 32, 32)
+    qd = to_dev(qa)
+    hd = qd.to(torch.float16)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    isum = qg.debug_block_sums("q8_0", qd, hd, packed, N, path).cpu().numpy()
+    ref = oracle.block_sums_q8_0(qa, blocks)
+    assert isum[0, 0, 0] == 516128 and isum[1, 0, 0] == -516128
+    assert np.array_equal(isum, ref)
+
+
+@pytest.mark.parametrize("path", ["small", "large"])
+def test_w8a8_special_rows(path):
+    M, K, N = 70, 256, 64
+    x, bits, blocks = make_w8a8(M, K, N, seed=3)
+    x = x.copy()
+    x[5] = 0.0                      # zero row
+    x[6] = 0.0
+    x[6, 17] = -2.75                # one-hot row
+    x[7] *= 1e-30                   # tiny magnitudes
+    blocks = blocks.copy()
+    blocks[9, :, 0:2] = 0           # d = 0 row
+    out, _ = gpu_w8a8(x, None, blocks, N, path, out_dtype=torch.float32)
+    oq, os_ = oracle.quantize_act(x)
+    y, _ = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    assert np.array_equal(out_bits(out), y.view(np.uint32))
+    assert np.all(out[5].cpu().numpy().view(np.uint32) == 0)
+
+
+def test_w8a8_batch_invariance_and_paths():
+    """Each row alone (M=1, decode kernel) gives the same bits as inside mixed
+    batches on either kernel, at any position, next to zero and outlier rows."""
+    K, N = 512, 272
+    rng = np.random.default_rng(11)
+    xs, bits = synth.activations(77, 300, K, dtype="bf16", outlier_frac=0.01)
+    blocks = synth.q8_0_weights(177, N, K)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    xd = bf16_dev(bits)
+    q, s, _, h = qg.quantize_act(xd, q16=True)
+    probe = rng.choice(300, size=12, replace=False)
+    alone = {}
+    for r in probe:
+        o = qg.gemm_w8a8_q8_0(q[r:r + 1], h[r:r + 1], s[r:r + 1], packed, N, path="small")
+        alone[r] = out_bits(o)[0]
+    for M in (8, 64, 65, 300):
+        for path in ("small", "large"):
+            idx = torch.from_numpy(rng.permutation(300)[:M])
+            for r in probe[:4]:
+                idx[rng.integers(0, M)] = int(r)
+            qi, si, hi = q[idx.to(DEV)], s[idx.to(DEV)], h[idx.to(DEV)]
+            o = out_bits(qg.gemm_w8a8_q8_0(qi, hi, si, packed, N, path=path))
+            for j, r in enumerate(idx.tolist()):
+                if r in alone:
+                    assert np.array_equal(o[j], alone[r]), (M, path, j, r)
+    full_s = out_bits(qg.gemm_w8a8_q8_0(q, h, s, packed, N, path="small"))
+    full_l = out_bits(qg.gemm_w8a8_q8_0(q, h, s, packed, N, path="large"))
+    assert np.array_equal(full_s, full_l)
+
+
+# --------------------------------------------------------------------- W4A8
+def gpu_w4a8(bits, sblocks, N, path, out_dtype=torch.bfloat16):
+    K = bits.shape[1]
+    q, s, bs, h = qg.quantize_act(bf16_dev(bits), block_sums=True, q16=True)
+    packed = qg.pack_q4k(to_dev(sblocks), N, K)
+    out = qg.gemm_w4a8_q4k(q, h, s, bs, packed, N, out_dtype=out_dtype, path=path)
+    torch.cuda.synchronize()
+    qg.check_device_error()
+    return out, (q, h, s, bs, packed)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 256, 16), (5, 512, 40), (64, 1024, 130), (65, 256, 129),
+                                   (200, 768, 300), (300, 2048, 64)])
+@pytest.mark.parametrize("path", ["small", "large"])
+def test_w4a8_matches_oracle(M, K, N, path):
+    x, bits = synth.activations(M + K, M, K, dtype="bf16", outlier_frac=0.01)
+    sblocks = synth.q4k_weights(M + K + 100, N, K)
+    out, _ = gpu_w4a8(bits, sblocks, N, path)
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+    got = out_bits(out)
+    bad = np.argwhere(got != ob)
+    assert bad.size == 0, "first mismatches %s" % bad[:5].tolist()
+    out32, _ = gpu_w4a8(bits, sblocks, N, path, out_dtype=torch.float32)
+    assert np.array_equal(out_bits(out32), y.view(np.uint32))
+
+
+@pytest.mark.parametrize("path", ["small", "large"])
+def test_w4a8_block_sums_exact(path):
+    M, K, N = 33, 512, 40
+    x, bits = synth.activations(9, M, K, dtype="bf16", outlier_frac=0.05)
+    sblocks = synth.q4k_weights(109, N, K)
+    q, s, bs, h = qg.quantize_act(bf16_dev(bits), block_sums=True, q16=True)
+    packed = qg.pack_q4k(to_dev(sblocks), N, K)
+    isum = qg.debug_block_sums("q4k", q, h, packed, N, path).cpu().numpy()
+    oq, _ = oracle.quantize_act(bits)
+    ri, ra = oracle.block_sums_q4k(oq, sblocks)
+    assert np.array_equal(isum, ri)
+    assert np.array_equal(bs.cpu().numpy(), ra)
+
+
+def test_w4a8_batch_invariance():
+    K, N = 512, 96
+    xs, bits = synth.activations(31, 150, K, dtype="bf16", outlier_frac=0.01)
+    sblocks = synth.q4k_weights(131, N, K)
+    full_s, (q, h, s, bs, packed) = gpu_w4a8(bits, sblocks, N, "small")
+    full_l, _ = gpu_w4a8(bits, sblocks, N, "large")
+    assert np.array_equal(out_bits(full_s), out_bits(full_l))
+    for r in (0, 17, 149):
+        o = qg.gemm_w4a8_q4k(q[r:r + 1], h[r:r + 1], s[r:r + 1], bs[r:r + 1], packed, N)
+        assert np.array_equal(out_bits(o)[0], out_bits(full_l)[r])
