@@ -255,6 +255,41 @@ def cpu_baseline(rows_sample=1024):
             "sample": "%d of 2048 rows of both projections (quantize + W8A8 GEMM)" % rows_sample}
 
 
+def run_only(args):
+    """One kernel of the layer on one shape: for profiling and quick timing."""
+    import bit_quantized_gemm_gb300 as qg
+    kind, dims = args.only.split(":")
+    M, K, N = (int(v) for v in dims.split(","))
+    dev = torch.device("cuda", 0)
+    name = "w4a8_q4k" if kind == "w4a8" else "prefill_27b_w8a8"
+    x, bits = synth.activations(7, M, K, dtype="bf16", outlier_frac=0.01)
+    xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    q, s, bs, h = qg.quantize_act(xd, block_sums=True, q16=True)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if kind == "w8a8":
+        packed = qg.pack_q8_0(torch.from_numpy(synth.q8_0_weights(107, N, K)).to(dev), N, K)
+        fn = lambda: qg.gemm_w8a8_q8_0(q, h, s, packed, N, out=out, path=args.path)
+    elif kind == "w4a8":
+        packed = qg.pack_q4k(torch.from_numpy(synth.q4k_weights(107, N, K)).to(dev), N, K)
+        fn = lambda: qg.gemm_w4a8_q4k(q, h, s, bs, packed, N, out=out, path=args.path)
+    elif kind == "quant":
+        fn = lambda: qg.quantize_act(xd, q16=True, out=(q, s, None, h))
+    else:
+        raise SystemExit("unknown kind " + kind)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    for _ in range(args.warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    t = timed_launches(fn, args.steps, flush)
+    qg.check_device_error()
+    ms = statistics.median(t)
+    print(json.dumps({"only": args.only, "path": args.path, "ms_median": round(ms, 5),
+                      "ms_all": [round(v, 5) for v in t],
+                      "tops": round(2.0 * M * N * K / ms / 1e9, 2)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -263,6 +298,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-workload rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", default=None,
+                    help="KIND:M,K,N (KIND w8a8|w4a8|quant): time that one launch alone "
+                         "(--warmup untimed + --steps timed launches, L2 flushed before each); "
+                         "used for profiling")
+    ap.add_argument("--path", default="auto", choices=["auto", "small", "large"])
     args = ap.parse_args()
     rank, world, local = env_rank()
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
@@ -302,6 +342,8 @@ def main():
     if not torch.cuda.is_available():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         sys.exit(1)
+    if args.only:
+        return run_only(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:

@@ -18,10 +18,10 @@ cudaError_t launch_pack_q4k(const void* sblocks, int64_t N, int64_t K, void* pac
                             cudaStream_t st);
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,
                                const void* packed, int64_t N, void* out, bool out_f32,
-                               int64_t ldo, int32_t* dbg, cudaStream_t st);
+                               int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
 cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* asum, int64_t M,
                               int64_t K, const void* packed, int64_t N, void* out, bool out_f32,
-                              int64_t ldo, int32_t* dbg, cudaStream_t st);
+                              int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
@@ -223,7 +223,7 @@ static qg_status gemm_q8_0(const int8_t* q, const uint16_t* q16, const float* sc
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,
                        [&](int64_t m0, int64_t mc, void* o, int32_t* d) {
                          return launch_decode_q8_0(q + m0 * K, scale + m0, mc, K, w, N, o, f32,
-                                                   ldo, d, st);
+                                                   ldo, d, error_word(), st);
                        });
 }
 
@@ -232,7 +232,7 @@ static qg_status gemm_q4k(const int8_t* q, const uint16_t* q16, const float* sca
                           void* out, qg_dtype odt, int64_t ldo, qg_path path, int32_t* dbg,
                           void* stream) {
   if (!bsum) return fail(QG_EINVAL, "block_sums is required for W4A8");
-  if (!aligned(bsum, 4)) return fail(QG_EALIGN, "block_sums needs 4-byte alignment");
+  if (!aligned(bsum, 16)) return fail(QG_EALIGN, "block_sums needs 16-byte alignment");
   bool large = false;
   qg_status s = check_gemm_common(q, q16, scale, M, K, w, N, dbg ? reinterpret_cast<void*>(dbg) : out,
                                   odt, dbg ? N : ldo, path, kQ4kWeights, &large);
@@ -247,7 +247,7 @@ static qg_status gemm_q4k(const int8_t* q, const uint16_t* q16, const float* sca
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,
                        [&](int64_t m0, int64_t mc, void* o, int32_t* d) {
                          return launch_decode_q4k(q + m0 * K, scale + m0, bsum + m0 * B, mc, K, w,
-                                                  N, o, f32, ldo, d, st);
+                                                  N, o, f32, ldo, d, error_word(), st);
                        });
 }
 

@@ -34,29 +34,49 @@
 
 namespace qg {
 
-constexpr int kBN = 128;  // weight rows per tile
-constexpr int kBM = 256;  // tokens per tile
-constexpr int kBK = 64;   // K per stage
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
+#ifndef QG_STAGES
+#define QG_STAGES 4
+#endif
+#ifndef QG_EPI_WARPS
+#define QG_EPI_WARPS 8
+#endif
+constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lanes)
+constexpr int kBK = 64;       // K per stage
+constexpr int kStages = QG_STAGES;
+constexpr int kEpiWarps = QG_EPI_WARPS;  // multiple of 4 (tensor-memory lane quarters)
 constexpr int kLThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
-constexpr uint32_t kStageBBytes = kBM * kBK * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
-constexpr int kColsPerThread = kBM / (kEpiWarps / 4);  // 128
 
+// Tile width BM = tokens per tile (MMA N, tensor-memory columns). 256 suits
+// W8A8 (one FMA per element per block); W4A8's two FMAs per element need
+// the register room of BM = 128.
+template <int BM>
+struct LargeCfg {
+  static_assert(BM % 16 == 0 && BM >= 64 && BM <= 256 && 512 % BM == 0, "tile width");
+  static constexpr int kBM = BM;
+  static constexpr int kTBufs = 512 / BM;  // per-block accumulators filling tensor memory
+  static constexpr uint32_t kStageBBytes = BM * kBK * 2;
+  static constexpr int kColsPerThread = BM / (kEpiWarps / 4);
+};
+
+template <int BM>
 struct LargeSmem {
   uint8_t a[kStages][kStageABytes];
-  uint8_t b[kStages][kStageBBytes];
-  float asum[kAsumRing][kBM];
+  uint8_t b[kStages][LargeCfg<BM>::kStageBBytes];
+  float asum[kAsumRing][BM];
   uint64_t full[kStages], empty[kStages];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[LargeCfg<BM>::kTBufs], tempty[LargeCfg<BM>::kTBufs];
   uint64_t afull[kAsumRing], aempty[kAsumRing];
   uint32_t tmem_base;
 };
-constexpr size_t kLargeSmemBytes = sizeof(LargeSmem) + 1024;  // + alignment slack
-static_assert(kStageABytes % 1024 == 0 && kStageBBytes % 1024 == 0, "1024-B aligned stages");
+template <int BM>
+constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<BM>) + 1024; }  // + alignment slack
+static_assert(kStageABytes % 1024 == 0, "1024-B aligned stages");
+
+template <bool kQ4K>
+__host__ __device__ constexpr int bm_for() { return kQ4K ? 128 : 256; }
 
 struct LargeArgs {
   const float* d32;      // W8A8: [N][ldd] fp32 scales; W4A8: d*sc [N][ldd]
@@ -89,8 +109,14 @@ template <bool kQ4K, bool kDebug>
 __global__ void __launch_bounds__(kLThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const LargeArgs args) {
+  constexpr int BM = bm_for<kQ4K>();
+  using C = LargeCfg<BM>;
+  constexpr int kBM = C::kBM;
+  constexpr int kTBufs = C::kTBufs;
+  constexpr uint32_t kStageBBytes = C::kStageBBytes;
+  constexpr int kColsPerThread = C::kColsPerThread;
   extern __shared__ uint8_t smem_raw[];
-  LargeSmem& S = *reinterpret_cast<LargeSmem*>(
+  LargeSmem<BM>& S = *reinterpret_cast<LargeSmem<BM>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = args.M, N = args.N, K = args.K;
@@ -104,7 +130,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
       mbar_init(&S.tempty[i], kEpiWarps);
     }
@@ -204,7 +230,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
                          idesc, kk);
             }
             mma_commit(&S.tfull[tb]);
-            if (++tb == 2) { tb = 0; tphase ^= 1; }
+            if (++tb == kTBufs) { tb = 0; tphase ^= 1; }
           }
           mma_commit(&S.empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -232,9 +258,24 @@ __global__ void __launch_bounds__(kLThreads, 1)
 #pragma unroll
       for (int i = 0; i < kColsPerThread / 2; ++i) acc[i] = make_float2(0.f, 0.f);
 
+      // scales of four blocks at a time, fetched one group ahead
+      float4 dq = make_float4(0, 0, 0, 0), mq = dq, dq_next = dq, mq_next = dq;
+      if (nvalid) {
+        dq_next = __ldg(reinterpret_cast<const float4*>(drow));
+        if (kQ4K) mq_next = __ldg(reinterpret_cast<const float4*>(mrow));
+      }
       for (int blk = 0; blk < NB && ok; ++blk) {
-        const float dw = nvalid ? __ldg(drow + blk) : 0.0f;
-        const float ndm = (kQ4K && nvalid) ? -__ldg(mrow + blk) : 0.0f;
+        const int j = blk & 3;
+        if (j == 0) {
+          dq = dq_next;
+          mq = mq_next;
+          if (blk + 4 < NB && nvalid) {
+            dq_next = __ldg(reinterpret_cast<const float4*>(drow + blk + 4));
+            if (kQ4K) mq_next = __ldg(reinterpret_cast<const float4*>(mrow + blk + 4));
+          }
+        }
+        const float dw = j == 0 ? dq.x : j == 1 ? dq.y : j == 2 ? dq.z : dq.w;
+        const float ndm = kQ4K ? -(j == 0 ? mq.x : j == 1 ? mq.y : j == 2 ? mq.z : mq.w) : 0.0f;
         ok = mbar_wait(&S.tfull[tb], tphase, args.err);
         if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
         if (!ok) break;
@@ -280,7 +321,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           if (lane == 0) mbar_arrive(&S.aempty[aslot]);
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
-        if (++tb == 2) { tb = 0; tphase ^= 1; }
+        if (++tb == kTBufs) { tb = 0; tphase ^= 1; }
       }
       if (!ok || kDebug) continue;
       // final scale by the activation scale and store out[m][n]
@@ -345,22 +386,32 @@ static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 }
 
 static int num_sms() {
+  static int cached[64] = {};
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 template <bool kQ4K, bool kDebug>
 static cudaError_t launch_prefill_t(const CUtensorMap& ta, const CUtensorMap& tb,
                                    const LargeArgs& a, cudaStream_t st) {
+  constexpr int BM = bm_for<kQ4K>();
+  constexpr size_t kSmem = large_smem_bytes<BM>();
   auto kern = prefill_gemm_kernel<kQ4K, kDebug>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kLargeSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int tiles = (int)(ceil_div(a.M, kBM) * ceil_div(a.N, kBN));
+  static bool configured = false;  // once per process (idempotent if raced)
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kLThreads, kLargeSmemBytes, st>>>(ta, tb, a);
+  kern<<<grid, kLThreads, kSmem, st>>>(ta, tb, a);
   return cudaGetLastError();
 }
 
@@ -371,7 +422,8 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   const Q8Layout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, kBM))
+  constexpr int BM = bm_for<false>();
+  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, BM))
     return cudaErrorNotSupported;
   LargeArgs a{};
   a.d32 = reinterpret_cast<const float*>(base + L.off_d32);
@@ -394,7 +446,8 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   const Q4kLayout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, kBM))
+  constexpr int BM = bm_for<true>();
+  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, BM))
     return cudaErrorNotSupported;
   LargeArgs a{};
   a.d32 = reinterpret_cast<const float*>(base + L.off_ds32);

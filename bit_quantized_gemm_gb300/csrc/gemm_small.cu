@@ -6,226 +6,338 @@
 // are"; "How it works": int8 tensor cores with exact int32 sums).
 //
 // Design. For M <= 64 the layer is bound by reading the weights from HBM
-// (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). Each warp owns one
-// group of 16 weight rows and walks all K blocks in ascending order:
-//   * one 16-byte streaming load per lane per block brings that block's
-//     A-fragment of an m16n8k32 int8 MMA (the packed layout stores the bytes
-//     in register order; Q4_K nibbles are widened with two masks);
-//   * the tokens are the MMA's 8-wide N side (T = ceil(M/8) MMAs per block),
-//     read as 8-byte loads from the row-major int8 activations (L1/L2
-//     resident);
-//   * the MMA accumulates exactly in int32, starting from the bit pattern of
-//     1.5*2^23 so that the result reads back as a float with one FADD;
-//   * per (row, token) the epilogue applies acc = fmaf(isum, d, acc) (Q4_K:
-//     then fmaf(-asum, dmin*m, acc)) in block order, the same chain as the
-//     prefill kernel, so both paths give identical bits.
+// (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). A CTA owns R groups
+// of 16 weight rows and walks all K blocks in ascending order:
+//   * one producer thread streams, per stage of 16 blocks, the row groups'
+//     contiguous fragment-order weights and scales and the activation rows
+//     into a shared-memory ring with 1-D bulk copies (cp.async.bulk +
+//     mbarrier transaction counts), keeping tens of KB in flight per SM
+//     with no registers tied up;
+//   * each consumer warp owns one (row group, 8-token tile) pair: per block
+//     one 16-byte shared load gives the A fragments of two m16n8k16 fp16
+//     MMAs (biased int8 bytes widened to exact fp16 by byte permutes and one
+//     packed subtract; Q4_K nibbles by shift-and-mask), one 8-byte load the
+//     token fragment (int8 rows padded to 544 bytes: conflict-free), and the
+//     two MMAs sum the block exactly in fp32 from zero (|sum| < 2^20). This
+//     GPU runs legacy fp16 MMAs at 4x the rate of legacy int8 MMAs (which
+//     are no faster than dp4a), so int8 values travel as fp16 here;
+//   * acc = fmaf(isum, d, acc) (Q4_K: then fmaf(-asum, dmin*m, acc)) per
+//     block in order with packed f32x2 FMAs -- the same chain as the prefill
+//     kernel, so both paths give identical bits.
 #include "qg_common.cuh"
 
 namespace qg {
 
-constexpr int kSmallWarps = 2;  // warps per CTA (one 16-row group each)
-constexpr int kUnroll = 8;      // blocks of weights in flight per lane
+constexpr int kSBlk = 16;          // K blocks per pipeline stage
+constexpr int kARow = 544;         // bytes per activation row in a stage (512 + 32 pad)
 
-template <int T, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(kSmallWarps * 32) decode_gemm_kernel(
-    const int8_t* __restrict__ qa, const float* __restrict__ sa,
-    const int32_t* __restrict__ asum_g, int M, int K, int N, int64_t G,
-    const uint8_t* __restrict__ wstream, const uint8_t* __restrict__ wscale, void* __restrict__ out,
-    int out_f32, int64_t ldo, int32_t* __restrict__ dbg) {
+__device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int R, int TT, bool kQ4K>
+struct DecodeSmem {
+  static constexpr int kWBytes = R * kSBlk * (kQ4K ? 256 : 512);  // weights per stage
+  static constexpr int kSBytes = R * 512;                          // scales / headers
+  static constexpr int kABytes = TT * 8 * kARow;                   // activation rows
+  static constexpr int kBBytes = kQ4K ? TT * 8 * kSBlk * 4 : 0;    // block sums (W4A8)
+  static constexpr int kStage = kWBytes + kSBytes + kABytes + kBBytes;
+  static constexpr int kNst = (R == 1) ? 6 : 3;
+  static constexpr int kBarOff = kNst * kStage;
+  static constexpr int kTotal = kBarOff + 2 * kNst * 8;
+};
+
+struct DecodeArgs {
+  const int8_t* qa;        // [M][K]
+  const float* sa;         // [M]
+  const int32_t* bsum;     // [M][B] (W4A8)
+  const uint8_t* wstream;  // packed stream section
+  const uint8_t* wscale;   // packed scale / header section
+  void* out;
+  int64_t ldo;
+  int32_t* dbg;
+  uint32_t* err;
+  int M, K, N, G;
+  int out_f32;
+};
+
+template <int R, int TT, bool kQ4K, bool kDebug>
+__global__ void __launch_bounds__(32 * (1 + R * TT), 1) decode_gemm_kernel(const DecodeArgs a) {
+  using L = DecodeSmem<R, TT, kQ4K>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + L::kNst;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t g = (int64_t)blockIdx.x * kSmallWarps + warp;
-  if (g >= G) return;
-  const int r = lane >> 2, c = lane & 3;
-  const int n0 = (int)(16 * g + r), n1 = n0 + 8;
-  const int B = K / kBlk;
-
-  float acc[T][4];
-#pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-
-  const int magic4[4] = {kMagicBits, kMagicBits, kMagicBits, kMagicBits};
-
-  // activation rows of this lane's B fragments: token 8t + r
-  const int8_t* arow[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    const int m = 8 * t + r;
-    arow[t] = (m < M) ? qa + (int64_t)m * K + 8 * c : nullptr;
-  }
-
-  // Q8_0: fragment stream [G][B][32][16]; scales [G][B4/4][8][16 B]
-  // Q4_K: nibble stream [G][B/2][32][16]; headers [G][J][16][16 B]
+  const int B = a.K / kBlk;
   const int B4 = (B + 3) & ~3;
+  const int J = B / 8;
+  const int nstages = (B + kSBlk - 1) / kSBlk;
+  const int g0 = blockIdx.x * R;
+  const int M = a.M;
 
-  for (int b0 = 0; b0 < B; b0 += kUnroll) {
-    int4 wv[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int b = b0 + u;
-      if (!kQ4K) {
-        if (b < B) wv[u] = ldg_stream(wstream + (((int64_t)g * B + b) * 32 + lane) * 16);
-      } else if ((u & 1) == 0) {
-        if (b < B) wv[u] = ldg_stream(wstream + (((int64_t)g * (B / 2) + b / 2) * 32 + lane) * 16);
-      }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], R * TT);
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int b = b0 + u;
-      if (b >= B) break;
-      int a[4];
-      float d0, d1, m0 = 0.f, m1 = 0.f;
-      if (!kQ4K) {
-        a[0] = wv[u].x; a[1] = wv[u].y; a[2] = wv[u].z; a[3] = wv[u].w;
-        // fp16 scales of rows n0, n1 for this block
-        const uint4 sc = __ldg(reinterpret_cast<const uint4*>(
-            wscale + (((int64_t)g * (B4 / 4) + b / 4) * 8 + r) * 16));
-        const uint32_t w0 = (b & 2) ? sc.y : sc.x;  // d[n0][4p..4p+3] in x, y
-        const uint32_t w1 = (b & 2) ? sc.w : sc.z;  // d[n1][4p..4p+3] in z, w
-        d0 = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (w0 >> 16) : (w0 & 0xFFFF))));
-        d1 = __half2float(__ushort_as_half((uint16_t)((b & 1) ? (w1 >> 16) : (w1 & 0xFFFF))));
-      } else {
-        const int4 v = wv[u & ~1];
-        const uint32_t x0 = (u & 1) ? (uint32_t)v.z : (uint32_t)v.x;
-        const uint32_t x1 = (u & 1) ? (uint32_t)v.w : (uint32_t)v.y;
-        a[0] = (int)(x0 & 0x0F0F0F0Fu);
-        a[1] = (int)((x0 >> 4) & 0x0F0F0F0Fu);
-        a[2] = (int)(x1 & 0x0F0F0F0Fu);
-        a[3] = (int)((x1 >> 4) & 0x0F0F0F0Fu);
-        // headers of rows n0, n1 for super-block b/8
-        const int J = B / 8;
-        const uint8_t* h0 = wscale + (((int64_t)g * J + b / 8) * 16 + r) * 16;
-        const uint8_t* h1 = h0 + 8 * 16;
-        const uint4 H0 = __ldg(reinterpret_cast<const uint4*>(h0));
-        const uint4 H1 = __ldg(reinterpret_cast<const uint4*>(h1));
-        const int sub = b & 7;
-        auto field = [](const uint4& H, int f) -> float {
-          // 96-bit string in words y, z, w (bytes 4..15)
-          const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
-          const int pos = 6 * f;
-          uint32_t v;
-          if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
-          else if (pos >= 64) v = H.w >> (pos - 64);
-          else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
-          return (float)(v & 63u);
-        };
-        const float dd0 = __half2float(__ushort_as_half((uint16_t)(H0.x & 0xFFFF)));
-        const float dm0 = __half2float(__ushort_as_half((uint16_t)(H0.x >> 16)));
-        const float dd1 = __half2float(__ushort_as_half((uint16_t)(H1.x & 0xFFFF)));
-        const float dm1 = __half2float(__ushort_as_half((uint16_t)(H1.x >> 16)));
-        d0 = dd0 * field(H0, sub);       // exact products
-        d1 = dd1 * field(H1, sub);
-        m0 = dm0 * field(H0, 8 + sub);
-        m1 = dm1 * field(H1, 8 + sub);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    int st = 0;
+    uint32_t ph = 0;
+    for (int s = 0; s < nstages; ++s) {
+      const int blk0 = s * kSBlk;
+      const int nb = min(kSBlk, B - blk0);
+      uint8_t* base = smem + st * L::kStage;
+      uint32_t bytes = 0;
+      int ngroups = 0;
+      for (int r = 0; r < R; ++r)
+        if (g0 + r < a.G) ++ngroups;
+      if (!kQ4K)
+        bytes = ngroups * (nb * 512 + ((nb + 3) / 4) * 128);
+      else
+        bytes = ngroups * (nb * 256 + (nb / 8) * 256);
+      const int mrows = min(M, TT * 8);
+      bytes += mrows * nb * 32;
+      if (kQ4K) bytes += mrows * nb * 4;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&empty[st], ph ^ 1, a.err);
+        if (ok) mbar_arrive_expect_tx(&full[st], bytes);
       }
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        int2 bb = make_int2(0, 0);
-        if (arow[t]) bb = __ldg(reinterpret_cast<const int2*>(arow[t] + (int64_t)b * kBlk));
-        int d[4];
-        mma_s8_16832(d, a, bb.x, bb.y, magic4);
-        // d[0]: (n0, token 8t+2c), d[1]: (n0, 8t+2c+1), d[2]: (n1, 8t+2c), d[3]: (n1, 8t+2c+1)
-        const int mt0 = 8 * t + 2 * c;
-        if (kDebug) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = mt0 + (i & 1), n = (i < 2) ? n0 : n1;
-            if (m < M && n < N) dbg[((int64_t)m * N + n) * B + b] = d[i] - kMagicBits;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        for (int r = 0; r < ngroups; ++r) {
+          const int64_t g = g0 + r;
+          if (!kQ4K) {
+            bulk_copy(base + r * kSBlk * 512, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
+            bulk_copy(base + L::kWBytes + r * 512,
+                      a.wscale + (g * (B4 / 4) + blk0 / 4) * 128, ((nb + 3) / 4) * 128, &full[st]);
+          } else {
+            bulk_copy(base + r * kSBlk * 256, a.wstream + (g * (B / 2) + blk0 / 2) * 512,
+                      nb * 256, &full[st]);
+            bulk_copy(base + L::kWBytes + r * 512, a.wscale + (g * J + blk0 / 8) * 256,
+                      (nb / 8) * 256, &full[st]);
           }
         }
+      }
+      for (int m = lane; m < mrows; m += 32) {
+        bulk_copy(base + L::kWBytes + L::kSBytes + m * kARow,
+                  a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[st]);
+        if (kQ4K)
+          bulk_copy(base + L::kWBytes + L::kSBytes + L::kABytes + m * (kSBlk * 4),
+                    a.bsum + (int64_t)m * B + blk0, nb * 4, &full[st]);
+      }
+      if (++st == L::kNst) { st = 0; ph ^= 1; }
+    }
+    // drain: every stage released before the CTA exits
+    if (lane == 0) {
+      for (int i = 0; i < L::kNst; ++i) {
+        if (!mbar_wait(&empty[st], ph ^ 1, a.err)) break;
+        if (++st == L::kNst) { st = 0; ph ^= 1; }
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int r = cw / TT, t = cw % TT;
+  const int64_t g = g0 + r;
+  const bool gvalid = g < a.G;
+  const int gr = lane >> 2, c = lane & 3;
+  const int n0 = (int)(16 * g + gr), n1 = n0 + 8;
+  const int mrow = 8 * t + gr;                 // token of this lane's B fragment
+  const int mc0 = 8 * t + 2 * c, mc1 = mc0 + 1;  // tokens of this lane's accumulators
+  const bool tile_live = gvalid && (8 * t < M);
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+
+  float2 acc0 = make_float2(0.f, 0.f);  // row n0: tokens mc0, mc1
+  float2 acc1 = make_float2(0.f, 0.f);  // row n1: tokens mc0, mc1
+
+  int st = 0;
+  uint32_t ph = 0;
+  for (int s = 0; s < nstages; ++s) {
+    const int blk0 = s * kSBlk;
+    const int nb = min(kSBlk, B - blk0);
+    if (!mbar_wait(&full[st], ph, a.err)) break;
+    const uint8_t* base = smem + st * L::kStage;
+    if (tile_live) {
+      const uint8_t* wb = base + r * kSBlk * (kQ4K ? 256 : 512);
+      const uint8_t* sb = base + L::kWBytes + r * 512;
+      const uint8_t* ab = base + L::kWBytes + L::kSBytes + mrow * kARow + c * 8;
+      const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::kWBytes + L::kSBytes + L::kABytes);
+      // blocks in groups of kG (a quad of Q8_0 scales / one Q4_K super-block),
+      // each group fully unrolled so per-group scale arrays stay in registers
+      constexpr int kG = kQ4K ? 8 : 4;
+      for (int j0 = 0; j0 < nb; j0 += kG) {
+        float dA[kG], dB[kG], mA[kG], mB[kG];
         if (!kQ4K) {
-          acc[t][0] = fmaf(magic_to_float(d[0]), d0, acc[t][0]);
-          acc[t][1] = fmaf(magic_to_float(d[1]), d0, acc[t][1]);
-          acc[t][2] = fmaf(magic_to_float(d[2]), d1, acc[t][2]);
-          acc[t][3] = fmaf(magic_to_float(d[3]), d1, acc[t][3]);
+          const uint4 sc = *reinterpret_cast<const uint4*>(sb + (j0 >> 2) * 128 + gr * 16);
+          const __half2* h = reinterpret_cast<const __half2*>(&sc);
+          const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
+          const float2 f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
+          dA[0] = f0.x; dA[1] = f0.y; dA[2] = f1.x; dA[3] = f1.y;
+          dB[0] = f2.x; dB[1] = f2.y; dB[2] = f3.x; dB[3] = f3.y;
         } else {
-          float as0 = 0.f, as1 = 0.f;
-          if (mt0 < M) as0 = (float)__ldg(asum_g + (int64_t)mt0 * B + b);
-          if (mt0 + 1 < M) as1 = (float)__ldg(asum_g + (int64_t)(mt0 + 1) * B + b);
-          acc[t][0] = fmaf(-as0, m0, fmaf(magic_to_float(d[0]), d0, acc[t][0]));
-          acc[t][1] = fmaf(-as1, m0, fmaf(magic_to_float(d[1]), d0, acc[t][1]));
-          acc[t][2] = fmaf(-as0, m1, fmaf(magic_to_float(d[2]), d1, acc[t][2]));
-          acc[t][3] = fmaf(-as1, m1, fmaf(magic_to_float(d[3]), d1, acc[t][3]));
+          const uint4 H0 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + gr * 16);
+          const uint4 H1 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + (gr + 8) * 16);
+          // 6-bit fields: a 96-bit string in words y, z, w (bytes 4..15)
+          auto field = [](const uint4& H, int f) -> float {
+            const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
+            const int pos = 6 * f;
+            uint32_t v;
+            if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
+            else if (pos >= 64) v = H.w >> (pos - 64);
+            else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
+            return (float)(v & 63u);
+          };
+          const float2 dd0 = __half22float2(*reinterpret_cast<const __half2*>(&H0.x));
+          const float2 dd1 = __half22float2(*reinterpret_cast<const __half2*>(&H1.x));
+#pragma unroll
+          for (int u = 0; u < kG; ++u) {
+            dA[u] = dd0.x * field(H0, u);   // exact products
+            dB[u] = dd1.x * field(H1, u);
+            mA[u] = -(dd0.y * field(H0, 8 + u));
+            mB[u] = -(dd1.y * field(H1, 8 + u));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+          const int j = j0 + u;
+          if (j >= nb) break;
+          // A fragments for the block's two 16-wide halves h = 0, 1
+          uint32_t a0[4], a1[4];
+          if (!kQ4K) {
+            const uint4 w = *reinterpret_cast<const uint4*>(wb + j * 512 + lane * 16);
+            // x: row n0 k 8c..+3, y: row n1 k 8c..+3, z: n0 k 8c+4..+7, w: n1 k 8c+4..+7
+            biased_u8x4_to_f16x4(w.x, a0[0], a0[2]);
+            biased_u8x4_to_f16x4(w.y, a0[1], a0[3]);
+            biased_u8x4_to_f16x4(w.z, a1[0], a1[2]);
+            biased_u8x4_to_f16x4(w.w, a1[1], a1[3]);
+          } else {
+            const uint2 w =
+                *reinterpret_cast<const uint2*>(wb + (j >> 1) * 512 + lane * 16 + (j & 1) * 8);
+            a0[0] = nib_pair_to_f16x2<0>(w.x);
+            a0[1] = nib_pair_to_f16x2<4>(w.x);
+            a0[2] = nib_pair_to_f16x2<8>(w.x);
+            a0[3] = nib_pair_to_f16x2<12>(w.x);
+            a1[0] = nib_pair_to_f16x2<0>(w.y);
+            a1[1] = nib_pair_to_f16x2<4>(w.y);
+            a1[2] = nib_pair_to_f16x2<8>(w.y);
+            a1[3] = nib_pair_to_f16x2<12>(w.y);
+          }
+          uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;  // token k 8c+0..1, +2..3, +4..5, +6..7
+          if (mrow < M) {
+            const uint2 bv = *reinterpret_cast<const uint2*>(ab + j * 32);
+            biased_u8x4_to_f16x4(bv.x ^ 0x80808080u, b00, b01);
+            biased_u8x4_to_f16x4(bv.y ^ 0x80808080u, b10, b11);
+          }
+          float d[4];
+          mma_f16_16816(d, a0, b00, b01, zero4);
+          mma_f16_16816(d, a1, b10, b11, d);
+          // d[0]: (n0, mc0), d[1]: (n0, mc1), d[2]: (n1, mc0), d[3]: (n1, mc1), exact
+          if (kDebug) {
+            const int b = blk0 + j;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = (i & 1) ? mc1 : mc0, n = (i < 2) ? n0 : n1;
+              if (m < M && n < a.N) a.dbg[((int64_t)m * a.N + n) * B + b] = __float2int_rn(d[i]);
+            }
+          }
+          acc0 = __ffma2_rn(make_float2(d[0], d[1]), make_float2(dA[u], dA[u]), acc0);
+          acc1 = __ffma2_rn(make_float2(d[2], d[3]), make_float2(dB[u], dB[u]), acc1);
+          if (kQ4K) {
+            const float as0 = (mc0 < M) ? (float)bb[mc0 * kSBlk + j] : 0.f;
+            const float as1 = (mc1 < M) ? (float)bb[mc1 * kSBlk + j] : 0.f;
+            const float2 as = make_float2(as0, as1);
+            acc0 = __ffma2_rn(as, make_float2(mA[u], mA[u]), acc0);
+            acc1 = __ffma2_rn(as, make_float2(mB[u], mB[u]), acc1);
+          }
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (++st == L::kNst) { st = 0; ph ^= 1; }
   }
 
-  if (kDebug) return;
+  if (kDebug || !tile_live) return;
+  const float accs[4] = {acc0.x, acc0.y, acc1.x, acc1.y};
 #pragma unroll
-  for (int t = 0; t < T; ++t) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int m = 8 * t + 2 * c + (i & 1), n = (i < 2) ? n0 : n1;
-      if (m < M && n < N) {
-        const float y = acc[t][i] * __ldg(sa + m);
-        if (out_f32)
-          reinterpret_cast<float*>(out)[(int64_t)m * ldo + n] = y;
-        else
-          reinterpret_cast<uint16_t*>(out)[(int64_t)m * ldo + n] = f32_to_bf16_rne(y);
-      }
+  for (int i = 0; i < 4; ++i) {
+    const int m = (i & 1) ? mc1 : mc0, n = (i < 2) ? n0 : n1;
+    if (m < M && n < a.N) {
+      const float y = accs[i] * __ldg(a.sa + m);
+      if (a.out_f32)
+        reinterpret_cast<float*>(a.out)[(int64_t)m * a.ldo + n] = y;
+      else
+        reinterpret_cast<uint16_t*>(a.out)[(int64_t)m * a.ldo + n] = f32_to_bf16_rne(y);
     }
   }
 }
 
-template <bool kQ4K, bool kDebug>
-static cudaError_t launch_decode_t(int T, const int8_t* qa, const float* sa, const int32_t* asum,
-                                   int M, int K, int N, int64_t G, const uint8_t* ws,
-                                   const uint8_t* wsc, void* out, int out_f32, int64_t ldo,
-                                   int32_t* dbg, cudaStream_t st) {
-  dim3 grid((unsigned)ceil_div(G, kSmallWarps)), block(kSmallWarps * 32);
-#define QG_DECODE_CASE(TT)                                                                  \
-  case TT:                                                                                  \
-    decode_gemm_kernel<TT, kQ4K, kDebug><<<grid, block, 0, st>>>(qa, sa, asum, M, K, N, G, \
-                                                                 ws, wsc, out, out_f32, ldo, \
-                                                                 dbg);                      \
-    break;
-  switch (T) {
-    QG_DECODE_CASE(1)
-    QG_DECODE_CASE(2)
-    QG_DECODE_CASE(4)
-    QG_DECODE_CASE(8)
-    default:
-      return cudaErrorInvalidValue;
+template <int R, int TT, bool kQ4K, bool kDebug>
+static cudaError_t launch_decode_cfg(const DecodeArgs& a, cudaStream_t st) {
+  using L = DecodeSmem<R, TT, kQ4K>;
+  auto kern = decode_gemm_kernel<R, TT, kQ4K, kDebug>;
+  static bool configured = false;  // once per process (idempotent if raced)
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
-#undef QG_DECODE_CASE
+  dim3 grid((unsigned)ceil_div(a.G, R)), block(32 * (1 + R * TT));
+  kern<<<grid, block, L::kTotal, st>>>(a);
   return cudaGetLastError();
 }
 
-static int token_tiles(int M) {
-  const int t = (M + 7) / 8;
-  return t <= 1 ? 1 : t <= 2 ? 2 : t <= 4 ? 4 : 8;
+template <bool kQ4K, bool kDebug>
+static cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
+  if (a.M <= 8) return launch_decode_cfg<1, 1, kQ4K, kDebug>(a, st);
+  if (a.M <= 16) return launch_decode_cfg<1, 2, kQ4K, kDebug>(a, st);
+  if (a.M <= 32) return launch_decode_cfg<2, 4, kQ4K, kDebug>(a, st);
+  return launch_decode_cfg<2, 8, kQ4K, kDebug>(a, st);
 }
 
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,
                                const void* packed, int64_t N, void* out, bool out_f32,
-                               int64_t ldo, int32_t* dbg, cudaStream_t st) {
-  const Q8Layout L(N, K);
+                               int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+  const Q8Layout Lq(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
-  const int T = token_tiles((int)M);
-  if (dbg)
-    return launch_decode_t<false, true>(T, qa, sa, nullptr, (int)M, (int)K, (int)N, L.G,
-                                        base + L.off_stream, base + L.off_dsc, out, out_f32, ldo,
-                                        dbg, st);
-  return launch_decode_t<false, false>(T, qa, sa, nullptr, (int)M, (int)K, (int)N, L.G,
-                                       base + L.off_stream, base + L.off_dsc, out, out_f32, ldo,
-                                       nullptr, st);
+  DecodeArgs a{};
+  a.qa = qa; a.sa = sa; a.bsum = nullptr;
+  a.wstream = base + Lq.off_stream;
+  a.wscale = base + Lq.off_dsc;
+  a.out = out; a.ldo = ldo; a.dbg = dbg; a.err = err;
+  a.M = (int)M; a.K = (int)K; a.N = (int)N; a.G = (int)Lq.G;
+  a.out_f32 = out_f32 ? 1 : 0;
+  return dbg ? launch_decode_m<false, true>(a, st) : launch_decode_m<false, false>(a, st);
 }
 
 cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* asum, int64_t M,
                               int64_t K, const void* packed, int64_t N, void* out, bool out_f32,
-                              int64_t ldo, int32_t* dbg, cudaStream_t st) {
-  const Q4kLayout L(N, K);
+                              int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+  const Q4kLayout Lq(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
-  const int T = token_tiles((int)M);
-  if (dbg)
-    return launch_decode_t<true, true>(T, qa, sa, asum, (int)M, (int)K, (int)N, L.G,
-                                       base + L.off_stream, base + L.off_shdr, out, out_f32, ldo,
-                                       dbg, st);
-  return launch_decode_t<true, false>(T, qa, sa, asum, (int)M, (int)K, (int)N, L.G,
-                                      base + L.off_stream, base + L.off_shdr, out, out_f32, ldo,
-                                      nullptr, st);
+  DecodeArgs a{};
+  a.qa = qa; a.sa = sa; a.bsum = asum;
+  a.wstream = base + Lq.off_stream;
+  a.wscale = base + Lq.off_shdr;
+  a.out = out; a.ldo = ldo; a.dbg = dbg; a.err = err;
+  a.M = (int)M; a.K = (int)K; a.N = (int)N; a.G = (int)Lq.G;
+  a.out_f32 = out_f32 ? 1 : 0;
+  return dbg ? launch_decode_m<true, true>(a, st) : launch_decode_m<true, false>(a, st);
 }
 
 }  // namespace qg

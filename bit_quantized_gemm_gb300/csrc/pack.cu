@@ -20,7 +20,10 @@ __device__ __forceinline__ uint16_t q8_dbits(const uint8_t* blocks, int64_t B, i
   return (uint16_t)(p[0] | (p[1] << 8));
 }
 
-// one thread per (group g, block b, lane t): the 16 A-fragment bytes
+// one thread per (group g, block b, lane t): the 16 A-fragment bytes of the
+// decode kernel's two fp16 MMAs for this block, stored biased (q + 128 as an
+// unsigned byte) so that two byte permutes and one packed subtract turn four
+// of them into exact fp16 values
 __global__ void pack_q8_0_stream(const uint8_t* __restrict__ blocks, int64_t N, int64_t B,
                                  int64_t G, uint8_t* __restrict__ out) {
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -31,10 +34,10 @@ __global__ void pack_q8_0_stream(const uint8_t* __restrict__ blocks, int64_t N, 
   const int64_t n0 = 16 * g + r, n1 = n0 + 8, k0 = 32 * b + 8 * c;
   uint8_t v[16];
   for (int j = 0; j < 4; ++j) {
-    v[j] = (uint8_t)q8_val(blocks, B, N, n0, k0 + j);
-    v[4 + j] = (uint8_t)q8_val(blocks, B, N, n1, k0 + j);
-    v[8 + j] = (uint8_t)q8_val(blocks, B, N, n0, k0 + 4 + j);
-    v[12 + j] = (uint8_t)q8_val(blocks, B, N, n1, k0 + 4 + j);
+    v[j] = (uint8_t)(q8_val(blocks, B, N, n0, k0 + j) + 128);
+    v[4 + j] = (uint8_t)(q8_val(blocks, B, N, n1, k0 + j) + 128);
+    v[8 + j] = (uint8_t)(q8_val(blocks, B, N, n0, k0 + 4 + j) + 128);
+    v[12 + j] = (uint8_t)(q8_val(blocks, B, N, n1, k0 + 4 + j) + 128);
   }
   uint4 w;
   w.x = v[0] | (v[1] << 8) | (v[2] << 16) | ((uint32_t)v[3] << 24);
@@ -90,7 +93,11 @@ __device__ __forceinline__ int q4_field(const uint8_t* p, int f) {
   return (int)((v >> sh) & 63u);
 }
 
-// one thread per (group g, block b, lane t): 8 nibble-pair bytes
+// one thread per (group g, block b, lane t): two words of nibbles, one per
+// 16-wide half h of the block's 32 k (k = 32b + 8c + 4h + j, j = 0..3): rows
+// r and r+8 interleaved so that shift-and-mask yields fp16 pairs directly:
+//   bits 0-3 q[r][j0], 16-19 q[r][j1], 4-7 q[r+8][j0], 20-23 q[r+8][j1],
+//   8-11 q[r][j2], 24-27 q[r][j3], 12-15 q[r+8][j2], 28-31 q[r+8][j3]
 __global__ void pack_q4k_stream(const uint8_t* __restrict__ sb, int64_t N, int64_t J,
                                 int64_t B, int64_t G, uint8_t* __restrict__ out) {
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -98,16 +105,21 @@ __global__ void pack_q4k_stream(const uint8_t* __restrict__ sb, int64_t N, int64
   const int t = (int)(i % 32);
   const int64_t b = (i / 32) % B, g = i / 32 / B;
   const int r = t / 4, c = t % 4;
-  const int64_t n0 = 16 * g + r, n1 = n0 + 8, k0 = 32 * b + 8 * c;
-  uint32_t w0 = 0, w1 = 0;
-  for (int j = 0; j < 4; ++j) {
-    w0 |= (uint32_t)(q4_nib(sb, J, N, n0, k0 + j) | (q4_nib(sb, J, N, n1, k0 + j) << 4)) << (8 * j);
-    w1 |= (uint32_t)(q4_nib(sb, J, N, n0, k0 + 4 + j) | (q4_nib(sb, J, N, n1, k0 + 4 + j) << 4))
-          << (8 * j);
+  const int64_t n0 = 16 * g + r, n1 = n0 + 8;
+  uint32_t w[2];
+  for (int h = 0; h < 2; ++h) {
+    const int64_t k = 32 * b + 8 * c + 4 * h;
+    uint32_t a[4], e[4];
+    for (int j = 0; j < 4; ++j) {
+      a[j] = (uint32_t)q4_nib(sb, J, N, n0, k + j);
+      e[j] = (uint32_t)q4_nib(sb, J, N, n1, k + j);
+    }
+    w[h] = a[0] | (a[1] << 16) | (e[0] << 4) | (e[1] << 20) | (a[2] << 8) | (a[3] << 24) |
+           (e[2] << 12) | (e[3] << 28);
   }
   // [g][b/2][lane][16 B]: block 2p in bytes 0-7, block 2p+1 in bytes 8-15
   const int64_t off = (((g * (B / 2) + b / 2) * 32 + t) * 16) + (b & 1) * 8;
-  *reinterpret_cast<uint2*>(out + off) = make_uint2(w0, w1);
+  *reinterpret_cast<uint2*>(out + off) = make_uint2(w[0], w[1]);
 }
 
 // one thread per (group g, super-block j, row r in 0..15): the 16-byte header

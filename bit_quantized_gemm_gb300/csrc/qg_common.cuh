@@ -35,12 +35,12 @@ __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a
 // Packed weight layout (opaque to callers; sized by qg_*_packed_bytes).
 //
 // Q8_0, for N rows, K columns, B = K/32 blocks, G = ceil(N/16) row groups:
-//  stream  G*B*512 B   int8 weights in the decode kernel's fragment order:
-//                       for group g, block b, lane t (r = t/4, c = t%4) the
-//                       16 bytes are q[16g+r][32b+8c .. +3],
-//                       q[16g+r+8][32b+8c .. +3], q[16g+r][32b+8c+4 .. +7],
-//                       q[16g+r+8][32b+8c+4 .. +7] -- exactly the A-operand
-//                       registers of one m16n8k32 int8 MMA (K permuted the
+//  stream  G*B*512 B   weights in the decode kernel's fragment order, as
+//                       biased bytes q+128: for group g, block b, lane t
+//                       (r = t/4, c = t%4) the 16 bytes are q[16g+r][32b+8c
+//                       .. +3], q[16g+r+8][32b+8c .. +3], q[16g+r][32b+8c+4
+//                       .. +7], q[16g+r+8][32b+8c+4 .. +7] -- the A operands
+//                       of the block's two m16n8k16 fp16 MMAs (K permuted the
 //                       same way on both operands; integer sums do not
 //                       depend on the order).
 //  dsc     G*(B4/4)*128 B  fp16 scales for the decode kernel: for group g,
@@ -52,9 +52,8 @@ __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a
 // Q4_K, with J = K/256 super-blocks per row:
 //  stream  G*B*256 B   nibbles in fragment order: for group g, block pair p,
 //                       lane t: 8 bytes for block 2p then 8 for block 2p+1;
-//                       for one block the 8 bytes are words w0, w1 with
-//                       byte j of w0 = q[16g+r][32b+8c+j] | q[16g+r+8][..] << 4
-//                       and w1 the same for k = 32b+8c+4+j.
+//                       for one block two words, one per 16-wide half
+//                       (bit layout in pack.cu: fp16 pairs by shift-and-mask).
 //  shdr    G*J*256 B   the first 16 bytes (d, dmin, 6-bit fields) of each
 //                       super-block, [G][J][16 rows][16 B].
 //  q16     N*K*2 B     q (0..15) as fp16, row-major [N][K].
@@ -136,8 +135,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false (and records a timeout) after `limit` polls.
-// Each try_wait suspends the thread for a hardware-defined time slice, so the
-// default limit is on the order of seconds, far above any legitimate wait.
+// Each try_wait may suspend the thread for a short hardware-defined time
+// while the phase is incomplete, so the default limit amounts to seconds,
+// far above any legitimate wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           uint32_t limit = (1u << 24)) {
   for (uint32_t i = 0; i < limit; ++i) {
@@ -234,6 +234,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// The same wait, with the destination registers of the outstanding loads as
+// operands, so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+        "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+        "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]),
+        "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]),
+        "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+      :
+      : "memory");
+}
+
+// Warp-group register reallocation (all 128 threads of a warp group execute it).
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -257,6 +280,40 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
          | (0u << 7) | (0u << 10)        // A, B format: f16
          | ((uint32_t)(n >> 3) << 17)    // N >> 3
          | ((uint32_t)(m >> 4) << 24);   // M >> 4
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level fp16 MMA, fp32 accumulate: m16n8k16 (d = a*b + c). On integer-
+// valued operands with |sum| < 2^24 the fp32 accumulation is exact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
+
+// Four biased bytes (q + 128) -> two fp16 pairs holding q exactly:
+// the bytes become the low mantissa bits of 1024 + (q + 128), then 1152 is
+// subtracted (all values are integers below 2048, exact in fp16).
+__device__ __forceinline__ void biased_u8x4_to_f16x4(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// Two 4-bit values at bits [s, s+4) and [s+16, s+20) -> an fp16 pair.
+template <int kShift>
+__device__ __forceinline__ uint32_t nib_pair_to_f16x2(uint32_t w) {
+  uint32_t a = ((w >> kShift) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x64006400u));
+  return r;
 }
 
 // ---------------------------------------------------------------------------

@@ -148,7 +148,8 @@ size_t qg_q4k_packed_bytes(int64_t N, int64_t K);
 qg_status qg_pack_q4k(const void* superblocks, int64_t N, int64_t K, void* packed, void* stream);
 
 /* out[m][n] = the W4A8 result above.
- *   block_sums  [M][K/32] int32 from qg_quantize_act (required).
+ *   block_sums  [M][K/32] int32 from qg_quantize_act (required, 16-byte
+ *               aligned).
  *   Other arguments as for qg_gemm_w8a8_q8_0. */
 qg_status qg_gemm_w4a8_q4k(const int8_t* q, const uint16_t* q16, const float* scale,
                            const int32_t* block_sums, int64_t M, int64_t K,

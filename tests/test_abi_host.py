@@ -77,7 +77,7 @@ def test_q4k_and_quantize_validation(L):
     g = L.qg_gemm_w4a8_q4k_ex
     assert g(P(FAKE), P(FAKE), P(FAKE), None, 4, 256, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EINVAL
     assert g(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 4, 288, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EINVAL
-    assert g(P(FAKE), P(FAKE), P(FAKE), P(FAKE + 2), 4, 256, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EALIGN
+    assert g(P(FAKE), P(FAKE), P(FAKE), P(FAKE + 8), 4, 256, P(FAKE), 16, P(FAKE), 0, 16, 0, None) == _lib.QG_EALIGN
     qa = L.qg_quantize_act
     assert qa(None, 0, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
     assert qa(P(FAKE), 0, 4, 40, 40, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
