@@ -40,8 +40,8 @@ static __device__ uint32_t g_error_word_dev;
 namespace {
 
 constexpr int kVersion = 10000;        // 1.0.0
-constexpr int64_t kSmallMMax = 64;     // AUTO: decode kernel for M <= 64
-constexpr int64_t kDecodeRows = 64;    // rows per decode launch
+constexpr int64_t kSmallMMax = 16;     // AUTO: decode kernel for M <= 16
+constexpr int64_t kDecodeRows = 16;    // rows per decode launch
 constexpr int64_t kMaxN = int64_t(1) << 24;
 constexpr int64_t kMaxM = int64_t(1) << 24;
 
@@ -113,7 +113,7 @@ qg_status check_gemm_common(const int8_t* q, const uint16_t* q16, const float* s
 template <typename F>
 qg_status decode_chunks(int64_t M, int64_t K, int64_t N, int64_t ldo, size_t out_esize,
                         void* out, int32_t* dbg, F&& launch) {
-  // the decode kernel takes up to 64 rows per launch; rows are independent
+  // the decode kernel takes up to 16 rows per launch; rows are independent
   for (int64_t m0 = 0; m0 < M; m0 += kDecodeRows) {
     const int64_t mc = (M - m0) < kDecodeRows ? (M - m0) : kDecodeRows;
     void* o = out ? reinterpret_cast<char*>(out) + m0 * ldo * out_esize : nullptr;

@@ -5,31 +5,42 @@
 // StartLux-Prism": "Reproducible to the bit" and "The released files as they
 // are"; "How it works": int8 tensor cores with exact int32 sums).
 //
-// Design. For M <= 64 the layer is bound by reading the weights from HBM
-// (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). A CTA owns R groups
-// of 16 weight rows and walks all K blocks in ascending order:
-//   * one producer thread streams, per stage of 16 blocks, the row groups'
-//     contiguous fragment-order weights and scales and the activation rows
-//     into a shared-memory ring with 1-D bulk copies (cp.async.bulk +
-//     mbarrier transaction counts), keeping tens of KB in flight per SM
-//     with no registers tied up;
-//   * each consumer warp owns one (row group, 8-token tile) pair: per block
-//     one 16-byte shared load gives the A fragments of two m16n8k16 fp16
-//     MMAs (biased int8 bytes widened to exact fp16 by byte permutes and one
-//     packed subtract; Q4_K nibbles by shift-and-mask), one 8-byte load the
-//     token fragment (int8 rows padded to 544 bytes: conflict-free), and the
-//     two MMAs sum the block exactly in fp32 from zero (|sum| < 2^20). This
-//     GPU runs legacy fp16 MMAs at 4x the rate of legacy int8 MMAs (which
-//     are no faster than dp4a), so int8 values travel as fp16 here;
-//   * acc = fmaf(isum, d, acc) (Q4_K: then fmaf(-asum, dmin*m, acc)) per
-//     block in order with packed f32x2 FMAs -- the same chain as the prefill
-//     kernel, so both paths give identical bits.
+// Design. For M <= 16 the layer is bound by reading the weights from HBM
+// (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). A CTA owns one group
+// of 16 weight rows and all of K; K is cut into stages of 16 blocks.
+//   * warp 0 (one thread) streams each stage -- the group's contiguous
+//     fragment-order weights and scales, the activation rows (and for W4A8
+//     their block sums) -- into a shared-memory ring with 1-D bulk copies
+//     (cp.async.bulk + mbarrier transaction counts);
+//   * warps 1..8 split the stage's blocks (two each): per block one 16-byte
+//     shared load gives the A fragments of two m16n8k16 fp16 MMAs (biased
+//     int8 bytes widened to exact fp16 by byte permutes and one packed
+//     subtract; Q4_K nibbles by shift-and-mask), one 8-byte load per 8-token
+//     tile the token fragment (int8 rows padded to 544 bytes:
+//     conflict-free), and the two MMAs sum the block exactly in fp32 from
+//     zero (|sum| < 2^20). The exact block sums go to a shared stash. (This
+//     GPU runs legacy fp16 MMAs at 4x the rate of legacy int8 MMAs, which
+//     are no faster than dp4a, so int8 values travel as fp16 here);
+//   * warp 9 applies acc = fmaf(isum, d, acc) (Q4_K: then
+//     fmaf(-asum, dmin*m, acc)) over the stage's blocks in ascending order
+//     with packed f32x2 FMAs -- the same chain as the prefill kernel, so both
+//     paths give identical bits -- and hands the stage back to the producer.
+// K-parallel compute with a sequential fp32 chain keeps ten warps busy per
+// 16-row group, which small N (few groups) needs to reach HBM rate.
 #include "qg_common.cuh"
 
 namespace qg {
 
-constexpr int kSBlk = 16;          // K blocks per pipeline stage
-constexpr int kARow = 544;         // bytes per activation row in a stage (512 + 32 pad)
+constexpr int kCompWarps = 8;      // compute warps per CTA
+
+// K blocks per pipeline stage: 16 for Q8_0 (8 KB of weights per 16-row
+// group), 32 for Q4_K (the same bytes; per-stage overhead halves).
+template <bool kQ4K>
+__host__ __device__ constexpr int sblk() { return kQ4K ? 32 : 16; }
+// bytes per activation row in a stage: 32 per block + 32 of padding, so the
+// eight rows one 8-byte load touches fall in distinct banks
+template <bool kQ4K>
+__host__ __device__ constexpr int arow() { return sblk<kQ4K>() * 32 + 32; }
 
 __device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -40,16 +51,33 @@ __device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
-template <int R, int TT, bool kQ4K>
+// Shared-memory layout (offsets depend on M, fixed at launch):
+//   NW weight stages, each: weights | scales | M activation rows | (W4A8) M
+//   block-sum rows -- released by the chain warp;
+//   2 stash slots of exact block sums between compute and chain warps;
+//   barriers full[NW], empty[NW], xfull[2], xempty[2].
+template <int TT, bool kQ4K>
 struct DecodeSmem {
-  static constexpr int kWBytes = R * kSBlk * (kQ4K ? 256 : 512);  // weights per stage
-  static constexpr int kSBytes = R * 512;                          // scales / headers
-  static constexpr int kABytes = TT * 8 * kARow;                   // activation rows
-  static constexpr int kBBytes = kQ4K ? TT * 8 * kSBlk * 4 : 0;    // block sums (W4A8)
-  static constexpr int kStage = kWBytes + kSBytes + kABytes + kBBytes;
-  static constexpr int kNst = (R == 1) ? 6 : 3;
-  static constexpr int kBarOff = kNst * kStage;
-  static constexpr int kTotal = kBarOff + 2 * kNst * 8;
+  static constexpr int kSBlk = sblk<kQ4K>();
+  static constexpr int kARow = arow<kQ4K>();
+  static constexpr int kWBytes = kSBlk * (kQ4K ? 256 : 512);  // weights per stage
+  static constexpr int kSBytes = kQ4K ? kSBlk / 8 * 256 : kSBlk / 4 * 128;  // scales / headers
+  static constexpr int kXBytes = kSBlk * TT * 32 * 16;          // stash slot
+  static constexpr int kMaxNw = 8;
+  static __host__ __device__ int stage_bytes(int mrows) {
+    return (int)align_up(kWBytes + kSBytes + mrows * kARow + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
+  }
+  static __host__ __device__ int act_off() { return kWBytes + kSBytes; }
+  static __host__ __device__ int bsum_off(int mrows) { return kWBytes + kSBytes + mrows * kARow; }
+  // weight stages that fit in `budget` bytes next to the stash and barriers
+  static int num_stages(int mrows, int budget) {
+    const int fixed = 2 * kXBytes + 2 * (kMaxNw + 2) * 8;
+    int nw = (budget - fixed) / stage_bytes(mrows);
+    return nw < 2 ? 2 : (nw > kMaxNw ? kMaxNw : nw);
+  }
+  static __host__ __device__ int total(int mrows, int nw) {
+    return nw * stage_bytes(mrows) + 2 * kXBytes + 2 * (nw + 2) * 8;
+  }
 };
 
 struct DecodeArgs {
@@ -64,26 +92,41 @@ struct DecodeArgs {
   uint32_t* err;
   int M, K, N, G;
   int out_f32;
+  int nw;           // weight stages in the ring
 };
 
-template <int R, int TT, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(32 * (1 + R * TT), 1) decode_gemm_kernel(const DecodeArgs a) {
-  using L = DecodeSmem<R, TT, kQ4K>;
+template <int TT, bool kQ4K, bool kDebug>
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(const DecodeArgs a) {
+  using L = DecodeSmem<TT, kQ4K>;
+  constexpr int kSBlk = L::kSBlk;
+  constexpr int kARow = L::kARow;
+  constexpr int kBlkPerWarp = kSBlk / kCompWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + L::kNst;
+  const int NW = a.nw;
+  const int mrows = min(a.M, TT * 8);
+  const int SBY = L::stage_bytes(mrows);
+  float* stash_base = reinterpret_cast<float*>(smem + NW * SBY);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kXBytes);
+  uint64_t* empty = full + NW;    // weight stage consumed by the chain warp
+  uint64_t* xfull = empty + NW;   // stash slot written (count: compute warps)
+  uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.K / kBlk;
   const int B4 = (B + 3) & ~3;
   const int J = B / 8;
   const int nstages = (B + kSBlk - 1) / kSBlk;
-  const int g0 = blockIdx.x * R;
+  const int64_t g = blockIdx.x;
   const int M = a.M;
+  const int gr = lane >> 2, c = lane & 3;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::kNst; ++i) {
+    for (int i = 0; i < NW; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], R * TT);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xfull[i], kCompWarps);
+      mbar_init(&xempty[i], 1);
     }
     fence_barrier_init();
   }
@@ -96,218 +139,242 @@ __global__ void __launch_bounds__(32 * (1 + R * TT), 1) decode_gemm_kernel(const
     for (int s = 0; s < nstages; ++s) {
       const int blk0 = s * kSBlk;
       const int nb = min(kSBlk, B - blk0);
-      uint8_t* base = smem + st * L::kStage;
-      uint32_t bytes = 0;
-      int ngroups = 0;
-      for (int r = 0; r < R; ++r)
-        if (g0 + r < a.G) ++ngroups;
-      if (!kQ4K)
-        bytes = ngroups * (nb * 512 + ((nb + 3) / 4) * 128);
-      else
-        bytes = ngroups * (nb * 256 + (nb / 8) * 256);
-      const int mrows = min(M, TT * 8);
+      uint8_t* base = smem + st * SBY;
+      uint32_t bytes = !kQ4K ? nb * 512 + ((nb + 3) / 4) * 128 : nb * 256 + (nb / 8) * 256;
       bytes += mrows * nb * 32;
       if (kQ4K) bytes += mrows * nb * 4;
       bool ok = true;
       if (lane == 0) {
         ok = mbar_wait(&empty[st], ph ^ 1, a.err);
-        if (ok) mbar_arrive_expect_tx(&full[st], bytes);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
-        for (int r = 0; r < ngroups; ++r) {
-          const int64_t g = g0 + r;
+        if (ok) {
+          mbar_arrive_expect_tx(&full[st], bytes);
           if (!kQ4K) {
-            bulk_copy(base + r * kSBlk * 512, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
-            bulk_copy(base + L::kWBytes + r * 512,
-                      a.wscale + (g * (B4 / 4) + blk0 / 4) * 128, ((nb + 3) / 4) * 128, &full[st]);
+            bulk_copy(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
+            bulk_copy(base + L::kWBytes, a.wscale + (g * (B4 / 4) + blk0 / 4) * 128,
+                      ((nb + 3) / 4) * 128, &full[st]);
           } else {
-            bulk_copy(base + r * kSBlk * 256, a.wstream + (g * (B / 2) + blk0 / 2) * 512,
-                      nb * 256, &full[st]);
-            bulk_copy(base + L::kWBytes + r * 512, a.wscale + (g * J + blk0 / 8) * 256,
-                      (nb / 8) * 256, &full[st]);
+            bulk_copy(base, a.wstream + (g * (B / 2) + blk0 / 2) * 512, nb * 256, &full[st]);
+            bulk_copy(base + L::kWBytes, a.wscale + (g * J + blk0 / 8) * 256, (nb / 8) * 256,
+                      &full[st]);
           }
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       for (int m = lane; m < mrows; m += 32) {
-        bulk_copy(base + L::kWBytes + L::kSBytes + m * kARow,
+        bulk_copy(base + L::act_off() + m * kARow,
                   a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[st]);
         if (kQ4K)
-          bulk_copy(base + L::kWBytes + L::kSBytes + L::kABytes + m * (kSBlk * 4),
-                    a.bsum + (int64_t)m * B + blk0, nb * 4, &full[st]);
+          bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
+                    nb * 4, &full[st]);
       }
-      if (++st == L::kNst) { st = 0; ph ^= 1; }
+      if (++st == NW) { st = 0; ph ^= 1; }
     }
     // drain: every stage released before the CTA exits
     if (lane == 0) {
-      for (int i = 0; i < L::kNst; ++i) {
+      for (int i = 0; i < NW; ++i) {
         if (!mbar_wait(&empty[st], ph ^ 1, a.err)) break;
-        if (++st == L::kNst) { st = 0; ph ^= 1; }
+        if (++st == NW) { st = 0; ph ^= 1; }
       }
     }
     return;
   }
 
-  // --------------------------------------------------------------- consumers
-  const int cw = warp - 1;
-  const int r = cw / TT, t = cw % TT;
-  const int64_t g = g0 + r;
-  const bool gvalid = g < a.G;
-  const int gr = lane >> 2, c = lane & 3;
-  const int n0 = (int)(16 * g + gr), n1 = n0 + 8;
-  const int mrow = 8 * t + gr;                 // token of this lane's B fragment
-  const int mc0 = 8 * t + 2 * c, mc1 = mc0 + 1;  // tokens of this lane's accumulators
-  const bool tile_live = gvalid && (8 * t < M);
-  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-
-  float2 acc0 = make_float2(0.f, 0.f);  // row n0: tokens mc0, mc1
-  float2 acc1 = make_float2(0.f, 0.f);  // row n1: tokens mc0, mc1
-
-  int st = 0;
-  uint32_t ph = 0;
-  for (int s = 0; s < nstages; ++s) {
-    const int blk0 = s * kSBlk;
-    const int nb = min(kSBlk, B - blk0);
-    if (!mbar_wait(&full[st], ph, a.err)) break;
-    const uint8_t* base = smem + st * L::kStage;
-    if (tile_live) {
-      const uint8_t* wb = base + r * kSBlk * (kQ4K ? 256 : 512);
-      const uint8_t* sb = base + L::kWBytes + r * 512;
-      const uint8_t* ab = base + L::kWBytes + L::kSBytes + mrow * kARow + c * 8;
-      const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::kWBytes + L::kSBytes + L::kABytes);
-      // blocks in groups of kG (a quad of Q8_0 scales / one Q4_K super-block),
-      // each group fully unrolled so per-group scale arrays stay in registers
-      constexpr int kG = kQ4K ? 8 : 4;
-      for (int j0 = 0; j0 < nb; j0 += kG) {
-        float dA[kG], dB[kG], mA[kG], mB[kG];
-        if (!kQ4K) {
-          const uint4 sc = *reinterpret_cast<const uint4*>(sb + (j0 >> 2) * 128 + gr * 16);
-          const __half2* h = reinterpret_cast<const __half2*>(&sc);
-          const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
-          const float2 f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
-          dA[0] = f0.x; dA[1] = f0.y; dA[2] = f1.x; dA[3] = f1.y;
-          dB[0] = f2.x; dB[1] = f2.y; dB[2] = f3.x; dB[3] = f3.y;
-        } else {
-          const uint4 H0 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + gr * 16);
-          const uint4 H1 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + (gr + 8) * 16);
-          // 6-bit fields: a 96-bit string in words y, z, w (bytes 4..15)
-          auto field = [](const uint4& H, int f) -> float {
-            const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
-            const int pos = 6 * f;
-            uint32_t v;
-            if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
-            else if (pos >= 64) v = H.w >> (pos - 64);
-            else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
-            return (float)(v & 63u);
-          };
-          const float2 dd0 = __half22float2(*reinterpret_cast<const __half2*>(&H0.x));
-          const float2 dd1 = __half22float2(*reinterpret_cast<const __half2*>(&H1.x));
+  if (warp <= kCompWarps) {
+    // ------------------------------------------------------ compute warps
+    const int cw = warp - 1;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    int st = 0, xs = 0;
+    uint32_t ph = 0, xph = 0;
+    for (int s = 0; s < nstages; ++s) {
+      const int blk0 = s * kSBlk;
+      const int nb = min(kSBlk, B - blk0);
+      if (!mbar_wait(&full[st], ph, a.err)) break;
+      if (!mbar_wait(&xempty[xs], xph ^ 1, a.err)) break;
+      const uint8_t* base = smem + st * SBY;
+      float* stash = stash_base + xs * (L::kXBytes / 4);
 #pragma unroll
-          for (int u = 0; u < kG; ++u) {
-            dA[u] = dd0.x * field(H0, u);   // exact products
-            dB[u] = dd1.x * field(H1, u);
-            mA[u] = -(dd0.y * field(H0, 8 + u));
-            mB[u] = -(dd1.y * field(H1, 8 + u));
-          }
+      for (int u = 0; u < kBlkPerWarp; ++u) {
+        const int j = cw * kBlkPerWarp + u;
+        if (j >= nb) break;
+        uint32_t a0[4], a1[4];  // A fragments for the block's halves k 0-15 / 16-31
+        if (!kQ4K) {
+          const uint4 w = *reinterpret_cast<const uint4*>(base + j * 512 + lane * 16);
+          // x: row n0 k 8c..+3, y: row n1 k 8c..+3, z: n0 k 8c+4..+7, w: n1 k 8c+4..+7
+          biased_u8x4_to_f16x4(w.x, a0[0], a0[2]);
+          biased_u8x4_to_f16x4(w.y, a0[1], a0[3]);
+          biased_u8x4_to_f16x4(w.z, a1[0], a1[2]);
+          biased_u8x4_to_f16x4(w.w, a1[1], a1[3]);
+        } else {
+          const uint2 w =
+              *reinterpret_cast<const uint2*>(base + (j >> 1) * 512 + lane * 16 + (j & 1) * 8);
+          a0[0] = nib_pair_to_f16x2<0>(w.x);
+          a0[1] = nib_pair_to_f16x2<4>(w.x);
+          a0[2] = nib_pair_to_f16x2<8>(w.x);
+          a0[3] = nib_pair_to_f16x2<12>(w.x);
+          a1[0] = nib_pair_to_f16x2<0>(w.y);
+          a1[1] = nib_pair_to_f16x2<4>(w.y);
+          a1[2] = nib_pair_to_f16x2<8>(w.y);
+          a1[3] = nib_pair_to_f16x2<12>(w.y);
         }
 #pragma unroll
-        for (int u = 0; u < kG; ++u) {
-          const int j = j0 + u;
-          if (j >= nb) break;
-          // A fragments for the block's two 16-wide halves h = 0, 1
-          uint32_t a0[4], a1[4];
-          if (!kQ4K) {
-            const uint4 w = *reinterpret_cast<const uint4*>(wb + j * 512 + lane * 16);
-            // x: row n0 k 8c..+3, y: row n1 k 8c..+3, z: n0 k 8c+4..+7, w: n1 k 8c+4..+7
-            biased_u8x4_to_f16x4(w.x, a0[0], a0[2]);
-            biased_u8x4_to_f16x4(w.y, a0[1], a0[3]);
-            biased_u8x4_to_f16x4(w.z, a1[0], a1[2]);
-            biased_u8x4_to_f16x4(w.w, a1[1], a1[3]);
-          } else {
-            const uint2 w =
-                *reinterpret_cast<const uint2*>(wb + (j >> 1) * 512 + lane * 16 + (j & 1) * 8);
-            a0[0] = nib_pair_to_f16x2<0>(w.x);
-            a0[1] = nib_pair_to_f16x2<4>(w.x);
-            a0[2] = nib_pair_to_f16x2<8>(w.x);
-            a0[3] = nib_pair_to_f16x2<12>(w.x);
-            a1[0] = nib_pair_to_f16x2<0>(w.y);
-            a1[1] = nib_pair_to_f16x2<4>(w.y);
-            a1[2] = nib_pair_to_f16x2<8>(w.y);
-            a1[3] = nib_pair_to_f16x2<12>(w.y);
-          }
-          uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;  // token k 8c+0..1, +2..3, +4..5, +6..7
+        for (int t = 0; t < TT; ++t) {
+          const int mrow = 8 * t + gr;  // token of this lane's B fragment
+          uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;
           if (mrow < M) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(ab + j * 32);
+            const uint2 bv = *reinterpret_cast<const uint2*>(
+                base + L::act_off() + mrow * kARow + c * 8 + j * 32);
             biased_u8x4_to_f16x4(bv.x ^ 0x80808080u, b00, b01);
             biased_u8x4_to_f16x4(bv.y ^ 0x80808080u, b10, b11);
           }
           float d[4];
           mma_f16_16816(d, a0, b00, b01, zero4);
           mma_f16_16816(d, a1, b10, b11, d);
-          // d[0]: (n0, mc0), d[1]: (n0, mc1), d[2]: (n1, mc0), d[3]: (n1, mc1), exact
+          // d: (n0, tok 8t+2c), (n0, 8t+2c+1), (n1, 8t+2c), (n1, 8t+2c+1): exact sums
+          *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
+              make_float4(d[0], d[1], d[2], d[3]);
           if (kDebug) {
             const int b = blk0 + j;
+            const int n0 = (int)(16 * g + gr), mc0 = 8 * t + 2 * c;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int m = (i & 1) ? mc1 : mc0, n = (i < 2) ? n0 : n1;
+              const int m = mc0 + (i & 1), n = n0 + ((i < 2) ? 0 : 8);
               if (m < M && n < a.N) a.dbg[((int64_t)m * a.N + n) * B + b] = __float2int_rn(d[i]);
             }
           }
-          acc0 = __ffma2_rn(make_float2(d[0], d[1]), make_float2(dA[u], dA[u]), acc0);
-          acc1 = __ffma2_rn(make_float2(d[2], d[3]), make_float2(dB[u], dB[u]), acc1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xfull[xs]);
+      if (++st == NW) { st = 0; ph ^= 1; }
+      if (++xs == 2) { xs = 0; xph ^= 1; }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- chain warp
+  const int n0 = (int)(16 * g + gr), n1 = n0 + 8;
+  float2 acc[TT][2];  // [tile][row n0 / n1]: tokens 8t+2c, 8t+2c+1
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
+  bool ok = true;
+  int st = 0, xs = 0;
+  uint32_t ph = 0, xph = 0;
+  for (int s = 0; s < nstages && ok; ++s) {
+    const int blk0 = s * kSBlk;
+    const int nb = min(kSBlk, B - blk0);
+    ok = mbar_wait(&xfull[xs], xph, a.err);
+    if (!ok) break;
+    const uint8_t* base = smem + st * SBY;
+    const uint8_t* sb = base + L::kWBytes;
+    const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::bsum_off(mrows));
+    const float* stash = stash_base + xs * (L::kXBytes / 4);
+    // blocks in groups of kG (a quad of Q8_0 scales / one Q4_K super-block)
+    constexpr int kG = kQ4K ? 8 : 4;
+    for (int j0 = 0; j0 < nb; j0 += kG) {
+      float dA[kG], dB[kG], mA[kG], mB[kG];
+      if (!kQ4K) {
+        const uint4 sc = *reinterpret_cast<const uint4*>(sb + (j0 >> 2) * 128 + gr * 16);
+        const __half2* h = reinterpret_cast<const __half2*>(&sc);
+        const float2 f0 = __half22float2(h[0]), f1 = __half22float2(h[1]);
+        const float2 f2 = __half22float2(h[2]), f3 = __half22float2(h[3]);
+        dA[0] = f0.x; dA[1] = f0.y; dA[2] = f1.x; dA[3] = f1.y;
+        dB[0] = f2.x; dB[1] = f2.y; dB[2] = f3.x; dB[3] = f3.y;
+      } else {
+        const uint4 H0 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + gr * 16);
+        const uint4 H1 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + (gr + 8) * 16);
+        // 6-bit fields: a 96-bit string in words y, z, w (bytes 4..15)
+        auto field = [](const uint4& H, int f) -> float {
+          const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
+          const int pos = 6 * f;
+          uint32_t v;
+          if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
+          else if (pos >= 64) v = H.w >> (pos - 64);
+          else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
+          return (float)(v & 63u);
+        };
+        const float2 dd0 = __half22float2(*reinterpret_cast<const __half2*>(&H0.x));
+        const float2 dd1 = __half22float2(*reinterpret_cast<const __half2*>(&H1.x));
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+          dA[u] = dd0.x * field(H0, u);   // exact products
+          dB[u] = dd1.x * field(H1, u);
+          mA[u] = -(dd0.y * field(H0, 8 + u));
+          mB[u] = -(dd1.y * field(H1, 8 + u));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kG; ++u) {
+        const int j = j0 + u;
+        if (j >= nb) break;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float4 x = *reinterpret_cast<const float4*>(stash + ((j * TT + t) * 32 + lane) * 4);
+          acc[t][0] = __ffma2_rn(make_float2(x.x, x.y), make_float2(dA[u], dA[u]), acc[t][0]);
+          acc[t][1] = __ffma2_rn(make_float2(x.z, x.w), make_float2(dB[u], dB[u]), acc[t][1]);
           if (kQ4K) {
+            const int mc0 = 8 * t + 2 * c, mc1 = mc0 + 1;
             const float as0 = (mc0 < M) ? (float)bb[mc0 * kSBlk + j] : 0.f;
             const float as1 = (mc1 < M) ? (float)bb[mc1 * kSBlk + j] : 0.f;
             const float2 as = make_float2(as0, as1);
-            acc0 = __ffma2_rn(as, make_float2(mA[u], mA[u]), acc0);
-            acc1 = __ffma2_rn(as, make_float2(mB[u], mB[u]), acc1);
+            acc[t][0] = __ffma2_rn(as, make_float2(mA[u], mA[u]), acc[t][0]);
+            acc[t][1] = __ffma2_rn(as, make_float2(mB[u], mB[u]), acc[t][1]);
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    if (++st == L::kNst) { st = 0; ph ^= 1; }
+    if (lane == 0) {
+      mbar_arrive(&xempty[xs]);
+      mbar_arrive(&empty[st]);
+    }
+    if (++st == NW) { st = 0; ph ^= 1; }
+    if (++xs == 2) { xs = 0; xph ^= 1; }
   }
 
-  if (kDebug || !tile_live) return;
-  const float accs[4] = {acc0.x, acc0.y, acc1.x, acc1.y};
+  if (kDebug || !ok) return;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = (i & 1) ? mc1 : mc0, n = (i < 2) ? n0 : n1;
-    if (m < M && n < a.N) {
-      const float y = accs[i] * __ldg(a.sa + m);
-      if (a.out_f32)
-        reinterpret_cast<float*>(a.out)[(int64_t)m * a.ldo + n] = y;
-      else
-        reinterpret_cast<uint16_t*>(a.out)[(int64_t)m * a.ldo + n] = f32_to_bf16_rne(y);
+  for (int t = 0; t < TT; ++t) {
+    const float accs[4] = {acc[t][0].x, acc[t][0].y, acc[t][1].x, acc[t][1].y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = 8 * t + 2 * c + (i & 1), n = (i < 2) ? n0 : n1;
+      if (m < M && n < a.N) {
+        const float y = accs[i] * __ldg(a.sa + m);
+        if (a.out_f32)
+          reinterpret_cast<float*>(a.out)[(int64_t)m * a.ldo + n] = y;
+        else
+          reinterpret_cast<uint16_t*>(a.out)[(int64_t)m * a.ldo + n] = f32_to_bf16_rne(y);
+      }
     }
   }
 }
 
-template <int R, int TT, bool kQ4K, bool kDebug>
+template <int TT, bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_cfg(const DecodeArgs& a, cudaStream_t st) {
-  using L = DecodeSmem<R, TT, kQ4K>;
-  auto kern = decode_gemm_kernel<R, TT, kQ4K, kDebug>;
+  using L = DecodeSmem<TT, kQ4K>;
+  constexpr int kBudget = 70 * 1024;  // three CTAs per SM
+  auto kern = decode_gemm_kernel<TT, kQ4K, kDebug>;
   static bool configured = false;  // once per process (idempotent if raced)
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+    // the attribute only caps the launch size; occupancy follows the size passed at launch
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid((unsigned)ceil_div(a.G, R)), block(32 * (1 + R * TT));
-  kern<<<grid, block, L::kTotal, st>>>(a);
+  DecodeArgs b = a;
+  const int mrows = a.M < TT * 8 ? a.M : TT * 8;
+  b.nw = L::num_stages(mrows, kBudget);
+  dim3 grid((unsigned)a.G), block(32 * (kCompWarps + 2));
+  kern<<<grid, block, L::total(mrows, b.nw), st>>>(b);
   return cudaGetLastError();
 }
 
 template <bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
-  if (a.M <= 8) return launch_decode_cfg<1, 1, kQ4K, kDebug>(a, st);
-  if (a.M <= 16) return launch_decode_cfg<1, 2, kQ4K, kDebug>(a, st);
-  if (a.M <= 32) return launch_decode_cfg<2, 4, kQ4K, kDebug>(a, st);
-  return launch_decode_cfg<2, 8, kQ4K, kDebug>(a, st);
+  if (a.M <= 8) return launch_decode_cfg<1, kQ4K, kDebug>(a, st);
+  return launch_decode_cfg<2, kQ4K, kDebug>(a, st);
 }
 
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,

@@ -35,7 +35,7 @@ def test_status_strings_and_constants(L):
     for s in range(6):
         assert L.qg_status_string(s).decode().startswith("QG_")
     assert L.qg_version() == 10000
-    assert L.qg_small_m_max() == 64
+    assert L.qg_small_m_max() == 16
 
 
 def test_packed_sizes(L):
@@ -66,7 +66,7 @@ def _gemm(L, q=FAKE, q16=FAKE, s=FAKE, M=4, K=256, w=FAKE, N=16, out=FAKE, dt=0,
     (dict(ldo=8), _lib.QG_EINVAL), (dict(dt=7), _lib.QG_EINVAL), (dict(path=9), _lib.QG_EINVAL),
     (dict(q=FAKE + 8), _lib.QG_EALIGN), (dict(out=FAKE + 2), _lib.QG_EALIGN),
     (dict(w=FAKE + 16), _lib.QG_EALIGN), (dict(q16=FAKE + 4), _lib.QG_EALIGN),
-    (dict(M=65, q16=0), _lib.QG_EINVAL), (dict(M=4, q16=0, path=2), _lib.QG_EINVAL),
+    (dict(M=17, q16=0), _lib.QG_EINVAL), (dict(M=4, q16=0, path=2), _lib.QG_EINVAL),
 ])
 def test_gemm_argument_validation(L, kw, status):
     assert _gemm(L, **kw) == status
