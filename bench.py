@@ -108,6 +108,45 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def source_sha(path):
+    """git blob id of a file (identifies the kernel source a capture was taken on)."""
+    import hashlib
+    data = open(path, "rb").read()
+    return hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the prefill kernel on this workload, from the
+    committed ncu summary -- None when the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", "prefill_traffic_4b_step.json")
+    src = os.path.join(ROOT, "bit_quantized_gemm_gb300", "csrc", "gemm_large.cu")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_sha") != source_sha(src):
+            return None
+        return d.get("bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def reduce_max(value, world):
+    """Max over ranks (the slowest replica sets the job time)."""
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ops_per_rank, world, ms_max):
+    """Whole-job throughput (TOPS): every rank's units over the slowest rank's time."""
+    return world * ops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def make_step_inputs(dev):
     """Seeded inputs of the 4B-class prefill step (x bf16, packed Q8_0 weights)."""
     import bit_quantized_gemm_gb300 as qg
@@ -385,19 +424,16 @@ def main():
         barrier()
         t_wall = time.perf_counter() - t_wall0
     clocks = clk.summary()
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(sum(step_ms) / len(step_ms), world)
     ops = step_ops()
-    value = world * ops / (ms * 1e-3) / 1e12
+    value = job_value(ops, world, ms)
 
     # roofline of the dominant kernel (the prefill GEMM; both shapes of the step)
     gemm_tot = sum(sum(g) for g in gemm_ms) / len(gemm_ms)
     achieved = ops / (gemm_tot * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_burst,
-                "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4),
+                "traffic": measured_traffic(),
                 "peak_source": "%s bf16 dense burst (same rate as the fp16 kind the kernel uses)"
                                % peak_src,
                 "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands)",

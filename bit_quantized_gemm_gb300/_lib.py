@@ -55,6 +55,7 @@ def load():
         "qg_gemm_w4a8_q4k_ex": ([P, P, P, P, I64, I64, P, I64, P, I, I64, I, P], I),
         "qg_debug_block_sums_q8_0": ([P, P, I64, I64, P, I64, P, I, P], I),
         "qg_debug_block_sums_q4k": ([P, P, I64, I64, P, I64, P, I, P], I),
+        "qg_debug_wait_timeout": ([ctypes.c_uint32, P], I),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -170,6 +171,11 @@ def debug_block_sums(kind, q, q16, packed, N, path, stream=None):
     fn = load().qg_debug_block_sums_q8_0 if kind == "q8_0" else load().qg_debug_block_sums_q4k
     _check(fn(_ptr(q), _ptr(q16), M, K, _ptr(packed), N, _ptr(isum), PATHS[path], _stream(stream)))
     return isum
+
+
+def debug_wait_timeout(polls, stream=None):
+    """Launch one bounded wait that is made to run out (failure-detection test)."""
+    _check(load().qg_debug_wait_timeout(polls, _stream(stream)))
 
 
 def check_device_error(stream=None):

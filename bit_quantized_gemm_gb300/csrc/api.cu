@@ -279,6 +279,26 @@ qg_status qg_gemm_w4a8_q4k(const int8_t* q, const uint16_t* q16, const float* sc
                   nullptr, stream);
 }
 
+// A single bounded wait on a barrier that nothing arrives at: after `polls`
+// polls it records a timeout in the device error word and returns.
+__global__ void wait_timeout_probe_kernel(uint32_t polls, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, err, polls);
+}
+
+qg_status qg_debug_wait_timeout(uint32_t polls, void* stream) {
+  if (polls == 0 || polls > (1u << 20)) return fail(QG_EINVAL, "polls must be in [1, 2^20]");
+  uint32_t* err = error_word();
+  if (!err) return fail(QG_ECUDA, "no device error word on the current device");
+  wait_timeout_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(polls, err);
+  return from_cuda(cudaGetLastError(), "timeout probe launch");
+}
+
 static qg_status check_debug(const int32_t* isum, int64_t M, int64_t K, int64_t N) {
   if (!isum) return fail(QG_EINVAL, "null isum");
   if (M < 1 || N < 1 || K < kBlk) return fail(QG_EINVAL, "bad sizes");

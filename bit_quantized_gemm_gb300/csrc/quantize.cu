@@ -8,17 +8,16 @@
 // per-32-block sums of q (the W4A8 min term needs them) and an fp16 copy of q
 // (the prefill tensor-core operand).
 //
-// One CTA per row, 256 threads, 16-byte vector loads of 8 values. The row is
-// held in registers between the absmax pass and the quantize pass when it
-// fits (K <= 256*8*kRegChunks), else re-read (second read hits L2).
-// HBM-bound: per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with q16)
-// written.
+// One CTA per row, 16-byte vector loads of 8 values. The row is held in
+// registers between the absmax pass and the quantize pass when it fits
+// (K <= kThreads*8*kRegChunks), else re-read (second read hits L2); threads
+// and register chunks are chosen from K so that several rows per SM are in
+// flight. HBM-bound: per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with
+// q16) written.
 #include "qg_common.cuh"
 
 namespace qg {
 
-constexpr int kQThreads = 256;
-constexpr int kRegChunks = 9;  // 9 * 256 * 8 = 18432 values per row in registers
 
 template <bool kBf16>
 __device__ __forceinline__ void load_chunk(const void* row, int64_t c, float (&v)[8]) {
@@ -38,13 +37,23 @@ __device__ __forceinline__ void load_chunk(const void* row, int64_t c, float (&v
   }
 }
 
-__device__ __forceinline__ int quant1(float x, float s, bool zero_row) {
-  if (zero_row) return 0;
-  int r = __float2int_rn(__fdiv_rn(x, s));  // IEEE quotient, then ties-to-even
-  return max(-127, min(127, r));
+// rint(x / s) with the IEEE-rounded quotient, returned as a float.
+// r = x * rcp_rn(s) differs from the exact quotient by at most 2^-16 for
+// |x/s| <= 128 (two roundings of relative size 2^-24 each), and the rounded
+// quotient by at most 2^-16 + 2^-17 < 2^-15. rint() of the two can only
+// differ when a half-integer lies within 2^-15 of r; those rare elements take
+// the exact division.
+// inv = 0 selects the exact division for every element (used when s is
+// subnormal, where the reciprocal loses precision or overflows).
+__device__ __forceinline__ float qround(float x, float s, float inv) {
+  const float r = x * inv;
+  const float q0 = rintf(r);
+  if (__builtin_expect(inv == 0.0f || fabsf(r - q0) >= 0.5f - 3.0517578125e-05f, 0))
+    return rintf(__fdiv_rn(x, s));
+  return q0;
 }
 
-template <bool kBf16>
+template <bool kBf16, int kQThreads, int kRegChunks>
 __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
     const void* __restrict__ x, int64_t ldx, int K, int8_t* __restrict__ q,
     float* __restrict__ scale, int32_t* __restrict__ bsum, __half* __restrict__ q16) {
@@ -88,9 +97,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
 
   const float s = __fdiv_rn(amax, 127.0f);
   const bool zero_row = (amax == 0.0f);
+  float inv = 0.0f;
+  if (!zero_row && s >= 1.17549435e-38f) {  // normal s: 1/s is finite and exact to 2^-24
+    inv = __frcp_rn(s);
+    if (isinf(inv)) inv = 0.0f;
+  }
   if (tid == 0) scale[m] = s;
 
-  int8_t* qrow = q + m * (int64_t)K;
+  int8_t* qrow = q ? q + m * (int64_t)K : nullptr;
   __half* hrow = q16 ? q16 + m * (int64_t)K : nullptr;
   int32_t* brow = bsum ? bsum + m * (int64_t)(K / kBlk) : nullptr;
 
@@ -98,32 +112,44 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
   // compute on zeros and store nothing), so the block-sum shuffles always
   // see the full warp.
   auto emit = [&](int c, bool valid, const float (&t)[8]) {
-    int qi[8];
+    float qf[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) qi[j] = valid ? quant1(t[j], s, zero_row) : 0;
+    for (int j = 0; j < 8; ++j) {
+      float v = (valid && !zero_row) ? qround(t[j], s, inv) : 0.0f;
+      qf[j] = fminf(127.0f, fmaxf(-127.0f, v));
+    }
     if (valid) {
-      uint32_t lo = (qi[0] & 0xFF) | ((qi[1] & 0xFF) << 8) | ((qi[2] & 0xFF) << 16) |
-                    ((uint32_t)(qi[3] & 0xFF) << 24);
-      uint32_t hi = (qi[4] & 0xFF) | ((qi[5] & 0xFF) << 8) | ((qi[6] & 0xFF) << 16) |
-                    ((uint32_t)(qi[7] & 0xFF) << 24);
-      *reinterpret_cast<uint2*>(qrow + (int64_t)c * 8) = make_uint2(lo, hi);
+      if (qrow) {
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b0 = (uint32_t)__float2int_rz(qf[4 * h + 0]);
+          const uint32_t b1 = (uint32_t)__float2int_rz(qf[4 * h + 1]);
+          const uint32_t b2 = (uint32_t)__float2int_rz(qf[4 * h + 2]);
+          const uint32_t b3 = (uint32_t)__float2int_rz(qf[4 * h + 3]);
+          uint32_t lo, hi;
+          asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(b0), "r"(b1));  // b0.x, b1.x
+          asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(b2), "r"(b3));
+          asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w[h]) : "r"(lo), "r"(hi));
+        }
+        *reinterpret_cast<uint2*>(qrow + (int64_t)c * 8) = make_uint2(w[0], w[1]);
+      }
       if (hrow) {
         __half2 h[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          h[j] = __halves2half2(__int2half_rn(qi[2 * j]), __int2half_rn(qi[2 * j + 1]));
+        for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(qf[2 * j], qf[2 * j + 1]);  // exact
         *reinterpret_cast<uint4*>(hrow + (int64_t)c * 8) = *reinterpret_cast<uint4*>(h);
       }
     }
     if (brow) {
       // chunks 4j..4j+3 form block j; their owners are 4 consecutive lanes,
       // all valid or all invalid (the chunk count is a multiple of 4)
-      int part = 0;
+      float part = 0.0f;  // exact: |sum| <= 32 * 127
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part += qi[j];
+      for (int j = 0; j < 8; ++j) part += qf[j];
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (valid && (c & 3) == 0) brow[c >> 2] = part;
+      if (valid && (c & 3) == 0) brow[c >> 2] = (int32_t)part;
     }
   };
 
@@ -150,16 +176,36 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
   }
 }
 
+template <bool kBf16, int kT, int kRC>
+static void launch_q(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* q, float* scale,
+                     int32_t* bsum, uint16_t* q16, cudaStream_t st) {
+  quantize_act_kernel<kBf16, kT, kRC><<<(unsigned)M, kT, 0, st>>>(
+      x, ldx, (int)K, q, scale, bsum, reinterpret_cast<__half*>(q16));
+}
+
+template <bool kBf16>
+static void launch_q_k(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* q, float* scale,
+                       int32_t* bsum, uint16_t* q16, cudaStream_t st) {
+  // threads x register chunks x 8 values >= K where possible
+  if (K <= 128 * 3 * 8)
+    launch_q<kBf16, 128, 3>(x, M, K, ldx, q, scale, bsum, q16, st);
+  else if (K <= 128 * 5 * 8)
+    launch_q<kBf16, 128, 5>(x, M, K, ldx, q, scale, bsum, q16, st);
+  else if (K <= 256 * 5 * 8)
+    launch_q<kBf16, 256, 5>(x, M, K, ldx, q, scale, bsum, q16, st);
+  else if (K <= 256 * 9 * 8)
+    launch_q<kBf16, 256, 9>(x, M, K, ldx, q, scale, bsum, q16, st);
+  else
+    launch_q<kBf16, 512, 9>(x, M, K, ldx, q, scale, bsum, q16, st);
+}
+
 cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
                                 int8_t* q, float* scale, int32_t* bsum, uint16_t* q16,
                                 cudaStream_t st) {
-  dim3 grid((unsigned)M), block(kQThreads);
   if (bf16)
-    quantize_act_kernel<true><<<grid, block, 0, st>>>(x, ldx, (int)K, q, scale, bsum,
-                                                      reinterpret_cast<__half*>(q16));
+    launch_q_k<true>(x, M, K, ldx, q, scale, bsum, q16, st);
   else
-    quantize_act_kernel<false><<<grid, block, 0, st>>>(x, ldx, (int)K, q, scale, bsum,
-                                                       reinterpret_cast<__half*>(q16));
+    launch_q_k<false>(x, M, K, ldx, q, scale, bsum, q16, st);
   return cudaGetLastError();
 }
 

@@ -174,6 +174,12 @@ qg_status qg_debug_block_sums_q4k(const int8_t* q, const uint16_t* q16, int64_t 
                                   const void* w_packed, int64_t N, int32_t* isum,
                                   qg_path path, void* stream);
 
+/* Test support for failure detection: launches one bounded wait on a
+ * barrier that nothing completes; after `polls` polls (1 .. 2^20) it records
+ * a timeout in the device error word and returns, leaving the context usable.
+ * The following qg_check_device_error() reports QG_ETIMEOUT and clears it. */
+qg_status qg_debug_wait_timeout(uint32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

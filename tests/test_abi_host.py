@@ -21,7 +21,7 @@ def L():
 
 def test_exports_every_declared_symbol(L):
     names = _lib.declared_symbols()
-    assert len(names) >= 16
+    assert len(names) >= 17
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.SO_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -97,3 +97,8 @@ def test_q4k_and_quantize_validation(L):
 def test_binding_raises_without_gpu_work(L):
     with pytest.raises(qg.QGError):
         _lib._check(_lib.QG_EINVAL)
+
+
+def test_timeout_probe_validation(L):
+    assert L.qg_debug_wait_timeout(0, None) == _lib.QG_EINVAL
+    assert L.qg_debug_wait_timeout((1 << 20) + 1, None) == _lib.QG_EINVAL

@@ -265,3 +265,55 @@ def test_w4a8_batch_invariance():
     for r in (0, 17, 149):
         o = qg.gemm_w4a8_q4k(q[r:r + 1], h[r:r + 1], s[r:r + 1], bs[r:r + 1], packed, N)
         assert np.array_equal(out_bits(o)[0], out_bits(full_l)[r])
+
+
+def test_quantize_near_ties_and_tiny_scales():
+    """Elements whose quotient lands within a few ulps of a half-integer, and
+    rows with subnormal scales, take the exact-division branch; all must match
+    the oracle bit for bit."""
+    rng = np.random.default_rng(17)
+    M, K = 64, 512
+    x = np.zeros((M, K), np.float32)
+    for m in range(M):
+        am = np.float32(rng.uniform(0.5, 4.0))
+        s = am / np.float32(127)
+        h = rng.integers(-126, 126, size=K).astype(np.float32) + np.float32(0.5)
+        v = (h * s).astype(np.float32)
+        # nudge by -3..3 ulps around each half-integer multiple of s
+        steps = rng.integers(-3, 4, size=K)
+        v = np.array([np.float32(vi) for vi in v])
+        for i in range(K):
+            for _ in range(abs(int(steps[i]))):
+                v[i] = np.nextafter(v[i], np.float32(np.inf) if steps[i] > 0 else np.float32(-np.inf))
+        v[0] = am
+        x[m] = v
+    x[M - 1] = x[M - 1] * np.float32(1e-39 / 4.0)   # subnormal scale row
+    x[M - 2] = x[M - 2] * np.float32(2e-35)        # tiny but normal scale
+    q, s, bs, h = run_quant(x, None)
+    oq, os_, obs = oracle_quant(x, None)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(bs.cpu().numpy(), obs)
+    assert np.array_equal(h.float().cpu().numpy(), oq.astype(np.float32))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a fault: a barrier wait that nothing completes
+    gives up after its poll limit, the host reads QG_ETIMEOUT, the word is
+    cleared, and the next GEMM still runs and matches the oracle."""
+    import time
+    from bit_quantized_gemm_gb300 import _lib
+    qg.check_device_error()
+    t0 = time.time()
+    qg.debug_wait_timeout(256)
+    with pytest.raises(qg.QGError) as e:
+        qg.check_device_error()
+    assert e.value.status == _lib.QG_ETIMEOUT
+    assert time.time() - t0 < 30
+    qg.check_device_error()  # cleared
+    M, K, N = 3, 256, 48
+    x, bits, blocks = make_w8a8(M, K, N, seed=5)
+    out, _ = gpu_w8a8(x, bits, blocks, N, "large")
+    oq, os_ = oracle.quantize_act(bits)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    assert np.array_equal(out_bits(out), ob)
