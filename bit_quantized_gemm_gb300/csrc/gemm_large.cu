@@ -37,6 +37,9 @@ namespace qg {
 #ifndef QG_STAGES
 #define QG_STAGES 4
 #endif
+#ifndef QG_CTAS_PER_SM
+#define QG_CTAS_PER_SM 1
+#endif
 #ifndef QG_EPI_WARPS
 #define QG_EPI_WARPS 8
 #endif
@@ -46,7 +49,8 @@ constexpr int kStages = QG_STAGES;
 constexpr int kEpiWarps = QG_EPI_WARPS;  // multiple of 4 (tensor-memory lane quarters)
 constexpr int kLThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
-constexpr uint32_t kTmemCols = 512;
+constexpr int kCtasPerSm = QG_CTAS_PER_SM;  // CTAs sharing an SM (and its tensor memory)
+constexpr uint32_t kTmemCols = 512 / kCtasPerSm;
 constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
 
 // Tile width BM = tokens per tile (MMA N, tensor-memory columns). 256 suits
@@ -54,9 +58,9 @@ constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
 // the register room of BM = 128.
 template <int BM>
 struct LargeCfg {
-  static_assert(BM % 16 == 0 && BM >= 64 && BM <= 256 && 512 % BM == 0, "tile width");
+  static_assert(BM % 16 == 0 && BM >= 64 && BM <= 256 && kTmemCols % BM == 0, "tile width");
   static constexpr int kBM = BM;
-  static constexpr int kTBufs = 512 / BM;  // per-block accumulators filling tensor memory
+  static constexpr int kTBufs = kTmemCols / BM;  // per-block accumulators filling this CTA's tensor memory
   static constexpr uint32_t kStageBBytes = BM * kBK * 2;
   static constexpr int kColsPerThread = BM / (kEpiWarps / 4);
 };
@@ -75,8 +79,17 @@ template <int BM>
 constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<BM>) + 1024; }  // + alignment slack
 static_assert(kStageABytes % 1024 == 0, "1024-B aligned stages");
 
+#ifndef QG_BM_W8A8
+#define QG_BM_W8A8 256
+#endif
+#ifndef QG_BM_W4A8
+#define QG_BM_W4A8 128
+#endif
+#ifndef QG_EPI_BATCH
+#define QG_EPI_BATCH 1
+#endif
 template <bool kQ4K>
-__host__ __device__ constexpr int bm_for() { return kQ4K ? 128 : 256; }
+__host__ __device__ constexpr int bm_for() { return kQ4K ? QG_BM_W4A8 : QG_BM_W8A8; }
 
 struct LargeArgs {
   const float* d32;      // W8A8: [N][ldd] fp32 scales; W4A8: d*sc [N][ldd]
@@ -106,7 +119,7 @@ __device__ __forceinline__ void tile_coords(int tile, int MT, int NT, int& mt, i
 }
 
 template <bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(kLThreads, 1)
+__global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const LargeArgs args) {
   constexpr int BM = bm_for<kQ4K>();
@@ -258,24 +271,20 @@ __global__ void __launch_bounds__(kLThreads, 1)
 #pragma unroll
       for (int i = 0; i < kColsPerThread / 2; ++i) acc[i] = make_float2(0.f, 0.f);
 
-      // scales of four blocks at a time, fetched one group ahead
-      float4 dq = make_float4(0, 0, 0, 0), mq = dq, dq_next = dq, mq_next = dq;
+      // the scales of block blk+1 are fetched while block blk is processed;
+      // the load is volatile so the compiler keeps it a block ahead of its use
+      float d_next = 0.0f, m_next = 0.0f;
       if (nvalid) {
-        dq_next = __ldg(reinterpret_cast<const float4*>(drow));
-        if (kQ4K) mq_next = __ldg(reinterpret_cast<const float4*>(mrow));
+        d_next = ldg_f32_pinned(drow);
+        if (kQ4K) m_next = ldg_f32_pinned(mrow);
       }
       for (int blk = 0; blk < NB && ok; ++blk) {
-        const int j = blk & 3;
-        if (j == 0) {
-          dq = dq_next;
-          mq = mq_next;
-          if (blk + 4 < NB && nvalid) {
-            dq_next = __ldg(reinterpret_cast<const float4*>(drow + blk + 4));
-            if (kQ4K) mq_next = __ldg(reinterpret_cast<const float4*>(mrow + blk + 4));
-          }
+        const float dw = d_next;
+        const float ndm = kQ4K ? -m_next : 0.0f;
+        if (blk + 1 < NB && nvalid) {
+          d_next = ldg_f32_pinned(drow + blk + 1);
+          if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
         }
-        const float dw = j == 0 ? dq.x : j == 1 ? dq.y : j == 2 ? dq.z : dq.w;
-        const float ndm = kQ4K ? -(j == 0 ? mq.x : j == 1 ? mq.y : j == 2 ? mq.z : mq.w) : 0.0f;
         ok = mbar_wait(&S.tfull[tb], tphase, args.err);
         if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
         if (!ok) break;
@@ -285,34 +294,52 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const float2 dw2 = make_float2(dw, dw);
         const float2 ndm2 = make_float2(ndm, ndm);
         constexpr int kChunk = 16;  // columns per tensor-memory load
+        constexpr int kNch = kColsPerThread / kChunk;
+        // kBatch loads are issued before one wait, so the tensor-memory load
+        // latency is paid once per batch instead of once per chunk
+        constexpr int kBatch = QG_EPI_BATCH < kNch ? QG_EPI_BATCH : kNch;
+        static_assert(kNch % kBatch == 0, "batch must divide the chunks");
 #pragma unroll
-        for (int ch = 0; ch < kColsPerThread / kChunk; ++ch) {
-          uint32_t v[kChunk];
-          tmem_ld16(taddr + ch * kChunk, v);
+        for (int c0 = 0; c0 < kNch; c0 += kBatch) {
+          uint32_t v[kBatch][kChunk];
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) tmem_ld16(taddr + (c0 + b) * kChunk, v[b]);
           tmem_wait_ld();
-          if (ch == kColsPerThread / kChunk - 1) {
+          // pin the loaded registers after the wait: no use may move above it
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) asm volatile("" : "+r"(v[b][i]));
+          if (c0 + kBatch == kNch) {
+            // all of this block's columns are in registers: hand the buffer back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.tempty[tb]);
           }
-          if (kDebug) {
-            const int m0 = mt * kBM + half * kColsPerThread + ch * kChunk;
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i) {
-              const int m = m0 + i;
-              if (m < M && nvalid)
-                args.dbg[((int64_t)m * N + n) * NB + blk] = __float2int_rn(__uint_as_float(v[i]));
+          for (int b = 0; b < kBatch; ++b) {
+            const int ch = c0 + b;
+            if (kDebug) {
+              const int m0 = mt * kBM + half * kColsPerThread + ch * kChunk;
+#pragma unroll
+              for (int i = 0; i < kChunk; ++i) {
+                const int m = m0 + i;
+                if (m < M && nvalid)
+                  args.dbg[((int64_t)m * N + n) * NB + blk] =
+                      __float2int_rn(__uint_as_float(v[b][i]));
+              }
             }
-          }
 #pragma unroll
-          for (int i = 0; i < kChunk / 2; ++i) {
-            const float2 x = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            float2& a2 = acc[ch * (kChunk / 2) + i];
-            a2 = __ffma2_rn(x, dw2, a2);
-            if (kQ4K) {
-              const float2 as = *reinterpret_cast<const float2*>(
-                  &S.asum[aslot][half * kColsPerThread + ch * kChunk + 2 * i]);
-              a2 = __ffma2_rn(as, ndm2, a2);
+            for (int i = 0; i < kChunk / 2; ++i) {
+              const float2 x =
+                  make_float2(__uint_as_float(v[b][2 * i]), __uint_as_float(v[b][2 * i + 1]));
+              float2& a2 = acc[ch * (kChunk / 2) + i];
+              a2 = __ffma2_rn(x, dw2, a2);
+              if (kQ4K) {
+                const float2 as = *reinterpret_cast<const float2*>(
+                    &S.asum[aslot][half * kColsPerThread + ch * kChunk + 2 * i]);
+                a2 = __ffma2_rn(as, ndm2, a2);
+              }
             }
           }
         }
@@ -410,7 +437,8 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const CUtensorMap& tb
     configured = true;
   }
   const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int slots = num_sms() * kCtasPerSm;
+  const int grid = tiles < slots ? tiles : slots;
   kern<<<grid, kLThreads, kSmem, st>>>(ta, tb, a);
   return cudaGetLastError();
 }

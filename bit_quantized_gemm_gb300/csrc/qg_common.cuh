@@ -346,6 +346,14 @@ __device__ __forceinline__ int4 ldg_stream(const void* p) {
   return v;
 }
 
+// Read-only 4-byte global load as volatile asm: it stays where it is written
+// in program order (a prefetch the compiler may not sink to its use).
+__device__ __forceinline__ float ldg_f32_pinned(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
