@@ -23,11 +23,14 @@
 // Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (lane 0); for W4A8 the whole warp also converts
 //               the activation block sums of each block into a float ring
-//   warp 1      tensor-memory allocator and MMA issuer (lane 0)
-//   warps 2..9  epilogue: warp w reads lanes 32*(w%4).. of tensor memory and
-//               half (w-2)/4 of the 256 token columns; each thread keeps 128
-//               fp32 accumulators (one weight row x 128 tokens) in registers
-//               and applies acc = fma(isum, d, acc) with packed f32x2 FMAs.
+//   warps 1, 2  MMA issuers (lane 0): warp 1 the even blocks of each tile into
+//               accumulator 0, warp 2 the odd blocks into accumulator 1 --
+//               two issuers, so that one's barrier latencies overlap the
+//               other's work; warp 1 also allocates tensor memory
+//   warps 3..10 epilogue: warp w reads lanes 32*(w%4).. of tensor memory and
+//               half (w-3)/4 of the token columns; each thread keeps its fp32
+//               accumulators (one weight row x its tokens) in registers and
+//               applies acc = fma(isum, d, acc) with packed f32x2 FMAs.
 #include <cuda.h>
 
 #include "qg_common.cuh"
@@ -47,7 +50,8 @@ constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lane
 constexpr int kBK = 64;       // K per stage
 constexpr int kStages = QG_STAGES;
 constexpr int kEpiWarps = QG_EPI_WARPS;  // multiple of 4 (tensor-memory lane quarters)
-constexpr int kLThreads = 32 * (2 + kEpiWarps);
+constexpr int kFirstEpiWarp = 3;         // warp 0 producer, warps 1-2 MMA issuers
+constexpr int kLThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
 constexpr int kCtasPerSm = QG_CTAS_PER_SM;  // CTAs sharing an SM (and its tensor memory)
 constexpr uint32_t kTmemCols = 512 / kCtasPerSm;
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], 1);
+      mbar_init(&S.empty[i], 2);  // one commit from each MMA issuer
     }
     for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
@@ -214,38 +218,37 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer `par` handles block 2s+par of every stage s, in accumulator `par`
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBN, kBM);
+      static_assert(kTBufs >= 2, "two accumulators");
+      const int par = warp - 1;
       int stage = 0;
       uint32_t phase = 0;
-      int tb = 0;
       uint32_t tphase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         for (int s = 0; s < NS && ok; ++s) {
-          ok = mbar_wait(&S.full[stage], phase, args.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(S.a[stage]);
-          const uint32_t b_addr = smem_u32(S.b[stage]);
-          for (int j = 0; j < 2; ++j) {
-            if (2 * s + j >= NB) break;
-            ok = mbar_wait(&S.tempty[tb], tphase ^ 1, args.err);
+          if (2 * s + par < NB) {
+            ok = mbar_wait(&S.full[stage], phase, args.err);
+            if (ok) ok = mbar_wait(&S.tempty[par], tphase ^ 1, args.err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(tb * kBM);
+            const uint32_t a_addr = smem_u32(S.a[stage]);
+            const uint32_t b_addr = smem_u32(S.b[stage]);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(par * kBM);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t koff = (uint32_t)((j * 32 + kk * 16) * 2);  // bytes within row
+              const uint32_t koff = (uint32_t)((par * 32 + kk * 16) * 2);  // bytes within row
               mma_f16_ss(d_tmem, smem_desc_sw128(a_addr + koff), smem_desc_sw128(b_addr + koff),
                          idesc, kk);
             }
-            mma_commit(&S.tfull[tb]);
-            if (++tb == kTBufs) { tb = 0; tphase ^= 1; }
+            mma_commit(&S.tfull[par]);
+            tphase ^= 1;
           }
-          mma_commit(&S.empty[stage]);
+          mma_commit(&S.empty[stage]);  // arrives once this issuer's MMAs are done
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -254,9 +257,8 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    int tb = 0;
-    uint32_t tphase = 0;
+    const int half = (warp - kFirstEpiWarp) >> 2;
+    uint32_t tphases = 0;  // bit b: phase of accumulator b
     int aslot = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -285,7 +287,8 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           d_next = ldg_f32_pinned(drow + blk + 1);
           if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
         }
-        ok = mbar_wait(&S.tfull[tb], tphase, args.err);
+        const int tb = blk & 1;  // accumulator of this block (issuer blk % 2)
+        ok = mbar_wait(&S.tfull[tb], (tphases >> tb) & 1u, args.err);
         if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
         if (!ok) break;
         tc_fence_after();
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           if (lane == 0) mbar_arrive(&S.aempty[aslot]);
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
-        if (++tb == kTBufs) { tb = 0; tphase ^= 1; }
+        tphases ^= 1u << tb;
       }
       if (!ok || kDebug) continue;
       // final scale by the activation scale and store out[m][n]
