@@ -45,6 +45,7 @@ def load():
         "qg_small_m_max": ([], I64),
         "qg_check_device_error": ([P], I),
         "qg_quantize_act": ([P, I, I64, I64, I64, P, P, P, P, P], I),
+        "qg_quantize_act_static": ([P, I, I64, I64, I64, P, I64, P, P, P, P], I),
         "qg_q8_0_packed_bytes": ([I64, I64], SZ),
         "qg_pack_q8_0": ([P, I64, I64, P, P], I),
         "qg_gemm_w8a8_q8_0": ([P, P, P, I64, I64, P, I64, P, I, I64, P], I),
@@ -113,6 +114,25 @@ def quantize_act(x, block_sums=False, q16=False, out=None, stream=None):
     _check(load().qg_quantize_act(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(q),
                                   _ptr(s), _ptr(bs), _ptr(h), _stream(stream)))
     return q, s, bs, h
+
+
+def quantize_act_static(x, scale, block_sums=False, q16=False, out=None, stream=None):
+    """x: cuda [M, K] bf16/fp32; scale: cuda fp32 [M] (per row) or [1] (all rows)
+    -> (q int8, block_sums or None, q16 or None). Values beyond s*127 saturate."""
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    stride = 0 if scale.numel() == 1 else 1
+    if out is None:
+        dev = x.device
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        bs = torch.empty((M, K // 32), dtype=torch.int32, device=dev) if block_sums else None
+        h = torch.empty((M, K), dtype=torch.float16, device=dev) if q16 else None
+    else:
+        q, bs, h = out
+    _check(load().qg_quantize_act_static(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0),
+                                         _ptr(scale), stride, _ptr(q), _ptr(bs), _ptr(h),
+                                         _stream(stream)))
+    return q, bs, h
 
 
 def q8_0_packed_bytes(N, K):

@@ -12,6 +12,10 @@ namespace qg {
 cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
                                 int8_t* q, float* scale, int32_t* bsum, uint16_t* q16,
                                 cudaStream_t st);
+cudaError_t launch_quantize_act_static(const void* x, bool bf16, int64_t M, int64_t K,
+                                       int64_t ldx, const float* s_in, int64_t s_stride,
+                                       int8_t* q, int32_t* bsum, uint16_t* q16,
+                                       cudaStream_t st);
 cudaError_t launch_pack_q8_0(const void* blocks, int64_t N, int64_t K, void* packed,
                              cudaStream_t st);
 cudaError_t launch_pack_q4k(const void* sblocks, int64_t N, int64_t K, void* packed,
@@ -175,6 +179,28 @@ qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
     return fail(QG_EALIGN, "q and q16 need 16-byte, scale and block_sums 4-byte alignment");
   return from_cuda(launch_quantize_act(x, x_dtype == QG_BF16, M, K, ldx, q, scale, block_sums, q16,
                                        reinterpret_cast<cudaStream_t>(stream)),
+                   "quantize launch");
+}
+
+qg_status qg_quantize_act_static(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                                 int64_t ldx, const float* scale, int64_t scale_stride, int8_t* q,
+                                 int32_t* block_sums, uint16_t* q16, void* stream) {
+  if (!x || !q || !scale) return fail(QG_EINVAL, "null pointer argument");
+  if (x_dtype != QG_BF16 && x_dtype != QG_F32) return fail(QG_EINVAL, "x_dtype must be QG_BF16 or QG_F32");
+  if (M < 1 || M > kMaxM) return fail(QG_EINVAL, "M=%lld out of range [1, 2^24]", (long long)M);
+  if (scale_stride != 0 && scale_stride != 1) return fail(QG_EINVAL, "scale_stride must be 0 or 1");
+  qg_status s = check_k(K, kBlk);
+  if (s != QG_OK) return s;
+  const int64_t es = x_dtype == QG_BF16 ? 2 : 4;
+  if (ldx < K) return fail(QG_EINVAL, "ldx=%lld < K=%lld", (long long)ldx, (long long)K);
+  if (!aligned(x, 16) || (ldx * es) % 16 != 0)
+    return fail(QG_EALIGN, "x needs 16-byte alignment and a row stride that is a multiple of 16 bytes");
+  if (!aligned(q, 16) || !aligned(scale, 4) || (block_sums && !aligned(block_sums, 16)) ||
+      (q16 && !aligned(q16, 16)))
+    return fail(QG_EALIGN, "q and q16 need 16-byte, block_sums 16-byte, scale 4-byte alignment");
+  return from_cuda(launch_quantize_act_static(x, x_dtype == QG_BF16, M, K, ldx, scale,
+                                              scale_stride, q, block_sums, q16,
+                                              reinterpret_cast<cudaStream_t>(stream)),
                    "quantize launch");
 }
 

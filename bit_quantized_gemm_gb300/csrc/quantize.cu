@@ -53,10 +53,13 @@ __device__ __forceinline__ float qround(float x, float s, float inv) {
   return q0;
 }
 
-template <bool kBf16, int kQThreads, int kRegChunks>
+// kStatic: the scale is given (s_in[m * s_stride], e.g. calibrated once) and
+// not computed; values beyond it saturate at +-127.
+template <bool kBf16, int kQThreads, int kRegChunks, bool kStatic>
 __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
     const void* __restrict__ x, int64_t ldx, int K, int8_t* __restrict__ q,
-    float* __restrict__ scale, int32_t* __restrict__ bsum, __half* __restrict__ q16) {
+    float* __restrict__ scale, int32_t* __restrict__ bsum, __half* __restrict__ q16,
+    const float* __restrict__ s_in, int64_t s_stride) {
   const int64_t m = blockIdx.x;
   const int tid = threadIdx.x;
   const int nchunks = K / 8;
@@ -64,20 +67,23 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
 
   float v[kRegChunks][8];
   float amax = 0.0f;
+  if (kStatic) amax = 1.0f;  // no absmax pass: only the given scale matters
   const bool in_regs = nchunks <= kRegChunks * kQThreads;
 #pragma unroll
   for (int i = 0; i < kRegChunks; ++i) {
     const int c = tid + i * kQThreads;
     if (c < nchunks) {
       load_chunk<kBf16>(row, c, v[i]);
+      if (!kStatic) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
     }
   }
-  if (!in_regs) {
+  if (!in_regs && !kStatic) {
     for (int c = tid + kRegChunks * kQThreads; c < nchunks; c += kQThreads) {
       float t[8];
       load_chunk<kBf16>(row, c, t);
@@ -85,24 +91,28 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(t[j]));
     }
   }
-  // block-wide max
+  float s;
+  if (kStatic) {
+    s = s_in[m * s_stride];
+  } else {
+    // block-wide max
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  __shared__ float red[kQThreads / 32];
-  if ((tid & 31) == 0) red[tid >> 5] = amax;
-  __syncthreads();
-  amax = red[0];
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float red[kQThreads / 32];
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
 #pragma unroll
-  for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-
-  const float s = __fdiv_rn(amax, 127.0f);
-  const bool zero_row = (amax == 0.0f);
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    s = __fdiv_rn(amax, 127.0f);
+  }
+  const bool zero_row = kStatic ? (s == 0.0f) : (amax == 0.0f);
   float inv = 0.0f;
   if (!zero_row && s >= 1.17549435e-38f) {  // normal s: 1/s is finite and exact to 2^-24
     inv = __frcp_rn(s);
     if (isinf(inv)) inv = 0.0f;
   }
-  if (tid == 0) scale[m] = s;
+  if (!kStatic && tid == 0) scale[m] = s;
 
   int8_t* qrow = q ? q + m * (int64_t)K : nullptr;
   __half* hrow = q16 ? q16 + m * (int64_t)K : nullptr;
@@ -176,36 +186,60 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
   }
 }
 
-template <bool kBf16, int kT, int kRC>
-static void launch_q(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* q, float* scale,
-                     int32_t* bsum, uint16_t* q16, cudaStream_t st) {
-  quantize_act_kernel<kBf16, kT, kRC><<<(unsigned)M, kT, 0, st>>>(
-      x, ldx, (int)K, q, scale, bsum, reinterpret_cast<__half*>(q16));
+struct QArgs {
+  const void* x;
+  int64_t M, K, ldx;
+  int8_t* q;
+  float* scale;
+  int32_t* bsum;
+  uint16_t* q16;
+  const float* s_in;
+  int64_t s_stride;
+};
+
+template <bool kBf16, int kT, int kRC, bool kStatic>
+static void launch_q(const QArgs& a, cudaStream_t st) {
+  quantize_act_kernel<kBf16, kT, kRC, kStatic><<<(unsigned)a.M, kT, 0, st>>>(
+      a.x, a.ldx, (int)a.K, a.q, a.scale, a.bsum, reinterpret_cast<__half*>(a.q16), a.s_in,
+      a.s_stride);
 }
 
-template <bool kBf16>
-static void launch_q_k(const void* x, int64_t M, int64_t K, int64_t ldx, int8_t* q, float* scale,
-                       int32_t* bsum, uint16_t* q16, cudaStream_t st) {
+template <bool kBf16, bool kStatic>
+static void launch_q_k(const QArgs& a, cudaStream_t st) {
   // threads x register chunks x 8 values >= K where possible
+  const int64_t K = a.K;
   if (K <= 128 * 3 * 8)
-    launch_q<kBf16, 128, 3>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q<kBf16, 128, 3, kStatic>(a, st);
   else if (K <= 128 * 5 * 8)
-    launch_q<kBf16, 128, 5>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q<kBf16, 128, 5, kStatic>(a, st);
   else if (K <= 256 * 5 * 8)
-    launch_q<kBf16, 256, 5>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q<kBf16, 256, 5, kStatic>(a, st);
   else if (K <= 256 * 9 * 8)
-    launch_q<kBf16, 256, 9>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q<kBf16, 256, 9, kStatic>(a, st);
   else
-    launch_q<kBf16, 512, 9>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q<kBf16, 512, 9, kStatic>(a, st);
 }
 
 cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
                                 int8_t* q, float* scale, int32_t* bsum, uint16_t* q16,
                                 cudaStream_t st) {
+  const QArgs a{x, M, K, ldx, q, scale, bsum, q16, nullptr, 0};
   if (bf16)
-    launch_q_k<true>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q_k<true, false>(a, st);
   else
-    launch_q_k<false>(x, M, K, ldx, q, scale, bsum, q16, st);
+    launch_q_k<false, false>(a, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_act_static(const void* x, bool bf16, int64_t M, int64_t K,
+                                       int64_t ldx, const float* s_in, int64_t s_stride,
+                                       int8_t* q, int32_t* bsum, uint16_t* q16,
+                                       cudaStream_t st) {
+  const QArgs a{x, M, K, ldx, q, nullptr, bsum, q16, s_in, s_stride};
+  if (bf16)
+    launch_q_k<true, true>(a, st);
+  else
+    launch_q_k<false, true>(a, st);
   return cudaGetLastError();
 }
 

@@ -102,6 +102,22 @@ qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
                           void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Activation quantization with given scales (ranges calibrated once and     */
+/* cached, as the StartLux-Prism README's engine does at its first start,    */
+/* "Quick start"; the calibration itself is the caller's).                   */
+/*   row m uses s = scale[m * scale_stride] (scale_stride 1: per row, [M];    */
+/*   0: one scale for every row, [1]);                                        */
+/*   q = clamp(rint(x / s), -127, 127), IEEE division, ties to even; values  */
+/*   beyond the calibrated range saturate; s == 0 gives q = 0.               */
+/* x, q, block_sums, q16 as for qg_quantize_act (block_sums 16-byte aligned).*/
+/* The GEMMs take the same scale array as their activation scale ([M]; pass  */
+/* a per-row array when the calibration is per tensor).                      */
+/* ------------------------------------------------------------------------ */
+qg_status qg_quantize_act_static(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                                 int64_t ldx, const float* scale, int64_t scale_stride, int8_t* q,
+                                 int32_t* block_sums, uint16_t* q16, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Q8_0 weights (W8A8).                                                      */
 /* Input format: the weight matrix W [N][K] as N*K/32 blocks of 34 bytes,    */
 /* row-major over (n, b): {fp16 d (little endian); int8 q[32]}, weight =     */

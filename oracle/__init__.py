@@ -45,6 +45,7 @@ def lib():
         L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_bf16_to_f32.restype = ctypes.c_float
         L.orc_quantize_act.argtypes = [P, I, I64, I64, P, P, P]
+        L.orc_quantize_act_static.argtypes = [P, I, I64, I64, P, I64, P, P]
         L.orc_gemm_w8a8_q8_0.argtypes = [P, P, I64, I64, P, I64, P, P]
         L.orc_block_sums_q8_0.argtypes = [P, I64, I64, P, I64, P]
         L.orc_q4k_decode.argtypes = [P, P, P, P, P, P, P]
@@ -91,6 +92,25 @@ def quantize_act(x, bsum=False):
     bs = np.empty((M, K // 32), np.int32) if bsum else None
     lib().orc_quantize_act(_p(x), is_bf16, M, K, _p(q), _p(s), _p(bs))
     return (q, s, bs) if bsum else (q, s)
+
+
+def quantize_act_static(x, scale, bsum=False):
+    """x: float32 [M,K] or uint16 bf16 bits; scale: float32 [M] (per row) or [1]
+    (one for all rows) -> (q int8[, bsum int32])."""
+    if x.dtype == np.uint16:
+        is_bf16 = 1
+    else:
+        x = x.astype(np.float32, copy=False)
+        is_bf16 = 0
+    x = np.ascontiguousarray(x)
+    M, K = x.shape
+    scale = _c(np.atleast_1d(scale).astype(np.float32), np.float32)
+    stride = 0 if scale.shape[0] == 1 else 1
+    assert stride == 0 or scale.shape[0] == M
+    q = np.empty((M, K), np.int8)
+    bs = np.empty((M, K // 32), np.int32) if bsum else None
+    lib().orc_quantize_act_static(_p(x), is_bf16, M, K, _p(scale), stride, _p(q), _p(bs))
+    return (q, bs) if bsum else q
 
 
 def gemm_w8a8_q8_0(qa, sa, blocks):

@@ -103,6 +103,33 @@ void orc_quantize_act(const void* x, int x_is_bf16, int64_t M, int64_t K,
   }
 }
 
+void orc_quantize_act_static(const void* x, int x_is_bf16, int64_t M, int64_t K,
+                             const float* s_in, int64_t s_stride, int8_t* q, int32_t* bsum) {
+  for (int64_t m = 0; m < M; ++m) {
+    float scale = s_in[m * s_stride];
+    for (int64_t k = 0; k < K; ++k) {
+      float v = x_is_bf16 ? orc_bf16_to_f32(((const uint16_t*)x)[m * K + k])
+                          : ((const float*)x)[m * K + k];
+      int qi = 0;
+      if (scale != 0.0f) {
+        float r = rintf(v / scale);           /* IEEE division, then ties-to-even */
+        if (r > 127.0f) r = 127.0f;           /* saturate outside the calibrated range */
+        if (r < -127.0f) r = -127.0f;
+        qi = (int)r;
+      }
+      q[m * K + k] = (int8_t)qi;
+    }
+    if (bsum) {
+      int64_t B = K / QBLK;
+      for (int64_t b = 0; b < B; ++b) {
+        int32_t acc = 0;
+        for (int j = 0; j < QBLK; ++j) acc += q[m * K + b * QBLK + j];
+        bsum[m * B + b] = acc;
+      }
+    }
+  }
+}
+
 /* ---------------------------------------------------------------------- */
 /* W8A8, Q8_0 weights                                                      */
 /* ---------------------------------------------------------------------- */

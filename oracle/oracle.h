@@ -62,6 +62,13 @@ float orc_bf16_to_f32(uint16_t b);
 void orc_quantize_act(const void* x, int x_is_bf16, int64_t M, int64_t K,
                       int8_t* q, float* s, int32_t* bsum);
 
+/* Activation quantization with given (calibrated) scales: row m uses
+ * s = s_in[m * s_stride] (s_stride 0: one scale for every row);
+ * q = clamp(rint(x / s), -127, 127) with the correctly rounded division,
+ * q = 0 when s == 0. Values beyond the calibrated range saturate. */
+void orc_quantize_act_static(const void* x, int x_is_bf16, int64_t M, int64_t K,
+                             const float* s_in, int64_t s_stride, int8_t* q, int32_t* bsum);
+
 /* W8A8 with Q8_0 weights.
  * qa: [M][K] int8, sa: [M] fp32, blocks: [N][K/32] x 34 bytes.
  * y: [M][N] fp32 out (the value before bf16 rounding) or NULL;

@@ -28,9 +28,9 @@ def _kv(text, conv):
     return out
 
 
-def quantize_cases():
+def quantize_cases(name="quantize_ties.txt"):
     cases, cur = [], None
-    for line in _lines("quantize_ties.txt"):
+    for line in _lines(name):
         key, _, rest = line.partition(":") if not line.startswith("row ") else ("row", None, line[4:])
         if key == "row":
             cur = {"name": rest.strip()}

@@ -21,7 +21,7 @@ def L():
 
 def test_exports_every_declared_symbol(L):
     names = _lib.declared_symbols()
-    assert len(names) >= 17
+    assert len(names) >= 18
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.SO_PATH], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -102,3 +102,11 @@ def test_binding_raises_without_gpu_work(L):
 def test_timeout_probe_validation(L):
     assert L.qg_debug_wait_timeout(0, None) == _lib.QG_EINVAL
     assert L.qg_debug_wait_timeout((1 << 20) + 1, None) == _lib.QG_EINVAL
+
+
+def test_static_quantize_validation(L):
+    qs = L.qg_quantize_act_static
+    assert qs(P(FAKE), 0, 4, 64, 64, None, 1, P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qs(P(FAKE), 0, 4, 64, 64, P(FAKE), 2, P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qs(P(FAKE), 0, 4, 48, 48, P(FAKE), 1, P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qs(P(FAKE), 0, 4, 64, 64, P(FAKE), 1, P(FAKE), P(FAKE + 4), None, None) == _lib.QG_EALIGN

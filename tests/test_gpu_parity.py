@@ -317,3 +317,31 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     oq, os_ = oracle.quantize_act(bits)
     _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
     assert np.array_equal(out_bits(out), ob)
+
+
+@pytest.mark.parametrize("M,K,per_row", [(5, 256, True), (37, 2560, False), (16, 17408, True),
+                                         (300, 640, False)])
+def test_static_quantize_matches_oracle(M, K, per_row):
+    """Static (calibrated) scales: saturating int8, block sums and fp16 copy
+    bit-exact against the oracle; the W8A8 GEMM on them as well."""
+    x, bits = synth.activations(M + K + 3, M, K, dtype="bf16", outlier_frac=0.02)
+    rng = np.random.default_rng(M)
+    am = np.abs(x).max(axis=1).astype(np.float32)
+    # calibrated scales between 0.25x and 1.5x of the row's own absmax/127 (so some rows saturate)
+    s = (am / np.float32(127) * rng.uniform(0.25, 1.5, size=M).astype(np.float32)).astype(np.float32)
+    s[0] = 0.0
+    if not per_row:
+        s = s[1:2].copy()
+    sd = to_dev(s)
+    q, bs, h = qg.quantize_act_static(bf16_dev(bits), sd, block_sums=True, q16=True)
+    oq, obs = oracle.quantize_act_static(bits, s, bsum=True)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(bs.cpu().numpy(), obs)
+    assert np.array_equal(h.float().cpu().numpy(), oq.astype(np.float32))
+    N = 96
+    blocks = synth.q8_0_weights(K + 1, N, K)
+    srow = s if per_row else np.full(M, s[0], np.float32)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    out = qg.gemm_w8a8_q8_0(q, h, to_dev(srow), packed, N)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, srow, blocks)
+    assert np.array_equal(out_bits(out), ob)

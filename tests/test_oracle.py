@@ -353,3 +353,40 @@ def test_gemm_q4k_batch_invariance():
     qn, sn = oracle.quantize_act(-x)
     yn, _ = oracle.gemm_w4a8_q4k(qn, sn, sblocks)
     assert np.array_equal(yn, -y)
+
+
+# ----------------------------------------------------------------- static scales
+@pytest.mark.parametrize("case", golden_io.quantize_cases("quantize_static.txt"), ids=lambda c: c["name"])
+def test_quantize_static_golden(case):
+    x = np.zeros((1, 32), np.float32)
+    for k, v in case["x"].items():
+        x[0, k] = v
+    q, bs = oracle.quantize_act_static(x, np.array([case["s"]], np.float32), bsum=True)
+    exp = np.zeros(32, np.int8)
+    for k, v in case["q"].items():
+        exp[k] = v
+    assert np.array_equal(q[0], exp)
+    assert bs[0, 0] == case["bsum"][0]
+
+
+def test_quantize_static_with_dynamic_scale_equals_dynamic():
+    """Given the dynamic per-row scale, the static quantizer reproduces the
+    dynamic one bit for bit (a separate code path reaching the same result)."""
+    x, bits = synth.activations(23, 29, 384, dtype="bf16", outlier_frac=0.02)
+    q, s, bs = oracle.quantize_act(bits, bsum=True)
+    q2, bs2 = oracle.quantize_act_static(bits, s, bsum=True)
+    assert np.array_equal(q, q2) and np.array_equal(bs, bs2)
+
+
+def test_quantize_static_saturates_and_is_row_independent():
+    x, _ = synth.activations(24, 12, 256, dtype="f32", outlier_frac=0.05)
+    s_tensor = np.array([np.float32(np.abs(x).max() / 127 / 8)], np.float32)  # 8x too small
+    q = oracle.quantize_act_static(x, s_tensor)
+    assert np.abs(q.astype(np.int32)).max() == 127
+    big = np.abs(x / s_tensor[0]) >= 127.5
+    assert np.all(np.abs(q[big]) == 127)
+    # per-row scales equal to the tensor scale give the same q
+    q_rows = oracle.quantize_act_static(x, np.full(12, s_tensor[0], np.float32))
+    assert np.array_equal(q, q_rows)
+    # sign symmetry
+    assert np.array_equal(oracle.quantize_act_static(-x, s_tensor), -q)
