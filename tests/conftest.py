@@ -13,4 +13,4 @@ if TESTS not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size workload (GPU)")
+    config.addinivalue_line("markers", "slow: full-size workload (GPU, about a minute)")
