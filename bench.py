@@ -498,6 +498,9 @@ def main():
         torch.cuda.empty_cache()
         rows = bench_rows(dev, flush, hbm, tf_burst, quick=True)
 
+    # one quantize launch per projection, plus the GEMM's own launches (the
+    # prefill GEMM splits a ragged last wave into a second, narrow-tile launch)
+    launches_per_step = sum(1 + qg.gemm_launch_count("q8_0", M, K, N) for (M, K, N) in STEP_SHAPES)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline()
@@ -511,7 +514,7 @@ def main():
                            "parallelism": "replicas" if world > 1 else "single",
                            "l2": "flushed between timed steps (512 MiB write, outside events)",
                            "wall_s": round(t_wall, 3)},
-                "gpu_launches": 2 * len(STEP_SHAPES) * args.steps,
+                "gpu_launches": launches_per_step * args.steps,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "rows": rows}
         print(json.dumps(line))

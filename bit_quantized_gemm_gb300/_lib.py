@@ -57,6 +57,7 @@ def load():
         "qg_debug_block_sums_q8_0": ([P, P, I64, I64, P, I64, P, I, P], I),
         "qg_debug_block_sums_q4k": ([P, P, I64, I64, P, I64, P, I, P], I),
         "qg_debug_wait_timeout": ([ctypes.c_uint32, P], I),
+        "qg_gemm_launch_count": ([I, I64, I64, I64, I], I),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -200,6 +201,11 @@ def debug_wait_timeout(polls, stream=None):
 
 def check_device_error(stream=None):
     _check(load().qg_check_device_error(_stream(stream)))
+
+
+def gemm_launch_count(kind, M, K, N, path="auto"):
+    """Kernel launches one GEMM call of these sizes makes (kind "q8_0" or "q4k")."""
+    return int(load().qg_gemm_launch_count(0 if kind == "q8_0" else 1, M, K, N, PATHS[path]))
 
 
 def small_m_max():

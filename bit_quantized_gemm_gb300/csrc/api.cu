@@ -29,6 +29,7 @@ cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* 
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
+int prefill_launches_q8_0(int64_t M, int64_t N);
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
                                bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err,
@@ -147,6 +148,16 @@ const char* qg_status_string(qg_status s) {
 const char* qg_last_error(void) { return t_last_error; }
 int qg_version(void) { return kVersion; }
 int64_t qg_small_m_max(void) { return kSmallMMax; }
+
+int qg_gemm_launch_count(int weights_kind, int64_t M, int64_t K, int64_t N, qg_path path) {
+  if (weights_kind != 0 && weights_kind != 1) return 0;
+  if (M < 1 || M > kMaxM || N < 1 || N > kMaxN) return 0;
+  if (check_k(K, weights_kind ? kQ4kWeights : kBlk) != QG_OK) return 0;
+  if (path != QG_PATH_AUTO && path != QG_PATH_SMALL && path != QG_PATH_LARGE) return 0;
+  const bool large = (path == QG_PATH_LARGE) || (path == QG_PATH_AUTO && M > kSmallMMax);
+  if (!large) return (int)ceil_div(M, kDecodeRows);
+  return weights_kind ? 1 : prefill_launches_q8_0(M, N);
+}
 
 qg_status qg_check_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

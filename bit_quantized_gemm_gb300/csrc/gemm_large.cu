@@ -15,22 +15,30 @@
 // one FMA per (row, token, block), in block order -- the same chain as the
 // decode kernel, so both paths give identical bits.
 //
-// Tile: 128 weight rows (MMA M, tensor-memory lanes) x 256 tokens (MMA N,
-// tensor-memory columns), K staged 64 at a time (two blocks) through a
-// 4-deep TMA ring with 128-byte swizzle. Two 256-column accumulators
-// alternate per block (512 columns, all of tensor memory), so the MMA of
-// block b+1 overlaps the epilogue of block b.
-// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+// Tile: 128 weight rows (MMA M, tensor-memory lanes) x BM tokens (MMA N,
+// tensor-memory columns; BM = 256 for W8A8, 128 for W4A8), K staged 64 at a
+// time (two blocks) through a 4-deep TMA ring with 128-byte swizzle. Block b of
+// a tile accumulates in buffer b % kTBufs (two 256-column buffers at BM = 256:
+// all 512 columns), so the MMA of block b+1 overlaps the epilogue of block b.
+// Warp roles (352 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (lane 0); for W4A8 the whole warp also converts
 //               the activation block sums of each block into a float ring
-//   warps 1, 2  MMA issuers (lane 0): warp 1 the even blocks of each tile into
-//               accumulator 0, warp 2 the odd blocks into accumulator 1 --
-//               two issuers, so that one's barrier latencies overlap the
-//               other's work; warp 1 also allocates tensor memory
+//   warps 1, 2  MMA issuers (lane 0): warp 1 the even blocks of each tile,
+//               warp 2 the odd ones -- two issuers, so that one's barrier
+//               latencies overlap the other's work; warp 1 also allocates
+//               tensor memory
 //   warps 3..10 epilogue: warp w reads lanes 32*(w%4).. of tensor memory and
 //               half (w-3)/4 of the token columns; each thread keeps its fp32
 //               accumulators (one weight row x its tokens) in registers and
-//               applies acc = fma(isum, d, acc) with packed f32x2 FMAs.
+//               applies acc = fma(isum, d, acc) with packed f32x2 FMAs. Each
+//               thread hands its part of a buffer back itself, as soon as its
+//               loads are done (no warp-wide operation on this path).
+//
+// Waves: a GEMM whose 256-token tiles leave the last wave of SMs mostly idle
+// runs as two launches -- the weight-row tiles that fill whole waves with
+// 256-token tiles, and the remaining rows over all tokens as narrow tiles
+// (32..128 tokens) spread over the SMs. Every output element still gets its
+// whole K chain from one thread, so the split changes no bit.
 #include <cuda.h>
 
 #include "qg_common.cuh"
@@ -45,6 +53,18 @@ namespace qg {
 #endif
 #ifndef QG_EPI_WARPS
 #define QG_EPI_WARPS 8
+#endif
+#ifndef QG_FORCE_BM
+#define QG_FORCE_BM 0  // tuning: nonzero runs every W8A8 GEMM as one launch of this width
+#endif
+#ifndef QG_BM_W4A8
+#define QG_BM_W4A8 128
+#endif
+#ifndef QG_EPI_BATCH
+#define QG_EPI_BATCH 0  // loads per wait; 0: all chunks of a block up to 64 columns, else 1
+#endif
+#ifndef QG_CHUNK
+#define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
 #endif
 constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 64;       // K per stage
@@ -62,11 +82,14 @@ constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
 // the register room of BM = 128.
 template <int BM>
 struct LargeCfg {
-  static_assert(BM % 16 == 0 && BM >= 64 && BM <= 256 && kTmemCols % BM == 0, "tile width");
+  static_assert(BM % 16 == 0 && BM >= 32 && BM <= 256 && kTmemCols % BM == 0, "tile width");
   static constexpr int kBM = BM;
-  static constexpr int kTBufs = kTmemCols / BM;  // per-block accumulators filling this CTA's tensor memory
+  // per-block accumulators in this CTA's tensor memory (at most 8)
+  static constexpr int kTBufs = kTmemCols / BM < 8 ? kTmemCols / BM : 8;
   static constexpr uint32_t kStageBBytes = BM * kBK * 2;
   static constexpr int kColsPerThread = BM / (kEpiWarps / 4);
+  static_assert(kColsPerThread % 16 == 0, "whole 16-column tensor-memory loads per thread");
+  static constexpr int kChunk = QG_CHUNK < kColsPerThread ? QG_CHUNK : kColsPerThread;
 };
 
 template <int BM>
@@ -83,17 +106,6 @@ template <int BM>
 constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<BM>) + 1024; }  // + alignment slack
 static_assert(kStageABytes % 1024 == 0, "1024-B aligned stages");
 
-#ifndef QG_BM_W8A8
-#define QG_BM_W8A8 256
-#endif
-#ifndef QG_BM_W4A8
-#define QG_BM_W4A8 128
-#endif
-#ifndef QG_EPI_BATCH
-#define QG_EPI_BATCH 1
-#endif
-template <bool kQ4K>
-__host__ __device__ constexpr int bm_for() { return kQ4K ? QG_BM_W4A8 : QG_BM_W8A8; }
 
 struct LargeArgs {
   const float* d32;      // W8A8: [N][ldd] fp32 scales; W4A8: d*sc [N][ldd]
@@ -122,11 +134,10 @@ __device__ __forceinline__ void tile_coords(int tile, int MT, int NT, int& mt, i
   nt = idx / gm;
 }
 
-template <bool kQ4K, bool kDebug>
+template <bool kQ4K, bool kDebug, int BM>
 __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const LargeArgs args) {
-  constexpr int BM = bm_for<kQ4K>();
   using C = LargeCfg<BM>;
   constexpr int kBM = C::kBM;
   constexpr int kTBufs = C::kTBufs;
@@ -149,11 +160,11 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     }
     for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpiWarps);
+      mbar_init(&S.tempty[i], kEpiWarps * 32);  // every epilogue thread hands back its loads
     }
     for (int i = 0; i < kAsumRing; ++i) {
       mbar_init(&S.afull[i], 32);
-      mbar_init(&S.aempty[i], kEpiWarps);
+      mbar_init(&S.aempty[i], kEpiWarps * 32);
     }
     fence_barrier_init();
   }
@@ -220,33 +231,37 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // issuer `par` handles block 2s+par of every stage s, in accumulator `par`
+    // issuer `par` handles block 2s+par of every stage s; block b of a tile
+    // accumulates in buffer b % kTBufs, so each issuer owns kTBufs/2 buffers
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBN, kBM);
-      static_assert(kTBufs >= 2, "two accumulators");
+      static_assert(kTBufs >= 2 && kTBufs % 2 == 0, "accumulators split between two issuers");
       const int par = warp - 1;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t tphase = 0;
+      uint32_t tph = 0;  // bit b: phase of the next wait on tempty[b]
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         for (int s = 0; s < NS && ok; ++s) {
-          if (2 * s + par < NB) {
+          const int blk = 2 * s + par;
+          if (blk < NB) {
+            const int tb = blk % kTBufs;
+            const uint32_t tpar = ((tph >> tb) & 1u) ^ 1u;
             ok = mbar_wait(&S.full[stage], phase, args.err);
-            if (ok) ok = mbar_wait(&S.tempty[par], tphase ^ 1, args.err);
+            if (ok) ok = mbar_wait(&S.tempty[tb], tpar, args.err);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(S.a[stage]);
             const uint32_t b_addr = smem_u32(S.b[stage]);
-            const uint32_t d_tmem = tmem_base + (uint32_t)(par * kBM);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(tb * kBM);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
               const uint32_t koff = (uint32_t)((par * 32 + kk * 16) * 2);  // bytes within row
               mma_f16_ss(d_tmem, smem_desc_sw128(a_addr + koff), smem_desc_sw128(b_addr + koff),
                          idesc, kk);
             }
-            mma_commit(&S.tfull[par]);
-            tphase ^= 1;
+            mma_commit(&S.tfull[tb]);
+            tph ^= 1u << tb;
           }
           mma_commit(&S.empty[stage]);  // arrives once this issuer's MMAs are done
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int half = (warp - kFirstEpiWarp) >> 2;
-    uint32_t tphases = 0;  // bit b: phase of accumulator b
+    uint32_t tph = 0;  // bit b: phase of the next wait on tfull[b]
     int aslot = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -287,26 +302,36 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           d_next = ldg_f32_pinned(drow + blk + 1);
           if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
         }
-        const int tb = blk & 1;  // accumulator of this block (issuer blk % 2)
-        ok = mbar_wait(&S.tfull[tb], (tphases >> tb) & 1u, args.err);
+        const int tb = blk % kTBufs;
+        // `ok` is uniform across the warp without a vote: every lane runs the
+        // same polling loop on the same barrier and sees the same answers (a
+        // per-block warp vote or shuffle here costs about 9 % of the time)
+        ok = mbar_wait(&S.tfull[tb], (tph >> tb) & 1u, args.err);
         if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
         if (!ok) break;
+        tph ^= 1u << tb;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(tb * kBM + half * kColsPerThread);
         const float2 dw2 = make_float2(dw, dw);
         const float2 ndm2 = make_float2(ndm, ndm);
-        constexpr int kChunk = 16;  // columns per tensor-memory load
+        constexpr int kChunk = C::kChunk;  // columns per tensor-memory load
         constexpr int kNch = kColsPerThread / kChunk;
         // kBatch loads are issued before one wait, so the tensor-memory load
         // latency is paid once per batch instead of once per chunk
-        constexpr int kBatch = QG_EPI_BATCH < kNch ? QG_EPI_BATCH : kNch;
+        constexpr int kBatchCfg = QG_EPI_BATCH ? QG_EPI_BATCH : (kColsPerThread <= 64 ? kNch : 1);
+        constexpr int kBatch = kBatchCfg > kNch ? kNch : kBatchCfg;
         static_assert(kNch % kBatch == 0, "batch must divide the chunks");
 #pragma unroll
         for (int c0 = 0; c0 < kNch; c0 += kBatch) {
           uint32_t v[kBatch][kChunk];
 #pragma unroll
-          for (int b = 0; b < kBatch; ++b) tmem_ld16(taddr + (c0 + b) * kChunk, v[b]);
+          for (int b = 0; b < kBatch; ++b) {
+            if constexpr (kChunk == 32)
+              tmem_ld32(taddr + (c0 + b) * kChunk, v[b]);
+            else
+              tmem_ld16(taddr + (c0 + b) * kChunk, v[b]);
+          }
           tmem_wait_ld();
           // pin the loaded registers after the wait: no use may move above it
 #pragma unroll
@@ -314,10 +339,10 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) asm volatile("" : "+r"(v[b][i]));
           if (c0 + kBatch == kNch) {
-            // all of this block's columns are in registers: hand the buffer back
+            // all of this thread's columns of the block are in registers:
+            // each thread hands its part of the buffer back (no warp sync)
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.tempty[tb]);
+            mbar_arrive(&S.tempty[tb]);
           }
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
@@ -347,11 +372,9 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           }
         }
         if (kQ4K) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.aempty[aslot]);
+          mbar_arrive(&S.aempty[aslot]);  // this thread's reads of the slot are done
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
-        tphases ^= 1u << tb;
       }
       if (!ok || kDebug) continue;
       // final scale by the activation scale and store out[m][n]
@@ -426,12 +449,13 @@ static int num_sms() {
   return n;
 }
 
-template <bool kQ4K, bool kDebug>
-static cudaError_t launch_prefill_t(const CUtensorMap& ta, const CUtensorMap& tb,
-                                   const LargeArgs& a, cudaStream_t st) {
-  constexpr int BM = bm_for<kQ4K>();
+template <bool kQ4K, bool kDebug, int BM>
+static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, const LargeArgs& a,
+                                   cudaStream_t st) {
   constexpr size_t kSmem = large_smem_bytes<BM>();
-  auto kern = prefill_gemm_kernel<kQ4K, kDebug>;
+  CUtensorMap tb;
+  if (!make_tmap(&tb, q16, a.M, a.K, BM)) return cudaErrorNotSupported;
+  auto kern = prefill_gemm_kernel<kQ4K, kDebug, BM>;
   static bool configured = false;  // once per process (idempotent if raced)
   if (!configured) {
     cudaError_t e =
@@ -446,16 +470,54 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const CUtensorMap& tb
   return cudaGetLastError();
 }
 
+// Relative cost of one 32-block step of one tile at tile width BM (a 256-wide
+// step = 1): the epilogue's fixed per-step work (barrier waits, tensor-memory
+// hand-back, loop) does not shrink with the width, so narrow tiles cost more
+// per token but fill the SMs that a ragged last wave of wide tiles leaves idle.
+static double step_cost(int bm) {
+  switch (bm) {
+    case 256: return 1.0;
+    case 128: return 0.70;
+    case 64: return 0.56;
+    default: return 0.52;  // 32
+  }
+}
+
+// Wave plan of a W8A8 prefill GEMM: the weight-row tiles [0, nt_wide) run as
+// 256-token tiles, the rest (all tokens) as bm_tail-token tiles in a second
+// launch, when that shortens the estimated time (nt_wide = NT: one launch).
+struct PrefillPlan {
+  int nt_wide;
+  int bm_tail;
+};
+static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
+  const int64_t NT = ceil_div(N, kBN), MT = ceil_div(M, 256);
+  auto waves = [&](int64_t tiles) { return (double)ceil_div(tiles, (int64_t)sms); };
+  PrefillPlan best{(int)NT, 256};
+  double best_t = waves(MT * NT) * step_cost(256);
+  const int64_t nt_wide = (sms * (MT * NT / sms)) / MT;  // weight-row tiles that fill whole waves
+  for (int64_t nw = nt_wide; nw >= 0 && nw >= nt_wide - 1; --nw) {
+    for (int bm : {128, 64, 32}) {
+      const double t = (nw ? waves(MT * nw) * step_cost(256) : 0.0) +
+                       waves(ceil_div(M, (int64_t)bm) * (NT - nw)) * step_cost(bm);
+      if (t < best_t * 0.97) { best_t = t; best = PrefillPlan{(int)nw, bm}; }
+    }
+  }
+  return best;
+}
+
+int prefill_launches_q8_0(int64_t M, int64_t N) {
+  const PrefillPlan p = QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM}
+                                    : plan_prefill_w8a8(M, N, num_sms());
+  return (p.nt_wide > 0 && (int64_t)p.nt_wide * kBN < N) ? 2 : 1;
+}
+
 // returns cudaErrorNotSupported when the tensor-map encoder is unavailable
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
   const Q8Layout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
-  CUtensorMap ta, tb;
-  constexpr int BM = bm_for<false>();
-  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, BM))
-    return cudaErrorNotSupported;
   LargeArgs a{};
   a.d32 = reinterpret_cast<const float*>(base + L.off_d32);
   a.ldd = L.B4;
@@ -466,8 +528,35 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   a.out_f32 = out_f32 ? 1 : 0;
   a.dbg = dbg;
   a.err = err;
-  return dbg ? launch_prefill_t<false, true>(ta, tb, a, st)
-             : launch_prefill_t<false, false>(ta, tb, a, st);
+  const uint8_t* wq16 = base + L.off_q16;  // fp16 weights [N][K]
+  CUtensorMap ta;
+  if (dbg) {  // exported block sums: one launch of 256-token tiles
+    if (!make_tmap(&ta, wq16, N, K, kBN)) return cudaErrorNotSupported;
+    return launch_prefill_t<false, true, 256>(ta, q16, a, st);
+  }
+  const PrefillPlan p =
+      QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM} : plan_prefill_w8a8(M, N, num_sms());
+  const int64_t n0 = (int64_t)p.nt_wide * kBN;  // first weight row of the narrow part
+  if (n0 > 0) {
+    LargeArgs aw = a;
+    aw.N = (int)(n0 < N ? n0 : N);
+    if (!make_tmap(&ta, wq16, aw.N, K, kBN)) return cudaErrorNotSupported;
+    const cudaError_t e = launch_prefill_t<false, false, 256>(ta, q16, aw, st);
+    if (e != cudaSuccess || n0 >= N) return e;
+  }
+  // weight rows [n0, N) over all tokens, as narrow tiles
+  LargeArgs an = a;
+  an.N = (int)(N - n0);
+  an.d32 = a.d32 + n0 * a.ldd;
+  an.out = out_f32 ? (void*)(reinterpret_cast<float*>(out) + n0)
+                   : (void*)(reinterpret_cast<uint16_t*>(out) + n0);
+  if (!make_tmap(&ta, wq16 + n0 * K * 2, an.N, K, kBN)) return cudaErrorNotSupported;
+  switch (p.bm_tail) {
+    case 128: return launch_prefill_t<false, false, 128>(ta, q16, an, st);
+    case 64: return launch_prefill_t<false, false, 64>(ta, q16, an, st);
+    case 32: return launch_prefill_t<false, false, 32>(ta, q16, an, st);
+    default: return launch_prefill_t<false, false, 256>(ta, q16, an, st);
+  }
 }
 
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
@@ -476,10 +565,8 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
                                cudaStream_t st) {
   const Q4kLayout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
-  CUtensorMap ta, tb;
-  constexpr int BM = bm_for<true>();
-  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN) || !make_tmap(&tb, q16, M, K, BM))
-    return cudaErrorNotSupported;
+  CUtensorMap ta;
+  if (!make_tmap(&ta, base + L.off_q16, N, K, kBN)) return cudaErrorNotSupported;
   LargeArgs a{};
   a.d32 = reinterpret_cast<const float*>(base + L.off_ds32);
   a.dm32 = reinterpret_cast<const float*>(base + L.off_dm32);
@@ -492,8 +579,9 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.out_f32 = out_f32 ? 1 : 0;
   a.dbg = dbg;
   a.err = err;
-  return dbg ? launch_prefill_t<true, true>(ta, tb, a, st)
-             : launch_prefill_t<true, false>(ta, tb, a, st);
+  constexpr int BM = QG_BM_W4A8;
+  return dbg ? launch_prefill_t<true, true, BM>(ta, q16, a, st)
+             : launch_prefill_t<true, false, BM>(ta, q16, a, st);
 }
 
 }  // namespace qg

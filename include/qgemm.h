@@ -82,6 +82,14 @@ int64_t qg_small_m_max(void);
 /* Synchronizes `stream`, then reads and clears the device error word of the
  * current device: QG_OK, or QG_ETIMEOUT if a bounded wait gave up. */
 qg_status qg_check_device_error(void* stream);
+/* Number of kernel launches one qg_gemm_w8a8_q8_0(_ex) (weights_kind 0) or
+ * qg_gemm_w4a8_q4k(_ex) (weights_kind 1) call with these sizes and path
+ * makes on the current device: the decode kernel takes up to 16 rows per
+ * launch; the prefill kernel runs as one launch, or, for W8A8 shapes whose
+ * last wave of 256-token tiles would leave most SMs idle, as two (the rows
+ * that fill whole waves, then the rest as narrow tiles). 0 if the sizes or
+ * the path are invalid. Host-only: launches nothing; reads the SM count. */
+int qg_gemm_launch_count(int weights_kind, int64_t M, int64_t K, int64_t N, qg_path path);
 
 /* ------------------------------------------------------------------------ */
 /* Activation quantization (per token, dynamic absmax; see the definition    */

@@ -110,3 +110,16 @@ def test_static_quantize_validation(L):
     assert qs(P(FAKE), 0, 4, 64, 64, P(FAKE), 2, P(FAKE), None, None, None) == _lib.QG_EINVAL
     assert qs(P(FAKE), 0, 4, 48, 48, P(FAKE), 1, P(FAKE), None, None, None) == _lib.QG_EINVAL
     assert qs(P(FAKE), 0, 4, 64, 64, P(FAKE), 1, P(FAKE), P(FAKE + 4), None, None) == _lib.QG_EALIGN
+
+
+def test_gemm_launch_count_host_rules(L):
+    # the decode kernel takes up to 16 rows per launch; invalid requests give 0
+    assert qg.gemm_launch_count("q8_0", 1, 5120, 17408) == 1
+    assert qg.gemm_launch_count("q8_0", 16, 5120, 17408) == 1
+    assert qg.gemm_launch_count("q8_0", 40, 5120, 17408, path="small") == 3
+    assert qg.gemm_launch_count("q4k", 33, 5120, 17408, path="small") == 3
+    assert L.qg_gemm_launch_count(0, 0, 5120, 17408, 0) == 0
+    assert L.qg_gemm_launch_count(0, 8, 5100, 17408, 0) == 0      # K not a multiple of 32
+    assert L.qg_gemm_launch_count(1, 8, 4096 + 32, 17408, 0) == 0  # K not a multiple of 256
+    assert L.qg_gemm_launch_count(2, 8, 5120, 17408, 0) == 0
+    assert L.qg_gemm_launch_count(0, 8, 5120, 17408, 7) == 0

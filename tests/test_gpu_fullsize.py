@@ -142,3 +142,15 @@ def test_tiny_config():
     oq, os_ = oracle.quantize_act(x)
     _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
     assert np.array_equal(bits_of(out), ob)
+
+
+def test_launch_plan_of_the_benchmark_step():
+    # on 152 SMs the 4B down projection (160 tiles of 256 tokens) runs as one
+    # full wave of wide tiles plus a narrow-tile launch; gate/up fills 4 waves
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("plan figures are for 152 SMs")
+    assert qg.gemm_launch_count("q8_0", 2048, 2560, 9728) == 1
+    assert qg.gemm_launch_count("q8_0", 2048, 9728, 2560) == 2
+    assert qg.gemm_launch_count("q8_0", 8192, 5120, 17408) == 1
+    assert qg.gemm_launch_count("q4k", 4096, 5120, 17408) == 1
+    assert qg.gemm_launch_count("q8_0", 8, 5120, 17408) == 1
