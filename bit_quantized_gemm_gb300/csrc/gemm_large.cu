@@ -377,14 +377,26 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
         }
       }
       if (!ok || kDebug) continue;
-      // final scale by the activation scale and store out[m][n]
+      // final scale by the activation scale and store out[m][n]. The thread's
+      // kColsPerThread scales are fetched first, spread over the warp (lane l
+      // holds sa[mbase + 32j + l]) by coalesced loads, and broadcast by one
+      // shuffle per column, so no load waits behind a store to `out` (loading
+      // sa[m] inside the store loop serialized ~128 load latencies per tile)
       const int mbase = mt * kBM + half * kColsPerThread;
+      constexpr int kSv = (kColsPerThread + 31) / 32;
+      float sv[kSv];
+#pragma unroll
+      for (int j = 0; j < kSv; ++j) {
+        const int m = mbase + 32 * j + lane;
+        sv[j] = (32 * j + lane < kColsPerThread && m < M) ? __ldg(args.sa + m) : 0.0f;
+      }
 #pragma unroll
       for (int i = 0; i < kColsPerThread; ++i) {  // fully unrolled: acc stays in registers
         const int m = mbase + i;
+        const float sam = __shfl_sync(0xffffffffu, sv[i / 32], i % 32);
         if (m < M && nvalid) {
           const float a = (i & 1) ? acc[i / 2].y : acc[i / 2].x;
-          const float y = a * __ldg(args.sa + m);
+          const float y = a * sam;
           if (args.out_f32)
             reinterpret_cast<float*>(args.out)[(int64_t)m * args.ldo + n] = y;
           else
