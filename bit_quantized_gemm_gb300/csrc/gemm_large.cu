@@ -40,13 +40,20 @@
 // (32..128 tokens) spread over the SMs. Every output element still gets its
 // whole K chain from one thread, so the split changes no bit.
 #include <cuda.h>
+#include <cstring>
 
 #include "qg_common.cuh"
 
 namespace qg {
 
 #ifndef QG_STAGES
-#define QG_STAGES 4
+#define QG_STAGES 0  // TMA ring depth; 0: 3 stages at BM = 256 (room for output staging), else 4
+#endif
+#ifndef QG_OUT_CHUNK
+#define QG_OUT_CHUNK 128  // output columns per trip of the output loop (>= kColsPerThread: unrolled)
+#endif
+#ifndef QG_TMA_OUT
+#define QG_TMA_OUT 1  // bf16 outputs staged in shared memory and stored by TMA
 #endif
 #ifndef QG_CTAS_PER_SM
 #define QG_CTAS_PER_SM 1
@@ -68,7 +75,6 @@ namespace qg {
 #endif
 constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 64;       // K per stage
-constexpr int kStages = QG_STAGES;
 constexpr int kEpiWarps = QG_EPI_WARPS;  // multiple of 4 (tensor-memory lane quarters)
 constexpr int kFirstEpiWarp = 3;         // warp 0 producer, warps 1-2 MMA issuers
 constexpr int kLThreads = 32 * (kFirstEpiWarp + kEpiWarps);
@@ -89,21 +95,28 @@ struct LargeCfg {
   static constexpr uint32_t kStageBBytes = BM * kBK * 2;
   static constexpr int kColsPerThread = BM / (kEpiWarps / 4);
   static_assert(kColsPerThread % 16 == 0, "whole 16-column tensor-memory loads per thread");
+  static constexpr int kStages = QG_STAGES ? QG_STAGES : (BM == 256 ? 3 : 4);
   static constexpr int kChunk = QG_CHUNK < kColsPerThread ? QG_CHUNK : kColsPerThread;
 };
 
-template <int BM>
+template <bool kQ4K, int BM>
 struct LargeSmem {
+  static constexpr int kStages = LargeCfg<BM>::kStages;
+  static constexpr int kCols = LargeCfg<BM>::kColsPerThread;
   uint8_t a[kStages][kStageABytes];
   uint8_t b[kStages][LargeCfg<BM>::kStageBBytes];
-  float asum[kAsumRing][BM];
+  // bf16 output tile staged for the TMA store: per epilogue half, kCols token
+  // rows x 128 weight rows (row-major, the store's box)
+  uint16_t ostage[QG_TMA_OUT ? 2 : 1][QG_TMA_OUT ? kCols * kBN : 8];
+  float asum[kQ4K ? kAsumRing : 1][BM];
+  float sa_stage[kEpiWarps][kCols];  // per epilogue warp: its tile's activation scales
   uint64_t full[kStages], empty[kStages];
   uint64_t tfull[LargeCfg<BM>::kTBufs], tempty[LargeCfg<BM>::kTBufs];
   uint64_t afull[kAsumRing], aempty[kAsumRing];
   uint32_t tmem_base;
 };
-template <int BM>
-constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<BM>) + 1024; }  // + alignment slack
+template <bool kQ4K, int BM>
+constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<kQ4K, BM>) + 1024; }  // + alignment slack
 static_assert(kStageABytes % 1024 == 0, "1024-B aligned stages");
 
 
@@ -117,6 +130,7 @@ struct LargeArgs {
   int64_t ldd;
   int M, N, K;
   int out_f32;
+  int tma_out;           // 1: bf16 outputs leave through the TMA store (tmO)
   int32_t* dbg;          // [M][N][B] isum export (debug) or null
   uint32_t* err;
 };
@@ -137,14 +151,16 @@ __device__ __forceinline__ void tile_coords(int tile, int MT, int NT, int& mt, i
 template <bool kQ4K, bool kDebug, int BM>
 __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const LargeArgs args) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO, const LargeArgs args) {
   using C = LargeCfg<BM>;
+  constexpr int kStages = C::kStages;
   constexpr int kBM = C::kBM;
   constexpr int kTBufs = C::kTBufs;
   constexpr uint32_t kStageBBytes = C::kStageBBytes;
   constexpr int kColsPerThread = C::kColsPerThread;
   extern __shared__ uint8_t smem_raw[];
-  LargeSmem<BM>& S = *reinterpret_cast<LargeSmem<BM>*>(
+  LargeSmem<kQ4K, BM>& S = *reinterpret_cast<LargeSmem<kQ4K, BM>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = args.M, N = args.N, K = args.K;
@@ -274,6 +290,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     const int quarter = warp & 3;
     const int half = (warp - kFirstEpiWarp) >> 2;
     uint32_t tph = 0;  // bit b: phase of the next wait on tfull[b]
+    const bool ostore = args.tma_out && quarter == 0 && lane == 0;  // issues this half's stores
     int aslot = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -287,6 +304,23 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
       float2 acc[kColsPerThread / 2];
 #pragma unroll
       for (int i = 0; i < kColsPerThread / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+      // this tile's activation scales, copied to shared memory in the
+      // background for the output phase (its previous reader, the last
+      // tile's output phase, ended with a warp sync)
+      const int mbase = mt * kBM + half * kColsPerThread;
+      float* sw = S.sa_stage[warp - kFirstEpiWarp];
+      if (!kDebug) {
+#pragma unroll
+        for (int j = 0; j < (kColsPerThread + 31) / 32; ++j) {
+          const int c = 32 * j + lane, m = mbase + c;
+          if (c < kColsPerThread) {
+            if (m < M)
+              cp_async_4(sw + c, args.sa + m);
+            else
+              sw[c] = 0.0f;
+          }
+        }
+      }
 
       // the scales of block blk+1 are fetched while block blk is processed;
       // the load is volatile so the compiler keeps it a block ahead of its use
@@ -376,34 +410,81 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
       }
-      if (!ok || kDebug) continue;
-      // final scale by the activation scale and store out[m][n]. The thread's
-      // kColsPerThread scales are fetched first, spread over the warp (lane l
-      // holds sa[mbase + 32j + l]) by coalesced loads, and broadcast by one
-      // shuffle per column, so no load waits behind a store to `out` (loading
-      // sa[m] inside the store loop serialized ~128 load latencies per tile)
-      const int mbase = mt * kBM + half * kColsPerThread;
-      constexpr int kSv = (kColsPerThread + 31) / 32;
-      float sv[kSv];
-#pragma unroll
-      for (int j = 0; j < kSv; ++j) {
-        const int m = mbase + 32 * j + lane;
-        sv[j] = (32 * j + lane < kColsPerThread && m < M) ? __ldg(args.sa + m) : 0.0f;
+      if (kDebug) continue;
+      if (args.tma_out) {
+        // the store issued one tile ago must have read this half's staging
+        // buffer; the four warps of the half also agree on going on (a wait
+        // that gave up in one of them stops all four, none is left at a barrier)
+        if (ostore) bulk_wait_read_all();
+        ok = bar_and(1 + half, 128, ok);
       }
+      if (!ok) break;
+      // final scale by the activation scale. This code runs once per tile,
+      // cold in the instruction cache, so it is kept short: packed f32x2
+      // multiplies and bf16x2 conversions, scales read through restrict
+      // pointers (without them every scale load waited behind the previous
+      // output's store). A rolled variant (kCh < kColsPerThread: trips of kCh
+      // columns, accumulators slid down after each) measured slower.
+      cp_async_wait_all();
+      __syncwarp();
+      constexpr int kCh = kColsPerThread < QG_OUT_CHUNK ? kColsPerThread : QG_OUT_CHUNK;
+      const float* __restrict__ swr = sw;
+      if (args.tma_out) {
+        // bf16 outputs into this half's staging tile, then one thread stores
+        // it with TMA (rows >= M and columns >= N are clipped); the store
+        // drains while the next tile computes
+        __nv_bfloat16* __restrict__ ob =
+            reinterpret_cast<__nv_bfloat16*>(S.ostage[QG_TMA_OUT ? half : 0]) + quarter * 32 + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kColsPerThread; c0 += kCh) {
 #pragma unroll
-      for (int i = 0; i < kColsPerThread; ++i) {  // fully unrolled: acc stays in registers
-        const int m = mbase + i;
-        const float sam = __shfl_sync(0xffffffffu, sv[i / 32], i % 32);
-        if (m < M && nvalid) {
-          const float a = (i & 1) ? acc[i / 2].y : acc[i / 2].x;
-          const float y = a * sam;
-          if (args.out_f32)
-            reinterpret_cast<float*>(args.out)[(int64_t)m * args.ldo + n] = y;
-          else
-            reinterpret_cast<uint16_t*>(args.out)[(int64_t)m * args.ldo + n] = f32_to_bf16_rne(y);
+          for (int j = 0; j < kCh; j += 2) {
+            const float4 q = *reinterpret_cast<const float4*>(swr + c0 + (j & ~3));
+            const float2 y = __fmul2_rn(acc[j / 2], (j & 2) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);  // both RNE
+            ob[(c0 + j) * kBN] = h.x;
+            ob[(c0 + j + 1) * kBN] = h.y;
+          }
+#pragma unroll
+          for (int i = 0; i < (kColsPerThread - kCh) / 2; ++i) acc[i] = acc[i + kCh / 2];
+        }
+        fence_proxy_async_smem();
+        named_barrier(1 + half, 128);
+        if (ostore && mbase < M) {  // no store of a box wholly past M
+          tma_store_2d(&tmO, S.ostage[QG_TMA_OUT ? half : 0], nt * kBN, mbase);
+          bulk_commit_group();
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kColsPerThread; c0 += kCh) {
+#pragma unroll
+          for (int j = 0; j < kCh; j += 2) {
+            const float4 q = *reinterpret_cast<const float4*>(swr + c0 + (j & ~3));
+            const float2 y = __fmul2_rn(acc[j / 2], (j & 2) ? make_float2(q.z, q.w) : make_float2(q.x, q.y));
+            const int m = mbase + c0 + j;
+            if (nvalid && m < M) {
+              if (args.out_f32)
+                reinterpret_cast<float*>(args.out)[(int64_t)m * args.ldo + n] = y.x;
+              else
+                reinterpret_cast<uint16_t*>(args.out)[(int64_t)m * args.ldo + n] =
+                    f32_to_bf16_rne(y.x);
+            }
+            if (nvalid && m + 1 < M) {
+              if (args.out_f32)
+                reinterpret_cast<float*>(args.out)[(int64_t)(m + 1) * args.ldo + n] = y.y;
+              else
+                reinterpret_cast<uint16_t*>(args.out)[(int64_t)(m + 1) * args.ldo + n] =
+                    f32_to_bf16_rne(y.y);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < (kColsPerThread - kCh) / 2; ++i) acc[i] = acc[i + kCh / 2];
         }
       }
+      __syncwarp();  // sw is rewritten at the next tile
     }
+    cp_async_wait_all();          // no copy into shared memory outlives the loop
+    if (ostore) bulk_wait_all();  // this CTA's output stores are complete
   }
 
   tc_fence_before();
@@ -450,6 +531,23 @@ static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 output [M][ldo] as the TMA store's destination, box = 128 weight rows
+// x `rows` tokens; false when the base or the row pitch is not 16-byte
+// aligned (the kernel then stores element by element)
+static bool make_out_tmap(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldo,
+                          uint32_t rows) {
+  if (!base || (reinterpret_cast<uintptr_t>(base) & 15) || (ldo * 2) % 16) return false;
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldo * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)kBN, rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
   static int cached[64] = {};
   int dev = 0, n = 0;
@@ -464,9 +562,15 @@ static int num_sms() {
 template <bool kQ4K, bool kDebug, int BM>
 static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, const LargeArgs& a,
                                    cudaStream_t st) {
-  constexpr size_t kSmem = large_smem_bytes<BM>();
-  CUtensorMap tb;
+  constexpr size_t kSmem = large_smem_bytes<kQ4K, BM>();
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  CUtensorMap tb, to;
   if (!make_tmap(&tb, q16, a.M, a.K, BM)) return cudaErrorNotSupported;
+  memset(&to, 0, sizeof(to));
+  LargeArgs args = a;
+  args.tma_out = (QG_TMA_OUT && !kDebug && !a.out_f32 &&
+                  make_out_tmap(&to, a.out, a.M, a.N, a.ldo, LargeCfg<BM>::kColsPerThread))
+                     ? 1 : 0;
   auto kern = prefill_gemm_kernel<kQ4K, kDebug, BM>;
   static bool configured = false;  // once per process (idempotent if raced)
   if (!configured) {
@@ -478,7 +582,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, cons
   const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
   const int slots = num_sms() * kCtasPerSm;
   const int grid = tiles < slots ? tiles : slots;
-  kern<<<grid, kLThreads, kSmem, st>>>(ta, tb, a);
+  kern<<<grid, kLThreads, kSmem, st>>>(ta, tb, to, args);
   return cudaGetLastError();
 }
 

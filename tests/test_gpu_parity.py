@@ -345,3 +345,42 @@ def test_static_quantize_matches_oracle(M, K, per_row):
     out = qg.gemm_w8a8_q8_0(q, h, to_dev(srow), packed, N)
     _, ob = oracle.gemm_w8a8_q8_0(oq, srow, blocks)
     assert np.array_equal(out_bits(out), ob)
+
+
+@pytest.mark.parametrize("M,K,N,ldo", [(300, 512, 256, 264), (513, 256, 384, 392),
+                                       (300, 512, 256, 259), (2048, 256, 1024, 1032)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_w8a8_padded_output_rows(M, K, N, ldo, out_dtype):
+    """Outputs written into rows of pitch ldo > N (bulk tensor stores when the
+    pitch is 16-byte aligned, element stores otherwise): the first N columns
+    hold the oracle's bits and the padding is left untouched."""
+    x, bits, blocks = make_w8a8(M, K, N, seed=M + ldo)
+    q, s, _, h = run_quant(x, bits, want_bs=False)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    big = torch.full((M, ldo), -7.0, dtype=out_dtype, device=DEV)
+    qg.gemm_w8a8_q8_0(q, h, s, packed, N, out=big[:, :N], path="large")
+    torch.cuda.synchronize()
+    qg.check_device_error()
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    want = ob if out_dtype == torch.bfloat16 else y.view(np.uint32)
+    assert np.array_equal(out_bits(big[:, :N].contiguous()), want)
+    assert bool((big[:, N:] == -7.0).all())
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_w4a8_padded_output_rows(out_dtype):
+    M, K, N, ldo = 300, 512, 256, 272
+    x, bits = synth.activations(77, M, K, dtype="bf16", outlier_frac=0.01)
+    sblocks = synth.q4k_weights(177, N, K)
+    q, s, bs, h = qg.quantize_act(bf16_dev(bits), block_sums=True, q16=True)
+    packed = qg.pack_q4k(to_dev(sblocks), N, K)
+    big = torch.full((M, ldo), -7.0, dtype=out_dtype, device=DEV)
+    qg.gemm_w4a8_q4k(q, h, s, bs, packed, N, out=big[:, :N], path="large")
+    torch.cuda.synchronize()
+    qg.check_device_error()
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+    want = ob if out_dtype == torch.bfloat16 else y.view(np.uint32)
+    assert np.array_equal(out_bits(big[:, :N].contiguous()), want)
+    assert bool((big[:, N:] == -7.0).all())
