@@ -35,8 +35,28 @@ constexpr int kCompWarps = 8;      // compute warps per CTA
 
 // K blocks per pipeline stage: 16 for Q8_0 (8 KB of weights per 16-row
 // group), 32 for Q4_K (the same bytes; per-stage overhead halves).
+#ifndef QG_DEC_SBLK_Q8
+#define QG_DEC_SBLK_Q8 16
+#endif
+// CTAs of 320 threads resident per SM (registers and shared memory are
+// budgeted for it)
+#ifndef QG_DEC_CTAS_Q4K
+#define QG_DEC_CTAS_Q4K 3
+#endif
 template <bool kQ4K>
-__host__ __device__ constexpr int sblk() { return kQ4K ? 32 : 16; }
+__host__ __device__ constexpr int dec_ctas() { return kQ4K ? QG_DEC_CTAS_Q4K : 3; }
+template <bool kQ4K>
+constexpr int dec_smem_budget() { return dec_ctas<kQ4K>() == 2 ? 110 * 1024 : 70 * 1024; }
+// Blocks a compute warp converts before their MMAs, and blocks whose sums the
+// chain warp loads before their FMAs: all of a warp's blocks / 4 for Q8_0,
+// one at a time for Q4_K (whose conversions and sub-block terms need the
+// registers; batching measured slower there).
+template <bool kQ4K>
+__host__ __device__ constexpr int dec_cbatch() { return kQ4K ? 1 : 32; }
+template <bool kQ4K>
+__host__ __device__ constexpr int dec_hbatch() { return kQ4K ? 1 : 4; }
+template <bool kQ4K>
+__host__ __device__ constexpr int sblk() { return kQ4K ? 32 : QG_DEC_SBLK_Q8; }
 // bytes per activation row in a stage: 32 per block + 32 of padding, so the
 // eight rows one 8-byte load touches fall in distinct banks
 template <bool kQ4K>
@@ -96,7 +116,7 @@ struct DecodeArgs {
 };
 
 template <int TT, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const DecodeArgs a) {
   using L = DecodeSmem<TT, kQ4K>;
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
@@ -193,33 +213,42 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(c
       if (!mbar_wait(&xempty[xs], xph ^ 1, a.err)) break;
       const uint8_t* base = smem + st * SBY;
       float* stash = stash_base + xs * (L::kXBytes / 4);
+      // this warp's blocks: fragments of all of them first (rows past nb
+      // of a short last stage compute unused sums that are never stored),
+      // so the blocks' load and MMA latencies overlap
+      constexpr int kCB = dec_cbatch<kQ4K>() < kBlkPerWarp ? dec_cbatch<kQ4K>() : kBlkPerWarp;
 #pragma unroll
-      for (int u = 0; u < kBlkPerWarp; ++u) {
-        const int j = cw * kBlkPerWarp + u;
-        if (j >= nb) break;
-        uint32_t a0[4], a1[4];  // A fragments for the block's halves k 0-15 / 16-31
+      for (int u0 = 0; u0 < kBlkPerWarp; u0 += kCB) {
+      uint32_t a0[kCB][4], a1[kCB][4];  // A fragments, k 0-15 / 16-31
+#pragma unroll
+      for (int u = 0; u < kCB; ++u) {
+        const int j = cw * kBlkPerWarp + u0 + u;
         if (!kQ4K) {
           const uint4 w = *reinterpret_cast<const uint4*>(base + j * 512 + lane * 16);
           // x: row n0 k 8c..+3, y: row n1 k 8c..+3, z: n0 k 8c+4..+7, w: n1 k 8c+4..+7
-          biased_u8x4_to_f16x4(w.x, a0[0], a0[2]);
-          biased_u8x4_to_f16x4(w.y, a0[1], a0[3]);
-          biased_u8x4_to_f16x4(w.z, a1[0], a1[2]);
-          biased_u8x4_to_f16x4(w.w, a1[1], a1[3]);
+          biased_u8x4_to_f16x4(w.x, a0[u][0], a0[u][2]);
+          biased_u8x4_to_f16x4(w.y, a0[u][1], a0[u][3]);
+          biased_u8x4_to_f16x4(w.z, a1[u][0], a1[u][2]);
+          biased_u8x4_to_f16x4(w.w, a1[u][1], a1[u][3]);
         } else {
           const uint2 w =
               *reinterpret_cast<const uint2*>(base + (j >> 1) * 512 + lane * 16 + (j & 1) * 8);
-          a0[0] = nib_pair_to_f16x2<0>(w.x);
-          a0[1] = nib_pair_to_f16x2<4>(w.x);
-          a0[2] = nib_pair_to_f16x2<8>(w.x);
-          a0[3] = nib_pair_to_f16x2<12>(w.x);
-          a1[0] = nib_pair_to_f16x2<0>(w.y);
-          a1[1] = nib_pair_to_f16x2<4>(w.y);
-          a1[2] = nib_pair_to_f16x2<8>(w.y);
-          a1[3] = nib_pair_to_f16x2<12>(w.y);
+          a0[u][0] = nib_pair_to_f16x2<0>(w.x);
+          a0[u][1] = nib_pair_to_f16x2<4>(w.x);
+          a0[u][2] = nib_pair_to_f16x2<8>(w.x);
+          a0[u][3] = nib_pair_to_f16x2<12>(w.x);
+          a1[u][0] = nib_pair_to_f16x2<0>(w.y);
+          a1[u][1] = nib_pair_to_f16x2<4>(w.y);
+          a1[u][2] = nib_pair_to_f16x2<8>(w.y);
+          a1[u][3] = nib_pair_to_f16x2<12>(w.y);
         }
+      }
 #pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          const int mrow = 8 * t + gr;  // token of this lane's B fragment
+      for (int t = 0; t < TT; ++t) {
+        const int mrow = 8 * t + gr;  // token of this lane's B fragment
+#pragma unroll
+        for (int u = 0; u < kCB; ++u) {
+          const int j = cw * kBlkPerWarp + u0 + u;
           uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;
           if (mrow < M) {
             const uint2 bv = *reinterpret_cast<const uint2*>(
@@ -228,12 +257,13 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(c
             biased_u8x4_to_f16x4(bv.y ^ 0x80808080u, b10, b11);
           }
           float d[4];
-          mma_f16_16816(d, a0, b00, b01, zero4);
-          mma_f16_16816(d, a1, b10, b11, d);
+          mma_f16_16816(d, a0[u], b00, b01, zero4);
+          mma_f16_16816(d, a1[u], b10, b11, d);
           // d: (n0, tok 8t+2c), (n0, 8t+2c+1), (n1, 8t+2c), (n1, 8t+2c+1): exact sums
-          *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
-              make_float4(d[0], d[1], d[2], d[3]);
-          if (kDebug) {
+          if (j < nb)
+            *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
+                make_float4(d[0], d[1], d[2], d[3]);
+          if (kDebug && j < nb) {
             const int b = blk0 + j;
             const int n0 = (int)(16 * g + gr), mc0 = 8 * t + 2 * c;
 #pragma unroll
@@ -243,6 +273,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(c
             }
           }
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xfull[xs]);
@@ -303,22 +334,42 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(c
           mB[u] = -(dd1.y * field(H1, 8 + u));
         }
       }
+      // the exact sums of kH blocks (and for W4A8 their activation sums)
+      // are loaded before their FMAs, so one shared-memory latency covers kH
+      // blocks (blocks past nb are loaded, never used; a per-block load
+      // right before its FMAs cost ~90 cycles a block)
+      constexpr int kH = dec_hbatch<kQ4K>();
 #pragma unroll
-      for (int u = 0; u < kG; ++u) {
-        const int j = j0 + u;
-        if (j >= nb) break;
+      for (int h = 0; h < kG; h += kH) {
+        float4 x[kH][TT];
+        float2 as[kH][TT];
 #pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          const float4 x = *reinterpret_cast<const float4*>(stash + ((j * TT + t) * 32 + lane) * 4);
-          acc[t][0] = __ffma2_rn(make_float2(x.x, x.y), make_float2(dA[u], dA[u]), acc[t][0]);
-          acc[t][1] = __ffma2_rn(make_float2(x.z, x.w), make_float2(dB[u], dB[u]), acc[t][1]);
-          if (kQ4K) {
-            const int mc0 = 8 * t + 2 * c, mc1 = mc0 + 1;
-            const float as0 = (mc0 < M) ? (float)bb[mc0 * kSBlk + j] : 0.f;
-            const float as1 = (mc1 < M) ? (float)bb[mc1 * kSBlk + j] : 0.f;
-            const float2 as = make_float2(as0, as1);
-            acc[t][0] = __ffma2_rn(as, make_float2(mA[u], mA[u]), acc[t][0]);
-            acc[t][1] = __ffma2_rn(as, make_float2(mB[u], mB[u]), acc[t][1]);
+        for (int u = 0; u < kH; ++u) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            const int j = j0 + h + u;
+            x[u][t] = *reinterpret_cast<const float4*>(stash + ((j * TT + t) * 32 + lane) * 4);
+            if (kQ4K) {
+              const int mc0 = 8 * t + 2 * c, mc1 = mc0 + 1;
+              as[u][t] = make_float2((mc0 < M) ? (float)bb[mc0 * kSBlk + j] : 0.f,
+                                     (mc1 < M) ? (float)bb[mc1 * kSBlk + j] : 0.f);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kH; ++u) {
+          if (j0 + h + u < nb) {
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+              const float4& xv = x[u][t];
+              const int uu = h + u;
+              acc[t][0] = __ffma2_rn(make_float2(xv.x, xv.y), make_float2(dA[uu], dA[uu]), acc[t][0]);
+              acc[t][1] = __ffma2_rn(make_float2(xv.z, xv.w), make_float2(dB[uu], dB[uu]), acc[t][1]);
+              if (kQ4K) {
+                acc[t][0] = __ffma2_rn(as[u][t], make_float2(mA[uu], mA[uu]), acc[t][0]);
+                acc[t][1] = __ffma2_rn(as[u][t], make_float2(mB[uu], mB[uu]), acc[t][1]);
+              }
+            }
           }
         }
       }
@@ -353,7 +404,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), 1) decode_gemm_kernel(c
 template <int TT, bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_cfg(const DecodeArgs& a, cudaStream_t st) {
   using L = DecodeSmem<TT, kQ4K>;
-  constexpr int kBudget = 70 * 1024;  // three CTAs per SM
+  constexpr int kBudget = dec_smem_budget<kQ4K>();
   auto kern = decode_gemm_kernel<TT, kQ4K, kDebug>;
   static bool configured = false;  // once per process (idempotent if raced)
   if (!configured) {
