@@ -116,8 +116,9 @@ def source_sha(path):
 
 
 def measured_traffic():
-    """DRAM bytes per launch of the prefill kernel on this workload, from the
-    committed ncu summary -- None when the kernel source changed since."""
+    """DRAM bytes per GEMM call (one or two launches) of the prefill kernel on
+    this workload, mean over the two projections, from the committed ncu
+    summary -- None when the kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "prefill_traffic_4b_step.json")
     src = os.path.join(ROOT, "bit_quantized_gemm_gb300", "csrc", "gemm_large.cu")
     try:
@@ -125,7 +126,7 @@ def measured_traffic():
             d = json.load(f)
         if d.get("source_sha") != source_sha(src):
             return None
-        return d.get("bytes_per_launch")
+        return d.get("bytes_per_gemm_call")
     except (OSError, ValueError):
         return None
 
@@ -479,6 +480,9 @@ def main():
                 "peak_source": "%s bf16 dense burst (same rate as the fp16 kind the kernel uses)"
                                % peak_src,
                 "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands)",
+                "per": "GEMM call (one or two launches of the kernel): achieved = 2*M*N*K of "
+                       "the step's two calls / their CUDA-event time; traffic = DRAM bytes "
+                       "of one call, mean of the two",
                 "gemm_ms_per_step": round(gemm_tot, 4)}
 
     # end to end through the public API with host buffers
