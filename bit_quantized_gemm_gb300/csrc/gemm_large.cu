@@ -47,7 +47,7 @@
 namespace qg {
 
 #ifndef QG_STAGES
-#define QG_STAGES 0  // TMA ring depth; 0: 3 stages at BM = 256 (room for output staging), else 4
+#define QG_STAGES 0  // TMA ring depth; 0: as many as fit (3 at BM = 256 with output staging)
 #endif
 #ifndef QG_OUT_CHUNK
 #define QG_OUT_CHUNK 128  // output columns per trip of the output loop (>= kColsPerThread: unrolled)
@@ -95,13 +95,27 @@ struct LargeCfg {
   static constexpr uint32_t kStageBBytes = BM * kBK * 2;
   static constexpr int kColsPerThread = BM / (kEpiWarps / 4);
   static_assert(kColsPerThread % 16 == 0, "whole 16-column tensor-memory loads per thread");
-  static constexpr int kStages = QG_STAGES ? QG_STAGES : (BM == 256 ? 3 : 4);
   static constexpr int kChunk = QG_CHUNK < kColsPerThread ? QG_CHUNK : kColsPerThread;
 };
 
+// TMA ring depth: as many stages as fit next to the output staging, the
+// activation-sum ring and the barriers (narrow tiles have small stages and
+// need many of them in flight: a stage's load takes ~1-2 us under load)
+template <bool kQ4K, int BM>
+__host__ __device__ constexpr int stages_for() {
+  constexpr int kCols = LargeCfg<BM>::kColsPerThread;
+  constexpr int kFixed = (QG_TMA_OUT ? 2 * kCols * kBN * 2 : 16) + (kQ4K ? kAsumRing : 1) * BM * 4 +
+                         kEpiWarps * kCols * 4 + 2048;  // + barriers and alignment slack
+  constexpr int kPer = (int)kStageABytes + BM * kBK * 2;
+  constexpr int n = (226 * 1024 - kFixed) / kPer;
+  // (W4A8 keeps 4: a deeper ring measured ~25 % slower there)
+  constexpr int cap = kQ4K ? 4 : 12;
+  return QG_STAGES ? QG_STAGES : (n > cap ? cap : n);
+}
+
 template <bool kQ4K, int BM>
 struct LargeSmem {
-  static constexpr int kStages = LargeCfg<BM>::kStages;
+  static constexpr int kStages = stages_for<kQ4K, BM>();
   static constexpr int kCols = LargeCfg<BM>::kColsPerThread;
   uint8_t a[kStages][kStageABytes];
   uint8_t b[kStages][LargeCfg<BM>::kStageBBytes];
@@ -154,7 +168,8 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const LargeArgs args) {
   using C = LargeCfg<BM>;
-  constexpr int kStages = C::kStages;
+  constexpr int kStages = stages_for<kQ4K, BM>();
+  constexpr bool kStageMode = C::kTBufs % 4 == 0;
   constexpr int kBM = C::kBM;
   constexpr int kTBufs = C::kTBufs;
   constexpr uint32_t kStageBBytes = C::kStageBBytes;
@@ -172,7 +187,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], 2);  // one commit from each MMA issuer
+      mbar_init(&S.empty[i], kStageMode ? 1 : 2);  // commits of the issuers that use the stage
     }
     for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
@@ -247,8 +262,12 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // issuer `par` handles block 2s+par of every stage s; block b of a tile
-    // accumulates in buffer b % kTBufs, so each issuer owns kTBufs/2 buffers
+    // Block mode (two accumulators, wide tiles): issuer `par` handles block
+    // 2s+par of every stage s, in buffer par. Stage mode (kTBufs a multiple
+    // of 4, narrow tiles, whose MMAs are short): issuer `par` takes whole
+    // stages -- the stages g = par, par+2, ... counted over all of this CTA's
+    // tiles -- and block j of stage g goes to buffer (2g+j) % kTBufs, so each
+    // issuer owns half the buffers and waits on a stage once for two blocks.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBN, kBM);
       static_assert(kTBufs >= 2 && kTBufs % 2 == 0, "accumulators split between two issuers");
@@ -257,28 +276,38 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
       uint32_t phase = 0;
       uint32_t tph = 0;  // bit b: phase of the next wait on tempty[b]
       bool ok = true;
+      int gs = 0;        // stages issued so far over all tiles (stage mode)
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        for (int s = 0; s < NS && ok; ++s) {
-          const int blk = 2 * s + par;
-          if (blk < NB) {
-            const int tb = blk % kTBufs;
+        for (int s = 0; s < NS && ok; ++s, ++gs) {
+          if (kStageMode && (gs & 1) != par) {
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            continue;
+          }
+          ok = mbar_wait(&S.full[stage], phase, args.err);
+          if (!ok) break;
+          const uint32_t a_addr = smem_u32(S.a[stage]);
+          const uint32_t b_addr = smem_u32(S.b[stage]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (!kStageMode && j != par) continue;
+            const int blk = 2 * s + j;
+            if (blk >= NB) continue;
+            const int tb = kStageMode ? (2 * gs + j) % kTBufs : blk % kTBufs;
             const uint32_t tpar = ((tph >> tb) & 1u) ^ 1u;
-            ok = mbar_wait(&S.full[stage], phase, args.err);
-            if (ok) ok = mbar_wait(&S.tempty[tb], tpar, args.err);
+            ok = mbar_wait(&S.tempty[tb], tpar, args.err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(S.a[stage]);
-            const uint32_t b_addr = smem_u32(S.b[stage]);
             const uint32_t d_tmem = tmem_base + (uint32_t)(tb * kBM);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t koff = (uint32_t)((par * 32 + kk * 16) * 2);  // bytes within row
+              const uint32_t koff = (uint32_t)((j * 32 + kk * 16) * 2);  // bytes within row
               mma_f16_ss(d_tmem, smem_desc_sw128(a_addr + koff), smem_desc_sw128(b_addr + koff),
                          idesc, kk);
             }
             mma_commit(&S.tfull[tb]);
             tph ^= 1u << tb;
           }
+          if (!ok) break;
           mma_commit(&S.empty[stage]);  // arrives once this issuer's MMAs are done
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -297,6 +326,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, MT, NT, mt, nt);
+      const int ti = (tile - (int)blockIdx.x) / (int)gridDim.x;  // this CTA's tile count so far
       const int n = nt * kBN + quarter * 32 + lane;
       const bool nvalid = n < N;
       const float* drow = args.d32 + (int64_t)(nvalid ? n : 0) * args.ldd;
@@ -322,21 +352,42 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
         }
       }
 
-      // the scales of block blk+1 are fetched while block blk is processed;
-      // the load is volatile so the compiler keeps it a block ahead of its use
-      float d_next = 0.0f, m_next = 0.0f;
+      // Weight scales are prefetched; the loads are volatile so the compiler
+      // keeps them where they are written. W8A8: one block ahead (a quad
+      // scheme measured ~15 % slower there: the main loop is sensitive to
+      // its code shape). W4A8: four blocks at a time (one 16-byte load of
+      // d*sc and of dmin*m; rows are 16-byte aligned, K a multiple of 256),
+      // the next quad fetched while the current one is used (+7 %).
+      float d_next = 0.0f;
+      float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f), m4 = d4, d4n = d4, m4n = d4;
       if (nvalid) {
-        d_next = ldg_f32_pinned(drow);
-        if (kQ4K) m_next = ldg_f32_pinned(mrow);
+        if (kQ4K) {
+          d4n = ldg_f32x4_pinned(drow);
+          m4n = ldg_f32x4_pinned(mrow);
+        } else {
+          d_next = ldg_f32_pinned(drow);
+        }
       }
       for (int blk = 0; blk < NB && ok; ++blk) {
-        const float dw = d_next;
-        const float ndm = kQ4K ? -m_next : 0.0f;
-        if (blk + 1 < NB && nvalid) {
-          d_next = ldg_f32_pinned(drow + blk + 1);
-          if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
+        float dw, ndm = 0.0f;
+        if (kQ4K) {
+          if ((blk & 3) == 0) {
+            d4 = d4n;
+            m4 = m4n;
+            if (blk + 4 < NB && nvalid) {
+              d4n = ldg_f32x4_pinned(drow + blk + 4);
+              m4n = ldg_f32x4_pinned(mrow + blk + 4);
+            }
+          }
+          const int q = blk & 3;
+          dw = q == 0 ? d4.x : q == 1 ? d4.y : q == 2 ? d4.z : d4.w;
+          ndm = -(q == 0 ? m4.x : q == 1 ? m4.y : q == 2 ? m4.z : m4.w);
+        } else {
+          dw = d_next;
+          if (blk + 1 < NB && nvalid) d_next = ldg_f32_pinned(drow + blk + 1);
         }
-        const int tb = blk % kTBufs;
+        const int tb = kStageMode ? (2 * (ti * NS + (blk >> 1)) + (blk & 1)) % kTBufs
+                                  : blk % kTBufs;
         // `ok` is uniform across the warp without a vote: every lane runs the
         // same polling loop on the same barrier and sees the same answers (a
         // per-block warp vote or shuffle here costs about 9 % of the time)

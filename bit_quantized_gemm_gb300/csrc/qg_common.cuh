@@ -406,6 +406,15 @@ __device__ __forceinline__ float ldg_f32_pinned(const float* p) {
   return v;
 }
 
+// 16-byte read-only load, volatile like ldg_f32_pinned (p 16-byte aligned)
+__device__ __forceinline__ float4 ldg_f32x4_pinned(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
