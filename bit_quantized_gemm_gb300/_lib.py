@@ -98,15 +98,16 @@ def _dtype_code(dt):
 
 
 # ----------------------------------------------------------------------- API
-def quantize_act(x, block_sums=False, q16=False, out=None, stream=None):
+def quantize_act(x, block_sums=False, q16=False, out=None, stream=None, int8=True):
     """x: cuda [M, K] bf16/fp32 (rows may be strided) ->
-    (q int8 [M,K], scale fp32 [M], block_sums int32 [M,K/32] or None, q16 fp16 [M,K] or None).
-    `out` may supply preallocated (q, scale, block_sums, q16)."""
+    (q int8 [M,K] or None, scale fp32 [M], block_sums int32 [M,K/32] or None,
+    q16 fp16 [M,K] or None). `out` may supply preallocated (q, scale, block_sums,
+    q16); int8=False skips q (the prefill GEMM reads q16 alone)."""
     assert x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     if out is None:
         dev = x.device
-        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        q = torch.empty((M, K), dtype=torch.int8, device=dev) if int8 else None
         s = torch.empty((M,), dtype=torch.float32, device=dev)
         bs = torch.empty((M, K // 32), dtype=torch.int32, device=dev) if block_sums else None
         h = torch.empty((M, K), dtype=torch.float16, device=dev) if q16 else None
@@ -165,9 +166,10 @@ def pack_q4k(superblocks, N, K, stream=None):
 
 def gemm_w8a8_q8_0(q, q16, scale, packed, N, out=None, out_dtype=torch.bfloat16, path="auto",
                    stream=None):
-    M, K = q.shape
+    """q (may be None when the prefill kernel runs), q16, scale from quantize_act."""
+    M, K = (q if q is not None else q16).shape
     if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=q.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=scale.device)
     _check(load().qg_gemm_w8a8_q8_0_ex(_ptr(q), _ptr(q16), _ptr(scale), M, K, _ptr(packed), N,
                                        _ptr(out), _dtype_code(out.dtype), out.stride(0),
                                        PATHS[path], _stream(stream)))
@@ -176,9 +178,9 @@ def gemm_w8a8_q8_0(q, q16, scale, packed, N, out=None, out_dtype=torch.bfloat16,
 
 def gemm_w4a8_q4k(q, q16, scale, block_sums, packed, N, out=None, out_dtype=torch.bfloat16,
                   path="auto", stream=None):
-    M, K = q.shape
+    M, K = (q if q is not None else q16).shape
     if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=q.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=scale.device)
     _check(load().qg_gemm_w4a8_q4k_ex(_ptr(q), _ptr(q16), _ptr(scale), _ptr(block_sums), M, K,
                                       _ptr(packed), N, _ptr(out), _dtype_code(out.dtype),
                                       out.stride(0), PATHS[path], _stream(stream)))

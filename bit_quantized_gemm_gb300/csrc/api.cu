@@ -94,19 +94,23 @@ qg_status check_k(int64_t K, int64_t mult) {
 qg_status check_gemm_common(const int8_t* q, const uint16_t* q16, const float* scale, int64_t M,
                             int64_t K, const void* w, int64_t N, void* out, qg_dtype odt,
                             int64_t ldo, qg_path path, int64_t kmult, bool* large) {
-  if (!q || !scale || !w || !out) return fail(QG_EINVAL, "null pointer argument");
+  if (!scale || !w || !out) return fail(QG_EINVAL, "null pointer argument");
   if (M < 1 || M > kMaxM) return fail(QG_EINVAL, "M=%lld out of range [1, 2^24]", (long long)M);
   if (N < 1 || N > kMaxN) return fail(QG_EINVAL, "N=%lld out of range [1, 2^24]", (long long)N);
   qg_status s = check_k(K, kmult);
   if (s != QG_OK) return s;
   if (odt != QG_BF16 && odt != QG_F32) return fail(QG_EINVAL, "out_dtype must be QG_BF16 or QG_F32");
   if (ldo < N) return fail(QG_EINVAL, "ldo=%lld < N=%lld", (long long)ldo, (long long)N);
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(w, 256) || !aligned(scale, 4))
+  if ((q && !aligned(q, 16)) || !aligned(out, 16) || !aligned(w, 256) || !aligned(scale, 4))
     return fail(QG_EALIGN, "q and out need 16-byte, w_packed 256-byte, scale 4-byte alignment");
   if (q16 && !aligned(q16, 16)) return fail(QG_EALIGN, "q16 needs 16-byte alignment");
   if (path != QG_PATH_AUTO && path != QG_PATH_SMALL && path != QG_PATH_LARGE)
     return fail(QG_EINVAL, "unknown path %d", (int)path);
   *large = (path == QG_PATH_LARGE) || (path == QG_PATH_AUTO && M > kSmallMMax);
+  if (!*large && !q)
+    return fail(QG_EINVAL,
+                "the decode kernel (M <= %lld or QG_PATH_SMALL) reads q, the int8 activations",
+                (long long)kSmallMMax);
   if (*large && !q16)
     return fail(QG_EINVAL,
                 "the prefill kernel (M > %lld or QG_PATH_LARGE) needs q16, the fp16 copy of q "
@@ -176,7 +180,8 @@ qg_status qg_check_device_error(void* stream) {
 qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
                           int8_t* q, float* scale, int32_t* block_sums, uint16_t* q16,
                           void* stream) {
-  if (!x || !q || !scale) return fail(QG_EINVAL, "null pointer argument");
+  if (!x || !scale) return fail(QG_EINVAL, "null pointer argument");
+  if (!q && !q16) return fail(QG_EINVAL, "q and q16 are both NULL: no activations to write");
   if (x_dtype != QG_BF16 && x_dtype != QG_F32) return fail(QG_EINVAL, "x_dtype must be QG_BF16 or QG_F32");
   if (M < 1 || M > kMaxM) return fail(QG_EINVAL, "M=%lld out of range [1, 2^24]", (long long)M);
   qg_status s = check_k(K, kBlk);
@@ -185,7 +190,7 @@ qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
   if (ldx < K) return fail(QG_EINVAL, "ldx=%lld < K=%lld", (long long)ldx, (long long)K);
   if (!aligned(x, 16) || (ldx * es) % 16 != 0)
     return fail(QG_EALIGN, "x needs 16-byte alignment and a row stride that is a multiple of 16 bytes");
-  if (!aligned(q, 16) || !aligned(scale, 4) || (block_sums && !aligned(block_sums, 4)) ||
+  if ((q && !aligned(q, 16)) || !aligned(scale, 4) || (block_sums && !aligned(block_sums, 4)) ||
       (q16 && !aligned(q16, 16)))
     return fail(QG_EALIGN, "q and q16 need 16-byte, scale and block_sums 4-byte alignment");
   return from_cuda(launch_quantize_act(x, x_dtype == QG_BF16, M, K, ldx, q, scale, block_sums, q16,
@@ -196,7 +201,8 @@ qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
 qg_status qg_quantize_act_static(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
                                  int64_t ldx, const float* scale, int64_t scale_stride, int8_t* q,
                                  int32_t* block_sums, uint16_t* q16, void* stream) {
-  if (!x || !q || !scale) return fail(QG_EINVAL, "null pointer argument");
+  if (!x || !scale) return fail(QG_EINVAL, "null pointer argument");
+  if (!q && !q16) return fail(QG_EINVAL, "q and q16 are both NULL: no activations to write");
   if (x_dtype != QG_BF16 && x_dtype != QG_F32) return fail(QG_EINVAL, "x_dtype must be QG_BF16 or QG_F32");
   if (M < 1 || M > kMaxM) return fail(QG_EINVAL, "M=%lld out of range [1, 2^24]", (long long)M);
   if (scale_stride != 0 && scale_stride != 1) return fail(QG_EINVAL, "scale_stride must be 0 or 1");
@@ -206,7 +212,7 @@ qg_status qg_quantize_act_static(const void* x, qg_dtype x_dtype, int64_t M, int
   if (ldx < K) return fail(QG_EINVAL, "ldx=%lld < K=%lld", (long long)ldx, (long long)K);
   if (!aligned(x, 16) || (ldx * es) % 16 != 0)
     return fail(QG_EALIGN, "x needs 16-byte alignment and a row stride that is a multiple of 16 bytes");
-  if (!aligned(q, 16) || !aligned(scale, 4) || (block_sums && !aligned(block_sums, 16)) ||
+  if ((q && !aligned(q, 16)) || !aligned(scale, 4) || (block_sums && !aligned(block_sums, 16)) ||
       (q16 && !aligned(q16, 16)))
     return fail(QG_EALIGN, "q and q16 need 16-byte, block_sums 16-byte, scale 4-byte alignment");
   return from_cuda(launch_quantize_act_static(x, x_dtype == QG_BF16, M, K, ldx, scale,

@@ -96,13 +96,14 @@ int qg_gemm_launch_count(int weights_kind, int64_t M, int64_t K, int64_t N, qg_p
 /* above).                                                                   */
 /*   x          [M][ldx] of x_dtype (QG_BF16 or QG_F32), rows of K values;   */
 /*              16-byte aligned, ldx >= K, ldx*elem_size % 16 == 0.          */
-/*   q          [M][K] int8 out, 16-byte aligned.                            */
+/*   q          [M][K] int8 out, 16-byte aligned, or NULL when only q16 is   */
+/*              wanted (the prefill kernel reads q16 alone).                 */
 /*   scale      [M] fp32 out.                                                */
 /*   block_sums [M][K/32] int32 out (sum of q over each 32-wide block, needed */
 /*              by the W4A8 GEMM), or NULL.                                   */
 /*   q16        [M][K] fp16 out holding the same integers as q (exact), the  */
 /*              operand of the prefill tensor-core kernel, or NULL. 16-byte   */
-/*              aligned.                                                     */
+/*              aligned. q and q16 are not both NULL (QG_EINVAL).             */
 /* K must be a positive multiple of 32 and at most 65536; M >= 1.             */
 /* ------------------------------------------------------------------------ */
 qg_status qg_quantize_act(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
@@ -141,7 +142,9 @@ size_t qg_q8_0_packed_bytes(int64_t N, int64_t K);
 qg_status qg_pack_q8_0(const void* blocks, int64_t N, int64_t K, void* packed, void* stream);
 
 /* out[m][n] = the W8A8 result above for m < M, n < N.
- *   q, scale  from qg_quantize_act ([M][K] int8, [M] fp32).
+ *   q, scale  from qg_quantize_act ([M][K] int8, [M] fp32). q is read only by
+ *             the decode kernel (M <= qg_small_m_max() under AUTO, or
+ *             QG_PATH_SMALL) and may be NULL when the prefill kernel runs.
  *   q16       the fp16 copy from qg_quantize_act; required when the prefill
  *             kernel runs (M > qg_small_m_max() under AUTO), else may be NULL.
  *   w_packed  from qg_pack_q8_0 with the same N, K.

@@ -67,6 +67,8 @@ def _gemm(L, q=FAKE, q16=FAKE, s=FAKE, M=4, K=256, w=FAKE, N=16, out=FAKE, dt=0,
     (dict(q=FAKE + 8), _lib.QG_EALIGN), (dict(out=FAKE + 2), _lib.QG_EALIGN),
     (dict(w=FAKE + 16), _lib.QG_EALIGN), (dict(q16=FAKE + 4), _lib.QG_EALIGN),
     (dict(M=17, q16=0), _lib.QG_EINVAL), (dict(M=4, q16=0, path=2), _lib.QG_EINVAL),
+    # q may be NULL only when the prefill kernel runs
+    (dict(M=17, q=0, path=1), _lib.QG_EINVAL), (dict(M=16, q=0), _lib.QG_EINVAL),
 ])
 def test_gemm_argument_validation(L, kw, status):
     assert _gemm(L, **kw) == status
@@ -86,6 +88,11 @@ def test_q4k_and_quantize_validation(L):
     assert qa(P(FAKE + 4), 1, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EALIGN
     assert qa(P(FAKE), 5, 4, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
     assert qa(P(FAKE), 0, 0, 64, 64, P(FAKE), P(FAKE), None, None, None) == _lib.QG_EINVAL
+    # q may be NULL when q16 is written, not both
+    assert qa(P(FAKE), 0, 4, 64, 64, None, P(FAKE), None, None, None) == _lib.QG_EINVAL
+    assert qa(P(FAKE), 0, 4, 64, 64, None, P(FAKE), None, P(FAKE + 8), None) == _lib.QG_EALIGN
+    qs = L.qg_quantize_act_static
+    assert qs(P(FAKE), 0, 4, 64, 64, P(FAKE), 1, None, None, None, None) == _lib.QG_EINVAL
     pk = L.qg_pack_q8_0
     assert pk(P(FAKE), 4, 64, P(FAKE + 16), None) == _lib.QG_EALIGN
     assert pk(None, 4, 64, P(FAKE), None) == _lib.QG_EINVAL

@@ -384,3 +384,23 @@ def test_w4a8_padded_output_rows(out_dtype):
     want = ob if out_dtype == torch.bfloat16 else y.view(np.uint32)
     assert np.array_equal(out_bits(big[:, :N].contiguous()), want)
     assert bool((big[:, N:] == -7.0).all())
+
+
+def test_quantize_without_int8_output_and_gemm_from_q16():
+    """q = NULL: the quantizer writes only the fp16 copy (plus scales and block
+    sums), identical to a full call; the prefill GEMM runs from it alone, and
+    the decode kernel, which needs q, is refused."""
+    M, K, N = 300, 1024, 256
+    x, bits, blocks = make_w8a8(M, K, N, seed=91, outl=0.01)
+    q, s, bs, h = qg.quantize_act(bf16_dev(bits), block_sums=True, q16=True)
+    q2, s2, bs2, h2 = qg.quantize_act(bf16_dev(bits), block_sums=True, q16=True, int8=False)
+    assert q2 is None
+    assert torch.equal(s2, s) and torch.equal(bs2, bs) and torch.equal(h2.view(torch.int16), h.view(torch.int16))
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    out = qg.gemm_w8a8_q8_0(None, h2, s2, packed, N)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quantize_act(bits)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    assert np.array_equal(out_bits(out), ob)
+    with pytest.raises(qg.QGError):
+        qg.gemm_w8a8_q8_0(None, h2, s2, packed, N, path="small")
