@@ -53,8 +53,11 @@ constexpr int dec_smem_budget() { return dec_ctas<kQ4K>() == 2 ? 110 * 1024 : 70
 // registers; batching measured slower there).
 template <bool kQ4K>
 __host__ __device__ constexpr int dec_cbatch() { return kQ4K ? 1 : 32; }
+#ifndef QG_DEC_HB_Q4K
+#define QG_DEC_HB_Q4K 1
+#endif
 template <bool kQ4K>
-__host__ __device__ constexpr int dec_hbatch() { return kQ4K ? 1 : 4; }
+__host__ __device__ constexpr int dec_hbatch() { return kQ4K ? QG_DEC_HB_Q4K : 4; }
 template <bool kQ4K>
 __host__ __device__ constexpr int sblk() { return kQ4K ? 32 : QG_DEC_SBLK_Q8; }
 // bytes per activation row in a stage: 32 per block + 32 of padding, so the
@@ -82,7 +85,11 @@ struct DecodeSmem {
   static constexpr int kARow = arow<kQ4K>();
   static constexpr int kWBytes = kSBlk * (kQ4K ? 256 : 512);  // weights per stage
   static constexpr int kSBytes = kQ4K ? kSBlk / 8 * 256 : kSBlk / 4 * 128;  // scales / headers
-  static constexpr int kXBytes = kSBlk * TT * 32 * 16;          // stash slot
+  static constexpr int kXBytes = kSBlk * TT * 32 * 16;          // exact sums of a stash slot
+  // Q4_K: the exact sub-block scales (d*sc, dmin*m) of the 16 rows, per block,
+  // decoded by the compute warps so the chain warp only loads them
+  static constexpr int kScBytes = kQ4K ? kSBlk * 16 * 8 : 0;
+  static constexpr int kSlotBytes = kXBytes + kScBytes;
   static constexpr int kMaxNw = 8;
   static __host__ __device__ int stage_bytes(int mrows) {
     return (int)align_up(kWBytes + kSBytes + mrows * kARow + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
@@ -91,14 +98,27 @@ struct DecodeSmem {
   static __host__ __device__ int bsum_off(int mrows) { return kWBytes + kSBytes + mrows * kARow; }
   // weight stages that fit in `budget` bytes next to the stash and barriers
   static int num_stages(int mrows, int budget) {
-    const int fixed = 2 * kXBytes + 2 * (kMaxNw + 2) * 8;
+    const int fixed = 2 * kSlotBytes + 2 * (kMaxNw + 2) * 8;
     int nw = (budget - fixed) / stage_bytes(mrows);
     return nw < 2 ? 2 : (nw > kMaxNw ? kMaxNw : nw);
   }
   static __host__ __device__ int total(int mrows, int nw) {
-    return nw * stage_bytes(mrows) + 2 * kXBytes + 2 * (nw + 2) * 8;
+    return nw * stage_bytes(mrows) + 2 * kSlotBytes + 2 * (nw + 2) * 8;
   }
 };
+
+// 6-bit field f (0..15: sc_0..7 then m_0..7) of a Q4_K super-block header
+// held as 16 bytes (d, dmin, then a 96-bit little-endian string of fields in
+// words y, z, w), as a float (exact)
+__device__ __forceinline__ float q4k_field(const uint4& H, int f) {
+  const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
+  const int pos = 6 * f;
+  uint32_t v;
+  if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
+  else if (pos >= 64) v = H.w >> (pos - 64);
+  else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
+  return (float)(v & 63u);
+}
 
 struct DecodeArgs {
   const int8_t* qa;        // [M][K]
@@ -126,7 +146,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   const int mrows = min(a.M, TT * 8);
   const int SBY = L::stage_bytes(mrows);
   float* stash_base = reinterpret_cast<float*>(smem + NW * SBY);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kXBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kSlotBytes);
   uint64_t* empty = full + NW;    // weight stage consumed by the chain warp
   uint64_t* xfull = empty + NW;   // stash slot written (count: compute warps)
   uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
@@ -212,7 +232,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       if (!mbar_wait(&full[st], ph, a.err)) break;
       if (!mbar_wait(&xempty[xs], xph ^ 1, a.err)) break;
       const uint8_t* base = smem + st * SBY;
-      float* stash = stash_base + xs * (L::kXBytes / 4);
+      float* stash = stash_base + xs * (L::kSlotBytes / 4);
       // this warp's blocks: fragments of all of them first (rows past nb
       // of a short last stage compute unused sums that are never stored),
       // so the blocks' load and MMA latencies overlap
@@ -275,6 +295,20 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
         }
       }
       }
+      if (kQ4K && lane < 16) {
+        // this warp's blocks: row `lane`'s d*sc and dmin*m (exact products)
+        float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
+#pragma unroll
+        for (int u = 0; u < kBlkPerWarp; ++u) {
+          const int j = cw * kBlkPerWarp + u;
+          if (j < nb) {
+            const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 +
+                                                            lane * 16);
+            const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&H.x));
+            scw[j * 16 + lane] = make_float2(dd.x * q4k_field(H, j & 7), dd.y * q4k_field(H, 8 + (j & 7)));
+          }
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xfull[xs]);
       if (++st == NW) { st = 0; ph ^= 1; }
@@ -299,9 +333,10 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     const uint8_t* base = smem + st * SBY;
     const uint8_t* sb = base + L::kWBytes;
     const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::bsum_off(mrows));
-    const float* stash = stash_base + xs * (L::kXBytes / 4);
-    // blocks in groups of kG (a quad of Q8_0 scales / one Q4_K super-block)
-    constexpr int kG = kQ4K ? 8 : 4;
+    const float* stash = stash_base + xs * (L::kSlotBytes / 4);
+    const float2* scs = reinterpret_cast<const float2*>(stash + L::kXBytes / 4);  // [block][row]
+    // blocks in groups of kG (a quad of Q8_0 scales)
+    constexpr int kG = 4;
     for (int j0 = 0; j0 < nb; j0 += kG) {
       float dA[kG], dB[kG], mA[kG], mB[kG];
       if (!kQ4K) {
@@ -312,26 +347,14 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
         dA[0] = f0.x; dA[1] = f0.y; dA[2] = f1.x; dA[3] = f1.y;
         dB[0] = f2.x; dB[1] = f2.y; dB[2] = f3.x; dB[3] = f3.y;
       } else {
-        const uint4 H0 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + gr * 16);
-        const uint4 H1 = *reinterpret_cast<const uint4*>(sb + (j0 >> 3) * 256 + (gr + 8) * 16);
-        // 6-bit fields: a 96-bit string in words y, z, w (bytes 4..15)
-        auto field = [](const uint4& H, int f) -> float {
-          const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
-          const int pos = 6 * f;
-          uint32_t v;
-          if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
-          else if (pos >= 64) v = H.w >> (pos - 64);
-          else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
-          return (float)(v & 63u);
-        };
-        const float2 dd0 = __half22float2(*reinterpret_cast<const __half2*>(&H0.x));
-        const float2 dd1 = __half22float2(*reinterpret_cast<const __half2*>(&H1.x));
+        // decoded by the compute warps: rows gr and gr+8 of each block
 #pragma unroll
         for (int u = 0; u < kG; ++u) {
-          dA[u] = dd0.x * field(H0, u);   // exact products
-          dB[u] = dd1.x * field(H1, u);
-          mA[u] = -(dd0.y * field(H0, 8 + u));
-          mB[u] = -(dd1.y * field(H1, 8 + u));
+          const float2 s0 = scs[(j0 + u) * 16 + gr], s1 = scs[(j0 + u) * 16 + gr + 8];
+          dA[u] = s0.x;
+          dB[u] = s1.x;
+          mA[u] = -s0.y;
+          mB[u] = -s1.y;
         }
       }
       // the exact sums of kH blocks (and for W4A8 their activation sums)
