@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 SO = os.path.join(HERE, "libqgemm.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "quantize.cu", "pack.cu", "gemm_small.cu", "gemm_large.cu"]
+SOURCES = ["api.cu", "quantize.cu", "pack.cu", "gemm_small.cu", "gemm_large.cu", "gemm_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-Xptxas", "-v", "-I", os.path.join(HERE, "..", "include")]

@@ -36,9 +36,12 @@
 //
 // Waves: a GEMM whose 256-token tiles leave the last wave of SMs mostly idle
 // runs as two launches -- the weight-row tiles that fill whole waves with
-// 256-token tiles, and the remaining rows over all tokens as narrow tiles
-// (32..128 tokens) spread over the SMs. Every output element still gets its
-// whole K chain from one thread, so the split changes no bit.
+// 256-token tiles, then the remaining rows over all tokens, either as narrow
+// tensor-memory tiles (32..128 tokens) or as the 16-row tiles of
+// gemm_skinny.cu (legacy fp16 MMA), whichever a per-step cycle table
+// predicts faster; small GEMMs may run as narrow or 16-row tiles alone.
+// Every output element still gets its whole K chain from one thread, so the
+// plan changes no bit.
 #include <cuda.h>
 #include <cstring>
 
@@ -60,6 +63,9 @@ namespace qg {
 #endif
 #ifndef QG_EPI_WARPS
 #define QG_EPI_WARPS 8
+#endif
+#ifndef QG_SKINNY
+#define QG_SKINNY 0
 #endif
 #ifndef QG_FORCE_BM
 #define QG_FORCE_BM 0  // tuning: nonzero runs every W8A8 GEMM as one launch of this width
@@ -568,7 +574,8 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 // fp16 matrix [rows][K] row-major, box = 64 (K) x box_rows, 128-byte swizzle
-static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+// (also used by gemm_skinny.cu)
+bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                       uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
@@ -637,41 +644,64 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, cons
   return cudaGetLastError();
 }
 
-// Relative cost of one 32-block step of one tile at tile width BM (a 256-wide
-// step = 1): the epilogue's fixed per-step work (barrier waits, tensor-memory
-// hand-back, loop) does not shrink with the width, so narrow tiles cost more
-// per token but fill the SMs that a ragged last wave of wide tiles leaves idle.
-static double step_cost(int bm) {
+// Cycles of one 32-block step of one tile (measured on GB300 with forced
+// choices): tensor-memory tiles of 128 weight rows x BM tokens, whose fixed
+// per-step barrier round trip does not shrink with BM; and 16-row tiles of
+// gemm_skinny.cu (two CTAs per SM), whose steps are cheap but whose tiles are
+// 8x smaller. Narrow work goes where the SMs fill best.
+static double tc_step_cycles(int bm) {
   switch (bm) {
-    case 256: return 1.0;
-    case 128: return 0.70;
-    case 64: return 0.56;
-    default: return 0.52;  // 32
+    case 256: return 800.0;
+    case 128: return 560.0;
+    case 64: return 450.0;
+    default: return 420.0;  // 32
   }
 }
+static int skinny_tb(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
+static double skinny_step_cycles(int tb) { return tb == 32 ? 120.0 : (tb == 64 ? 260.0 : 300.0); }
 
 // Wave plan of a W8A8 prefill GEMM: the weight-row tiles [0, nt_wide) run as
-// 256-token tiles, the rest (all tokens) as bm_tail-token tiles in a second
-// launch, when that shortens the estimated time (nt_wide = NT: one launch).
+// 256-token tensor-memory tiles; the remaining rows (all tokens) run in a
+// second launch, as bm_tail-token tensor-memory tiles or, with bm_tail = 0,
+// as 16-row tiles of gemm_skinny.cu. nt_wide = NT: one launch.
 struct PrefillPlan {
   int nt_wide;
   int bm_tail;
 };
 static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
   const int64_t NT = ceil_div(N, kBN), MT = ceil_div(M, 256);
-  auto waves = [&](int64_t tiles) { return (double)ceil_div(tiles, (int64_t)sms); };
+  auto waves = [&](int64_t tiles, int per_sm) {
+    return (double)ceil_div(tiles, (int64_t)sms * per_sm);
+  };
+  auto rest = [&](int64_t nw, int& bm_best) {  // best time of rows [nw*128, N) over all tokens
+    double best = 1e30;
+    for (int bm : {128, 64, 32}) {
+      const double t = waves(ceil_div(M, (int64_t)bm) * (NT - nw), 1) * tc_step_cycles(bm);
+      if (t < best) { best = t; bm_best = bm; }
+    }
+    const int tb = skinny_tb(M);
+    const double ts = waves(ceil_div(N - nw * kBN, (int64_t)16) * ceil_div(M, (int64_t)tb), 2) *
+                      skinny_step_cycles(tb);
+    if (ts < best) { best = ts; bm_best = 0; }
+    return best;
+  };
   PrefillPlan best{(int)NT, 256};
-  double best_t = waves(MT * NT) * step_cost(256);
+  double best_t = waves(MT * NT, 1) * tc_step_cycles(256);
   const int64_t nt_wide = (sms * (MT * NT / sms)) / MT;  // weight-row tiles that fill whole waves
   for (int64_t nw = nt_wide; nw >= 0 && nw >= nt_wide - 1; --nw) {
-    for (int bm : {128, 64, 32}) {
-      const double t = (nw ? waves(MT * nw) * step_cost(256) : 0.0) +
-                       waves(ceil_div(M, (int64_t)bm) * (NT - nw)) * step_cost(bm);
-      if (t < best_t * 0.97) { best_t = t; best = PrefillPlan{(int)nw, bm}; }
-    }
+    if (nw >= NT) continue;
+    int bm = 0;
+    const double t = (nw ? waves(MT * nw, 1) * tc_step_cycles(256) : 0.0) + rest(nw, bm);
+    if (t < best_t * 0.97) { best_t = t; best = PrefillPlan{(int)nw, bm}; }
   }
   return best;
 }
+
+// gemm_skinny.cu: 16-weight-row tiles on legacy fp16 MMA
+cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
+                               const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
+                               void* out, bool out_f32, int64_t ldo, uint32_t* err,
+                               cudaStream_t st);
 
 int prefill_launches_q8_0(int64_t M, int64_t N) {
   const PrefillPlan p = QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM}
@@ -701,6 +731,9 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
     if (!make_tmap(&ta, wq16, N, K, kBN)) return cudaErrorNotSupported;
     return launch_prefill_t<false, true, 256>(ta, q16, a, st);
   }
+  if (QG_SKINNY == 2)  // tuning: the whole GEMM as 16-row tiles
+    return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16), a.d32, a.ldd,
+                              N, out, out_f32, ldo, err, st);
   const PrefillPlan p =
       QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM} : plan_prefill_w8a8(M, N, num_sms());
   const int64_t n0 = (int64_t)p.nt_wide * kBN;  // first weight row of the narrow part
@@ -717,6 +750,9 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   an.d32 = a.d32 + n0 * a.ldd;
   an.out = out_f32 ? (void*)(reinterpret_cast<float*>(out) + n0)
                    : (void*)(reinterpret_cast<uint16_t*>(out) + n0);
+  if (p.bm_tail == 0 || QG_SKINNY == 1)  // 16-row tiles (legacy fp16 MMA)
+    return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16 + n0 * K * 2),
+                              an.d32, an.ldd, an.N, an.out, out_f32, ldo, err, st);
   if (!make_tmap(&ta, wq16 + n0 * K * 2, an.N, K, kBN)) return cudaErrorNotSupported;
   switch (p.bm_tail) {
     case 128: return launch_prefill_t<false, false, 128>(ta, q16, an, st);

@@ -406,6 +406,13 @@ __device__ __forceinline__ float ldg_f32_pinned(const float* p) {
   return v;
 }
 
+// 8-byte read-only load, volatile like ldg_f32_pinned (p 8-byte aligned)
+__device__ __forceinline__ float2 ldg_f32x2_pinned(const float* p) {
+  float2 v;
+  asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
 // 16-byte read-only load, volatile like ldg_f32_pinned (p 16-byte aligned)
 __device__ __forceinline__ float4 ldg_f32x4_pinned(const float* p) {
   float4 v;
