@@ -115,16 +115,25 @@ def source_sha(path):
     return hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
 
 
+def sources_sha(paths):
+    """One id for several files (their git blob ids, hashed in order)."""
+    import hashlib
+    h = hashlib.sha1()
+    for p in paths:
+        h.update(source_sha(p).encode())
+    return h.hexdigest()
+
+
 def measured_traffic():
-    """DRAM bytes per GEMM call (one or two launches) of the prefill kernel on
-    this workload, mean over the two projections, from the committed ncu
-    summary -- None when the kernel source changed since."""
+    """DRAM bytes per GEMM call (one or two launches) on this workload, mean
+    over the two projections, from the committed ncu summary -- None when a
+    kernel source it was taken on changed since."""
     p = os.path.join(ROOT, "profiles", "prefill_traffic_4b_step.json")
-    src = os.path.join(ROOT, "bit_quantized_gemm_gb300", "csrc", "gemm_large.cu")
     try:
         with open(p) as f:
             d = json.load(f)
-        if d.get("source_sha") != source_sha(src):
+        srcs = [os.path.join(ROOT, s) for s in d.get("source_files", [])]
+        if not srcs or d.get("source_sha") != sources_sha(srcs):
             return None
         return d.get("bytes_per_gemm_call")
     except (OSError, ValueError):
@@ -480,7 +489,8 @@ def main():
                 "traffic": measured_traffic(),
                 "peak_source": "%s bf16 dense burst (same rate as the fp16 kind the kernel uses)"
                                % peak_src,
-                "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands)",
+                "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands); "
+                          "the down projection's last weight-row tile: skinny_gemm_kernel",
                 "per": "GEMM call (one or two launches of the kernel): achieved = 2*M*N*K of "
                        "the step's two calls / their CUDA-event time; traffic = DRAM bytes "
                        "of one call, mean of the two",

@@ -657,7 +657,13 @@ static double tc_step_cycles(int bm) {
     default: return 420.0;  // 32
   }
 }
-static int skinny_tb(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
+// token-tile width of the 16-row tiles: the smallest that holds M, but 64
+// rather than 128 when 128-token tiles would leave SMs without a second CTA
+static int skinny_tb(int64_t M, int64_t rows, int sms) {
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  return ceil_div(rows, (int64_t)16) * ceil_div(M, (int64_t)128) < 2 * (int64_t)sms ? 64 : 128;
+}
 static double skinny_step_cycles(int tb) { return tb == 32 ? 120.0 : (tb == 64 ? 260.0 : 300.0); }
 
 // Wave plan of a W8A8 prefill GEMM: the weight-row tiles [0, nt_wide) run as
@@ -679,7 +685,7 @@ static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
       const double t = waves(ceil_div(M, (int64_t)bm) * (NT - nw), 1) * tc_step_cycles(bm);
       if (t < best) { best = t; bm_best = bm; }
     }
-    const int tb = skinny_tb(M);
+    const int tb = skinny_tb(M, N - nw * kBN, sms);
     const double ts = waves(ceil_div(N - nw * kBN, (int64_t)16) * ceil_div(M, (int64_t)tb), 2) *
                       skinny_step_cycles(tb);
     if (ts < best) { best = ts; bm_best = 0; }
@@ -700,7 +706,7 @@ static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
 // gemm_skinny.cu: 16-weight-row tiles on legacy fp16 MMA
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
-                               void* out, bool out_f32, int64_t ldo, uint32_t* err,
+                               void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
                                cudaStream_t st);
 
 int prefill_launches_q8_0(int64_t M, int64_t N) {
@@ -733,7 +739,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   }
   if (QG_SKINNY == 2)  // tuning: the whole GEMM as 16-row tiles
     return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16), a.d32, a.ldd,
-                              N, out, out_f32, ldo, err, st);
+                              N, out, out_f32, ldo, skinny_tb(M, N, num_sms()), err, st);
   const PrefillPlan p =
       QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM} : plan_prefill_w8a8(M, N, num_sms());
   const int64_t n0 = (int64_t)p.nt_wide * kBN;  // first weight row of the narrow part
@@ -752,7 +758,8 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
                    : (void*)(reinterpret_cast<uint16_t*>(out) + n0);
   if (p.bm_tail == 0 || QG_SKINNY == 1)  // 16-row tiles (legacy fp16 MMA)
     return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16 + n0 * K * 2),
-                              an.d32, an.ldd, an.N, an.out, out_f32, ldo, err, st);
+                              an.d32, an.ldd, an.N, an.out, out_f32, ldo,
+                              skinny_tb(M, an.N, num_sms()), err, st);
   if (!make_tmap(&ta, wq16 + n0 * K * 2, an.N, K, kBN)) return cudaErrorNotSupported;
   switch (p.bm_tail) {
     case 128: return launch_prefill_t<false, false, 128>(ta, q16, an, st);

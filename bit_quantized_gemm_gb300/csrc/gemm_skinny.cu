@@ -229,10 +229,11 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
 }
 
 // Weight rows [0, N) of the packed-layout views passed in (the caller offsets
-// wq16, d32 and out to its first row), all M tokens.
+// wq16, d32 and out to its first row), all M tokens, in tiles of tb (32, 64
+// or 128) tokens.
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
-                               void* out, bool out_f32, int64_t ldo, uint32_t* err,
+                               void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
                                cudaStream_t st) {
   SkinnyArgs a{};
   a.d32 = d32;
@@ -243,8 +244,8 @@ cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, 
   a.M = (int)M; a.N = (int)N; a.K = (int)K;
   a.out_f32 = out_f32 ? 1 : 0;
   a.err = err;
-  if (M <= 32) return launch_skinny_t<32>(wq16, q16, a, st);
-  if (M <= 64) return launch_skinny_t<64>(wq16, q16, a, st);
+  if (tb == 32) return launch_skinny_t<32>(wq16, q16, a, st);
+  if (tb == 64) return launch_skinny_t<64>(wq16, q16, a, st);
   return launch_skinny_t<128>(wq16, q16, a, st);
 }
 
