@@ -657,14 +657,19 @@ static double tc_step_cycles(int bm) {
     default: return 420.0;  // 32
   }
 }
-// token-tile width of the 16-row tiles: the smallest that holds M, but 64
-// rather than 128 when 128-token tiles would leave SMs without a second CTA
-static int skinny_tb(int64_t M, int64_t rows, int sms) {
-  if (M <= 32) return 32;
-  if (M <= 64) return 64;
-  return ceil_div(rows, (int64_t)16) * ceil_div(M, (int64_t)128) < 2 * (int64_t)sms ? 64 : 128;
+static double skinny_step_cycles(int tb) { return tb == 32 ? 135.0 : (tb == 64 ? 260.0 : 300.0); }
+// Token-tile width of the 16-row tiles (two CTAs per SM): the one of the
+// smallest estimated time, waves x step cost.
+static double skinny_time(int64_t M, int64_t rows, int sms, int tb) {
+  const int64_t ctas = ceil_div(rows, (int64_t)16) * ceil_div(M, (int64_t)tb);
+  return (double)ceil_div(ctas, 2 * (int64_t)sms) * skinny_step_cycles(tb);
 }
-static double skinny_step_cycles(int tb) { return tb == 32 ? 120.0 : (tb == 64 ? 260.0 : 300.0); }
+static int skinny_tb(int64_t M, int64_t rows, int sms) {
+  int best = 32;
+  for (int tb : {64, 128})
+    if (M > tb / 2 && skinny_time(M, rows, sms, tb) < skinny_time(M, rows, sms, best)) best = tb;
+  return best;
+}
 
 // Wave plan of a W8A8 prefill GEMM: the weight-row tiles [0, nt_wide) run as
 // 256-token tensor-memory tiles; the remaining rows (all tokens) run in a
@@ -685,10 +690,9 @@ static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
       const double t = waves(ceil_div(M, (int64_t)bm) * (NT - nw), 1) * tc_step_cycles(bm);
       if (t < best) { best = t; bm_best = bm; }
     }
-    const int tb = skinny_tb(M, N - nw * kBN, sms);
-    const double ts = waves(ceil_div(N - nw * kBN, (int64_t)16) * ceil_div(M, (int64_t)tb), 2) *
-                      skinny_step_cycles(tb);
-    if (ts < best) { best = ts; bm_best = 0; }
+    const int64_t rows = N - nw * kBN;
+    const double ts = skinny_time(M, rows, sms, skinny_tb(M, rows, sms));
+    if (ts * 1.1 < best) { best = ts; bm_best = 0; }  // the table is rougher for 16-row tiles
     return best;
   };
   PrefillPlan best{(int)NT, 256};
