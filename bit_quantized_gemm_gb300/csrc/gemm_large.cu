@@ -794,8 +794,10 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.dbg = dbg;
   a.err = err;
   constexpr int BM = QG_BM_W4A8;
-  return dbg ? launch_prefill_t<true, true, BM>(ta, q16, a, st)
-             : launch_prefill_t<true, false, BM>(ta, q16, a, st);
+  if (dbg) return launch_prefill_t<true, true, BM>(ta, q16, a, st);
+  // a GEMM of at most 64 tokens fills half of a 128-token tile: 64-token tiles
+  if (M <= 64) return launch_prefill_t<true, false, 64>(ta, q16, a, st);
+  return launch_prefill_t<true, false, BM>(ta, q16, a, st);
 }
 
 }  // namespace qg
