@@ -336,6 +336,77 @@ def cpu_baseline(rows_sample=1024):
             "sample": "%d of 2048 rows of both projections (quantize + W8A8 GEMM)" % rows_sample}
 
 
+# Token-row chunks per projection in the end-to-end step: chunk i's input
+# copy, compute and output copy overlap the neighbouring chunks' (rows are
+# batch-invariant, so chunking changes no bit of the output). One chunk per
+# projection measured fastest on GB300: the step is bound by the host copies
+# (both directions at once run at ~150 GB/s each), and smaller GEMMs plus more
+# launches cost more than the overlap gains, eager or as a CUDA graph.
+E2E_CHUNKS = (1, 1)
+
+
+def make_e2e_step(layers, dev, chunks=None):
+    """The step through the public API with pinned host buffers in and out.
+
+    Input copies run on one stream, the library's launches on the current
+    stream, output copies on a third (the two directions use separate copy
+    engines). Each projection is split into token-row chunks: a chunk's
+    quantize + GEMM waits only for its own input rows, and its output rows
+    leave as soon as its GEMM is done. Returns (step, h2d_bytes, d2h_bytes,
+    host_outputs)."""
+    import bit_quantized_gemm_gb300 as qg
+    chunks = tuple(chunks or E2E_CHUNKS)
+    hx = [L["x"].cpu().pin_memory() for L in layers]
+    hout = [torch.empty(L["out"].shape, dtype=torch.bfloat16).pin_memory() for L in layers]
+    h2d = sum(t.numel() * t.element_size() for t in hx)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    copy_stream = torch.cuda.Stream(device=dev)   # host -> device
+    back_stream = torch.cuda.Stream(device=dev)   # device -> host
+    plan = []  # per layer: row ranges
+    for L, c in zip(layers, chunks):
+        M = L["M"]
+        step_rows = -(-M // c)
+        plan.append([(r, min(M, r + step_rows)) for r in range(0, M, step_rows)])
+
+    def step():
+        comp = torch.cuda.current_stream(dev)  # (a capture stream while a graph records it)
+        copy_stream.wait_stream(comp)  # the copies start after the timing event
+        back_stream.wait_stream(comp)
+        copied = []
+        with torch.cuda.stream(copy_stream):
+            for L, hxi, ranges in zip(layers, hx, plan):
+                for (r0, r1) in ranges:
+                    L["x"][r0:r1].copy_(hxi[r0:r1], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(copy_stream)
+                    copied.append(ev)
+        done = []
+        k = 0
+        for L, ranges in zip(layers, plan):
+            for (r0, r1) in ranges:
+                comp.wait_event(copied[k])
+                k += 1
+                q = L["q"][r0:r1] if L["q"] is not None else None
+                qg.quantize_act(L["x"][r0:r1], q16=True,
+                                out=(q, L["s"][r0:r1], None, L["h"][r0:r1]))
+                qg.gemm_w8a8_q8_0(q, L["h"][r0:r1], L["s"][r0:r1], L["packed"], L["N"],
+                                  out=L["out"][r0:r1])
+                ev2 = torch.cuda.Event()
+                ev2.record(comp)
+                done.append(ev2)
+        k = 0
+        with torch.cuda.stream(back_stream):
+            for L, ho, ranges in zip(layers, hout, plan):
+                for (r0, r1) in ranges:
+                    back_stream.wait_event(done[k])
+                    k += 1
+                    ho[r0:r1].copy_(L["out"][r0:r1], non_blocking=True)
+        comp.wait_stream(copy_stream)
+        comp.wait_stream(back_stream)
+
+    return step, h2d, d2h, hout
+
+
 def run_only(args):
     """One kernel of the layer on one shape: for profiling and quick timing."""
     import bit_quantized_gemm_gb300 as qg
@@ -499,44 +570,7 @@ def main():
     # end to end through the public API with host buffers
     e2e = None
     if rank == 0 or world > 1:
-        hx = [L["x"].cpu().pin_memory() for L in layers]
-        hout = [torch.empty(L["out"].shape, dtype=torch.bfloat16).pin_memory() for L in layers]
-        h2d = sum(t.numel() * 2 for t in hx)
-        d2h = sum(t.numel() * 2 for t in hout)
-
-        copy_stream = torch.cuda.Stream(device=dev)   # host -> device
-        back_stream = torch.cuda.Stream(device=dev)   # device -> host
-        comp = torch.cuda.current_stream(dev)
-
-        def e2e_step():
-            """Both layers through the public API, host buffers in and out: the
-            input copies run on one stream ahead of the compute stream, and
-            each output is copied back on another as soon as its GEMM is done
-            (the two directions use separate copy engines)."""
-            import bit_quantized_gemm_gb300 as qg
-            copied = []
-            copy_stream.wait_stream(comp)  # the copies start after the timing event
-            back_stream.wait_stream(comp)
-            with torch.cuda.stream(copy_stream):
-                for L, hxi in zip(layers, hx):
-                    L["x"].copy_(hxi, non_blocking=True)
-                    ev = torch.cuda.Event()
-                    ev.record(copy_stream)
-                    copied.append(ev)
-            done = []
-            for L, ev in zip(layers, copied):
-                comp.wait_event(ev)
-                qg.quantize_act(L["x"], q16=True, out=(L["q"], L["s"], None, L["h"]))
-                qg.gemm_w8a8_q8_0(L["q"], L["h"], L["s"], L["packed"], L["N"], out=L["out"])
-                ev2 = torch.cuda.Event()
-                ev2.record(comp)
-                done.append(ev2)
-            with torch.cuda.stream(back_stream):
-                for L, ho, ev2 in zip(layers, hout, done):
-                    back_stream.wait_event(ev2)
-                    ho.copy_(L["out"], non_blocking=True)
-            comp.wait_stream(copy_stream)
-            comp.wait_stream(back_stream)
+        e2e_step, h2d, d2h, _ = make_e2e_step(layers, dev)
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()

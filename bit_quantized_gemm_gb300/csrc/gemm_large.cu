@@ -17,7 +17,8 @@
 //
 // Tile: 128 weight rows (MMA M, tensor-memory lanes) x BM tokens (MMA N,
 // tensor-memory columns; BM = 256 for W8A8, 128 for W4A8), K staged 64 at a
-// time (two blocks) through a 4-deep TMA ring with 128-byte swizzle. Block b of
+// time (two blocks) through a TMA ring with 128-byte swizzle (as deep as
+// shared memory allows; 3 stages at BM = 256). Block b of
 // a tile accumulates in buffer b % kTBufs (two 256-column buffers at BM = 256:
 // all 512 columns), so the MMA of block b+1 overlaps the epilogue of block b.
 // Warp roles (352 threads, one CTA per SM, persistent over tiles):
