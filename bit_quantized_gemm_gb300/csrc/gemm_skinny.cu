@@ -22,6 +22,8 @@
 //     per 8-byte load, fetched one stage ahead.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "qg_common.cuh"
 
 namespace qg {
@@ -29,6 +31,12 @@ namespace qg {
 // from gemm_large.cu
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows);
 
+#ifndef QG_SK_SCALE_AHEAD
+#define QG_SK_SCALE_AHEAD 3  // trips whose scales are loaded ahead of their use
+#endif
+#ifndef QG_SK_STAGES_PER_TRIP
+#define QG_SK_STAGES_PER_TRIP 1  // stages whose blocks a compute warp sums before their FMAs
+#endif
 constexpr int kSkRows = 16;  // weight rows per CTA (the MMA's M)
 constexpr int kSkBK = 64;    // K per stage: two blocks, one 128-byte swizzle row
 
@@ -136,49 +144,93 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, 2)
 #pragma unroll
   for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
 
-  // the two blocks' scales of a stage, one stage ahead (8-byte loads: a
-  // stage's first block is even; rows are padded to whole quads)
-  float2 sA = ldg_f32x2_pinned(drA), sB = ldg_f32x2_pinned(drB);
+  // kU stages (2*kU blocks) per trip: their sums first, so the blocks' MMA
+  // chains overlap, then their FMAs in block order. The trip's scales are
+  // loaded one trip ahead (kU = 1: 8-byte loads, a stage's first block is
+  // even; kU = 2: 16-byte loads, a pair's first block is a multiple of 4;
+  // rows are padded to whole quads)
+  constexpr int kU = QG_SK_STAGES_PER_TRIP;
+  static_assert(kU == 1 || kU == 2, "stages per trip");
+  using ScaleV = typename std::conditional<kU == 2, float4, float2>::type;
+  auto load_scales = [&](const float* p) -> ScaleV {
+    if constexpr (kU == 2) return ldg_f32x4_pinned(p);
+    else return ldg_f32x2_pinned(p);
+  };
+  // scales of the next kP trips in flight (a shift register of loads)
+  constexpr int kP = QG_SK_SCALE_AHEAD;
+  ScaleV pA[kP], pB[kP];
+#pragma unroll
+  for (int p = 0; p < kP; ++p) {
+    if (2 * kU * p < NB) {
+      pA[p] = load_scales(drA + 2 * kU * p);
+      pB[p] = load_scales(drB + 2 * kU * p);
+    }
+  }
   int st = 0;
   uint32_t ph = 0;
   bool ok = true;
-  for (int s = 0; s < NS && ok; ++s) {
-    const float2 cA = sA, cB = sB;
-    if (2 * s + 2 < NB) {
-      sA = ldg_f32x2_pinned(drA + 2 * s + 2);
-      sB = ldg_f32x2_pinned(drB + 2 * s + 2);
+  for (int s = 0; s < NS && ok; s += kU) {
+    const ScaleV cA = pA[0], cB = pB[0];
+#pragma unroll
+    for (int p = 0; p + 1 < kP; ++p) {
+      pA[p] = pA[p + 1];
+      pB[p] = pB[p + 1];
     }
-    ok = mbar_wait(&full[st], ph, args.err);
+    if (2 * (s + kU * kP) < NB) {
+      pA[kP - 1] = load_scales(drA + 2 * (s + kU * kP));
+      pB[kP - 1] = load_scales(drB + 2 * (s + kU * kP));
+    }
+    const int nst = (s + kU <= NS) ? kU : NS - s;  // stages in this trip
+    int sts[kU];
+    uint32_t phs[kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      sts[q] = st;
+      phs[q] = ph;
+      if (q < nst && ++st == kS) { st = 0; ph ^= 1; }
+    }
+#pragma unroll
+    for (int q = 0; q < kU; ++q)
+      if (q < nst && ok) ok = mbar_wait(&full[sts[q]], phs[q], args.err);
     if (!ok) break;
-    const uint32_t a_s = smem_u32(sm + st * C::kStageBytes);
-    const uint32_t b_s = a_s + C::kABytes;
-    // both blocks' sums first (a missing second block of a K tail reads the
-    // zero-filled box and is never used), then their FMAs in block order
-    float d[2][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
+    // every block's sums first (a missing second block of a K tail reads the
+    // zero-filled box and is never used; a missing stage is not read)
+    float d[2 * kU][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
+    for (int q = 0; q < kU; ++q) {
+      if (q < nst) {
+        const uint32_t a_s = smem_u32(sm + sts[q] * C::kStageBytes);
+        const uint32_t b_s = a_s + C::kABytes;
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {
-        const int kc = jb * 32 + kh * 16;
-        uint32_t af[4], bfr[4];
-        ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
-        ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
-        // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
-        if (kh == 0) {
-          mma_f16_16816(d[jb][0], af, bfr[0], bfr[1], zero4);
-          mma_f16_16816(d[jb][1], af, bfr[2], bfr[3], zero4);
-        } else {
-          mma_f16_16816(d[jb][0], af, bfr[0], bfr[1], d[jb][0]);
-          mma_f16_16816(d[jb][1], af, bfr[2], bfr[3], d[jb][1]);
+        for (int jb = 0; jb < 2; ++jb) {
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+            const int kc = jb * 32 + kh * 16;
+            uint32_t af[4], bfr[4];
+            ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
+            ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
+            // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
+            float(&dd)[2][4] = d[2 * q + jb];
+            if (kh == 0) {
+              mma_f16_16816(dd[0], af, bfr[0], bfr[1], zero4);
+              mma_f16_16816(dd[1], af, bfr[2], bfr[3], zero4);
+            } else {
+              mma_f16_16816(dd[0], af, bfr[0], bfr[1], dd[0]);
+              mma_f16_16816(dd[1], af, bfr[2], bfr[3], dd[1]);
+            }
+          }
         }
       }
     }
-    mbar_arrive(&empty[st]);  // this thread's reads of the stage are done
-    if (++st == kS) { st = 0; ph ^= 1; }
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
+    for (int q = 0; q < kU; ++q)
+      if (q < nst) mbar_arrive(&empty[sts[q]]);  // this thread's reads of the stage are done
+#pragma unroll
+    for (int jb = 0; jb < 2 * kU; ++jb) {
       if (2 * s + jb < NB) {
-        const float dA = jb ? cA.y : cA.x, dB = jb ? cB.y : cB.x;
+        const float* fa = reinterpret_cast<const float*>(&cA);
+        const float* fb = reinterpret_cast<const float*>(&cB);
+        const float dA = fa[jb], dB = fb[jb];
         const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
