@@ -229,6 +229,34 @@ def timed_rotating(fns, reps, batches=5):
     return times
 
 
+def timed_graph(fns, reps, batches=5):
+    """As timed_rotating, with the `reps` calls captured once as a CUDA graph
+    and replayed, so that the host's per-call cost (two library calls per
+    step for a quantize + GEMM pair) stays out of the device time."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            fns[i % len(fns)]()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(batches):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    return times
+
+
 def bench_rows(dev, flush, hbm, tf_burst, quick):
     """The other workloads of the layer, per launch (GEMM kernel only)."""
     import bit_quantized_gemm_gb300 as qg
@@ -299,6 +327,65 @@ def bench_rows(dev, flush, hbm, tf_burst, quick):
         else:
             r.update({"bound": "tensor", "frac": round(ops / t / 1e9 / tf_burst, 4)})
         rows["%s_M%d_K%d_N%d" % (name, M, K, N)] = r
+    del packs
+    torch.cuda.empty_cache()
+    rows.update(layer_rows(dev, hbm))
+    return rows
+
+
+def layer_rows(dev, hbm):
+    """The whole layer (x in, y out) at decode sizes through qg_linear_* (the
+    decode GEMM launched as a programmatic dependent of the quantize kernel)
+    against qg_quantize_act and the GEMM called separately, per call, cycling
+    through four weight copies like the decode rows. Each is timed as issued
+    (one host call per layer against two) and replayed from a CUDA graph
+    (device time only)."""
+    import bit_quantized_gemm_gb300 as qg
+    rows = {}
+    K, N = 5120, 17408
+    for kind, name in (("q8_0", "decode_w8a8"), ("q4k", "w4a8_q4k")):
+        q4k = kind == "q4k"
+        wts = torch.from_numpy(synth.config_weights(name, N, K)).to(dev)
+        pack = qg.pack_q4k if q4k else qg.pack_q8_0
+        packs = [pack(wts, N, K) for _ in range(ROTATE_COPIES)]
+        del wts
+        lin = qg.linear_w4a8_q4k if q4k else qg.linear_w8a8_q8_0
+        for M in (1, 8):
+            x, bits = synth.config_activations(name, M, K)
+            xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty((qg.linear_workspace_bytes(kind, M, K),), dtype=torch.uint8,
+                             device=dev)
+            q = torch.empty((M, K), dtype=torch.int8, device=dev)
+            s = torch.empty((M,), dtype=torch.float32, device=dev)
+            bs = torch.empty((M, K // 32), dtype=torch.int32, device=dev) if q4k else None
+
+            def two(p):
+                qg.quantize_act(xd, block_sums=q4k, out=(q, s, bs, None))
+                if q4k:
+                    qg.gemm_w4a8_q4k(q, None, s, bs, p, N, out=out)
+                else:
+                    qg.gemm_w8a8_q8_0(q, None, s, p, N, out=out)
+
+            layer = [lambda p=p: lin(xd, p, N, out=out, workspace=ws) for p in packs]
+            separate = [lambda p=p: two(p) for p in packs]
+            layer[0]()
+            separate[0]()
+            r = {"ms": round(statistics.median(timed_rotating(layer, 40)), 5),
+                 "ms_two_calls": round(statistics.median(timed_rotating(separate, 40)), 5)}
+            try:
+                r["ms_graph"] = round(statistics.median(timed_graph(layer, 40)), 5)
+                r["ms_two_calls_graph"] = round(statistics.median(timed_graph(separate, 40)), 5)
+            except RuntimeError as e:  # capture unavailable: keep the issued timings
+                r["graph"] = "unavailable: %s" % str(e).splitlines()[0][:120]
+            wbytes = N * K // 256 * 144 if q4k else N * K + N * (K // 32) * 2
+            algo = wbytes + 2 * M * K + 2 * M * N  # weights, bf16 x, bf16 out
+            gbs = algo / r["ms"] / 1e6
+            r.update({"launches": 2, "gbs": round(gbs, 1), "bound": "hbm",
+                      "frac": round(gbs / hbm, 4)})
+            rows["layer_%s_M%d_K%d_N%d" % (name, M, K, N)] = r
+        del packs
+        torch.cuda.empty_cache()
     return rows
 
 

@@ -58,6 +58,9 @@ def load():
         "qg_debug_block_sums_q4k": ([P, P, I64, I64, P, I64, P, I, P], I),
         "qg_debug_wait_timeout": ([ctypes.c_uint32, P], I),
         "qg_gemm_launch_count": ([I, I64, I64, I64, I], I),
+        "qg_linear_workspace_bytes": ([I, I64, I64], SZ),
+        "qg_linear_w8a8_q8_0": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
+        "qg_linear_w4a8_q4k": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -212,3 +215,39 @@ def gemm_launch_count(kind, M, K, N, path="auto"):
 
 def small_m_max():
     return int(load().qg_small_m_max())
+
+
+def linear_workspace_bytes(kind, M, K):
+    """Workspace bytes a linear_* call of these sizes needs."""
+    return int(load().qg_linear_workspace_bytes(0 if kind == "q8_0" else 1, M, K))
+
+
+def _linear(kind, x, packed, N, out, out_dtype, scale_out, workspace, stream):
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    need = linear_workspace_bytes(kind, M, K)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    fn = load().qg_linear_w8a8_q8_0 if kind == "q8_0" else load().qg_linear_w4a8_q4k
+    _check(fn(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(packed), N, _ptr(out),
+              _dtype_code(out.dtype), out.stride(0), _ptr(scale_out), _ptr(workspace), nbytes,
+              _stream(stream)))
+    return out
+
+
+def linear_w8a8_q8_0(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=None,
+                     workspace=None, stream=None):
+    """The whole layer: x cuda [M, K] bf16/fp32 (rows may be strided) -> out [M, N].
+    Quantize, then GEMM, through `workspace` (allocated here when not given);
+    for M <= small_m_max() the GEMM overlaps the quantize kernel (programmatic
+    dependent launch). scale_out: optional fp32 [M] receiving the row scales."""
+    return _linear("q8_0", x, packed, N, out, out_dtype, scale_out, workspace, stream)
+
+
+def linear_w4a8_q4k(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=None,
+                    workspace=None, stream=None):
+    """As linear_w8a8_q8_0, with Q4_K weights."""
+    return _linear("q4k", x, packed, N, out, out_dtype, scale_out, workspace, stream)

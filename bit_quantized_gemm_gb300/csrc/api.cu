@@ -20,16 +20,21 @@ cudaError_t launch_pack_q8_0(const void* blocks, int64_t N, int64_t K, void* pac
                              cudaStream_t st);
 cudaError_t launch_pack_q4k(const void* sblocks, int64_t N, int64_t K, void* packed,
                             cudaStream_t st);
+// pdl: launch with programmatic stream serialization (the kernel may start
+// while the previous kernel on the stream, the quantize kernel, still runs)
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,
                                const void* packed, int64_t N, void* out, bool out_f32,
-                               int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
+                               int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                               cudaStream_t st);
 cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* asum, int64_t M,
                               int64_t K, const void* packed, int64_t N, void* out, bool out_f32,
-                              int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
+                              int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                              cudaStream_t st);
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
 int prefill_launches_q8_0(int64_t M, int64_t N);
+
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
                                bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err,
@@ -131,6 +136,74 @@ qg_status decode_chunks(int64_t M, int64_t K, int64_t N, int64_t ldo, size_t out
     if (s != QG_OK) return s;
   }
   return QG_OK;
+}
+
+// Workspace of qg_linear_*, each part 256-byte aligned:
+// the row scales [M] (unless the caller passes scale_out), then the int8
+// activations [M][K] (decode kernel, M <= kSmallMMax) or their fp16 copy
+// [M][K] (prefill kernel), then for W4A8 the block sums [M][K/32].
+struct LinearWs {
+  int64_t off_scale, off_act, off_bsum, total;
+  LinearWs(bool q4k, int64_t M, int64_t K) {
+    off_scale = 0;
+    off_act = align_up(M * 4, 256);
+    const int64_t act = M <= kSmallMMax ? M * K : M * K * 2;
+    off_bsum = align_up(off_act + act, 256);
+    total = align_up(off_bsum + (q4k ? M * (K / kBlk) * 4 : 0), 256);
+  }
+};
+
+qg_status linear(bool q4k, const void* x, qg_dtype xdt, int64_t M, int64_t K, int64_t ldx,
+                 const void* w, int64_t N, void* out, qg_dtype odt, int64_t ldo, float* scale_out,
+                 void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !w || !out) return fail(QG_EINVAL, "null pointer argument");
+  if (xdt != QG_BF16 && xdt != QG_F32) return fail(QG_EINVAL, "x_dtype must be QG_BF16 or QG_F32");
+  if (odt != QG_BF16 && odt != QG_F32) return fail(QG_EINVAL, "out_dtype must be QG_BF16 or QG_F32");
+  if (M < 1 || M > kMaxM) return fail(QG_EINVAL, "M=%lld out of range [1, 2^24]", (long long)M);
+  if (N < 1 || N > kMaxN) return fail(QG_EINVAL, "N=%lld out of range [1, 2^24]", (long long)N);
+  qg_status s = check_k(K, q4k ? kQ4kWeights : kBlk);
+  if (s != QG_OK) return s;
+  const int64_t es = xdt == QG_BF16 ? 2 : 4;
+  if (ldx < K) return fail(QG_EINVAL, "ldx=%lld < K=%lld", (long long)ldx, (long long)K);
+  if (ldo < N) return fail(QG_EINVAL, "ldo=%lld < N=%lld", (long long)ldo, (long long)N);
+  if (!aligned(x, 16) || (ldx * es) % 16 != 0)
+    return fail(QG_EALIGN, "x needs 16-byte alignment and a row stride that is a multiple of 16 bytes");
+  if (!aligned(out, 16) || !aligned(w, 256) || (scale_out && !aligned(scale_out, 4)))
+    return fail(QG_EALIGN, "out needs 16-byte, w_packed 256-byte, scale_out 4-byte alignment");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool f32 = odt == QG_F32;
+  const LinearWs L(q4k, M, K);
+  if (!ws || ws_bytes < (size_t)L.total)
+    return fail(QG_EINVAL, "workspace of %lld bytes needed for M=%lld (qg_linear_workspace_bytes)",
+                (long long)L.total, (long long)M);
+  if (!aligned(ws, 256)) return fail(QG_EALIGN, "workspace needs 256-byte alignment");
+  char* base = reinterpret_cast<char*>(ws);
+  float* scale = scale_out ? scale_out : reinterpret_cast<float*>(base + L.off_scale);
+  const bool small = M <= kSmallMMax;
+  int8_t* q = small ? reinterpret_cast<int8_t*>(base + L.off_act) : nullptr;
+  uint16_t* q16 = small ? nullptr : reinterpret_cast<uint16_t*>(base + L.off_act);
+  int32_t* bsum = q4k ? reinterpret_cast<int32_t*>(base + L.off_bsum) : nullptr;
+  bool large = false;
+  s = check_gemm_common(q, q16, scale, M, K, w, N, out, odt, ldo, QG_PATH_AUTO,
+                        q4k ? kQ4kWeights : kBlk, &large);
+  if (s != QG_OK) return s;
+  s = from_cuda(launch_quantize_act(x, xdt == QG_BF16, M, K, ldx, q, scale, bsum, q16, st),
+                "quantize launch");
+  if (s != QG_OK) return s;
+  if (large)
+    return from_cuda(q4k ? launch_prefill_q4k(q16, scale, bsum, M, K, w, N, out, f32, ldo, nullptr,
+                                              error_word(), st)
+                         : launch_prefill_q8_0(q16, scale, M, K, w, N, out, f32, ldo, nullptr,
+                                               error_word(), st),
+                     "prefill GEMM launch");
+  // M <= kSmallMMax (one decode launch): the GEMM is a programmatic
+  // dependent of the quantize kernel, so its CTAs stream their first weight
+  // stages while the activations are quantized
+  return from_cuda(q4k ? launch_decode_q4k(q, scale, bsum, M, K, w, N, out, f32, ldo, nullptr,
+                                           error_word(), true, st)
+                       : launch_decode_q8_0(q, scale, M, K, w, N, out, f32, ldo, nullptr,
+                                            error_word(), true, st),
+                   "decode GEMM launch");
 }
 
 }  // namespace
@@ -266,7 +339,7 @@ static qg_status gemm_q8_0(const int8_t* q, const uint16_t* q16, const float* sc
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,
                        [&](int64_t m0, int64_t mc, void* o, int32_t* d) {
                          return launch_decode_q8_0(q + m0 * K, scale + m0, mc, K, w, N, o, f32,
-                                                   ldo, d, error_word(), st);
+                                                   ldo, d, error_word(), false, st);
                        });
 }
 
@@ -290,7 +363,7 @@ static qg_status gemm_q4k(const int8_t* q, const uint16_t* q16, const float* sca
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,
                        [&](int64_t m0, int64_t mc, void* o, int32_t* d) {
                          return launch_decode_q4k(q + m0 * K, scale + m0, bsum + m0 * B, mc, K, w,
-                                                  N, o, f32, ldo, d, error_word(), st);
+                                                  N, o, f32, ldo, d, error_word(), false, st);
                        });
 }
 
@@ -320,6 +393,28 @@ qg_status qg_gemm_w4a8_q4k(const int8_t* q, const uint16_t* q16, const float* sc
                            int64_t N, void* out, qg_dtype out_dtype, int64_t ldo, void* stream) {
   return gemm_q4k(q, q16, scale, block_sums, M, K, w_packed, N, out, out_dtype, ldo, QG_PATH_AUTO,
                   nullptr, stream);
+}
+
+size_t qg_linear_workspace_bytes(int weights_kind, int64_t M, int64_t K) {
+  if (weights_kind != 0 && weights_kind != 1) return 0;
+  if (M < 1 || M > kMaxM || check_k(K, weights_kind ? kQ4kWeights : kBlk) != QG_OK) return 0;
+  return (size_t)LinearWs(weights_kind == 1, M, K).total;
+}
+
+qg_status qg_linear_w8a8_q8_0(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
+                              const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                              int64_t ldo, float* scale_out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return linear(false, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out,
+                workspace, workspace_bytes, stream);
+}
+
+qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
+                             const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                             int64_t ldo, float* scale_out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return linear(true, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out,
+                workspace, workspace_bytes, stream);
 }
 
 // A single bounded wait on a barrier that nothing arrives at: after `polls`

@@ -144,6 +144,7 @@ struct DecodeArgs {
   int M, K, N, G;
   int out_f32;
   int nw;           // weight stages in the ring
+  int pdl;          // launched as a programmatic dependent of the quantize kernel
 };
 
 template <int TT, bool kQ4K, bool kDebug>
@@ -185,6 +186,29 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
+    // The activation rows (and W4A8 block sums) of stage r into ring slot `slot`.
+    auto copy_acts = [&](int r, int slot) {
+      const int blk0 = r * kSBlk;
+      const int nb = min(kSBlk, B - blk0);
+      uint8_t* base = smem + slot * SBY;
+      for (int m = lane; m < mrows; m += 32) {
+        bulk_copy(base + L::act_off() + m * kARow,
+                  a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[slot]);
+        if (kQ4K)
+          bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
+                    nb * 4, &full[slot]);
+      }
+    };
+    // Launched as a programmatic dependent, the weights and scales of the
+    // first P stages are requested before any activation: the quantize
+    // kernel may still be writing the activations, and griddep_wait()
+    // returns once it has completed. P is at most 3: every CTA's first three
+    // stages are ~1 us of HBM time, about what a decode-sized quantize
+    // lasts; more would still be arriving when the activations are
+    // requested, and stage 0's activations would queue behind them. An
+    // ordinary launch requests each stage's activations right after its
+    // weights.
+    const int P = a.pdl ? min(min(nstages, NW), 3) : 1;
     int st = 0;
     uint32_t ph = 0;
     for (int s = 0; s < nstages; ++s) {
@@ -212,12 +236,12 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      for (int m = lane; m < mrows; m += 32) {
-        bulk_copy(base + L::act_off() + m * kARow,
-                  a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[st]);
-        if (kQ4K)
-          bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
-                    nb * 4, &full[st]);
+      if (s + 1 == P) {
+        // the first P stages are slots 0..P-1 of the first round
+        if (a.pdl) griddep_wait();
+        for (int r = 0; r < P; ++r) copy_acts(r, r);
+      } else if (s >= P) {
+        copy_acts(s, st);
       }
       if (++st == NW) { st = 0; ph ^= 1; }
     }
@@ -418,6 +442,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   }
 
   if (kDebug || !ok) return;
+  griddep_wait();  // the activation scales come from the preceding quantize kernel
 #pragma unroll
   for (int t = 0; t < TT; ++t) {
     const float accs[4] = {acc[t][0].x, acc[t][0].y, acc[t][1].x, acc[t][1].y};
@@ -436,7 +461,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
 }
 
 template <int TT, bool kQ4K, bool kDebug>
-static cudaError_t launch_decode_cfg(const DecodeArgs& a, cudaStream_t st) {
+static cudaError_t launch_decode_cfg(const DecodeArgs& a, bool pdl, cudaStream_t st) {
   using L = DecodeSmem<TT, kQ4K>;
   // two-tile kernels (9..16 rows) carry twice the activation rows and stash
   constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K>();
@@ -452,20 +477,38 @@ static cudaError_t launch_decode_cfg(const DecodeArgs& a, cudaStream_t st) {
   DecodeArgs b = a;
   const int mrows = a.M < TT * 8 ? a.M : TT * 8;
   b.nw = L::num_stages(mrows, kBudget);
+  b.pdl = pdl ? 1 : 0;
   dim3 grid((unsigned)a.G), block(32 * (kCompWarps + 2));
-  kern<<<grid, block, L::total(mrows, b.nw), st>>>(b);
-  return cudaGetLastError();
+  if (!pdl) {
+    kern<<<grid, block, L::total(mrows, b.nw), st>>>(b);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: the CTAs may start while the previous
+  // kernel on the stream (the quantize kernel) runs, streaming their first
+  // weight stages meanwhile
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = (size_t)L::total(mrows, b.nw);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, b);
 }
 
 template <bool kQ4K, bool kDebug>
-static cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
-  if (a.M <= 8) return launch_decode_cfg<1, kQ4K, kDebug>(a, st);
-  return launch_decode_cfg<2, kQ4K, kDebug>(a, st);
+static cudaError_t launch_decode_m(const DecodeArgs& a, bool pdl, cudaStream_t st) {
+  if (a.M <= 8) return launch_decode_cfg<1, kQ4K, kDebug>(a, pdl, st);
+  return launch_decode_cfg<2, kQ4K, kDebug>(a, pdl, st);
 }
 
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,
                                const void* packed, int64_t N, void* out, bool out_f32,
-                               int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+                               int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                               cudaStream_t st) {
   const Q8Layout Lq(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
   DecodeArgs a{};
@@ -475,12 +518,13 @@ cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int
   a.out = out; a.ldo = ldo; a.dbg = dbg; a.err = err;
   a.M = (int)M; a.K = (int)K; a.N = (int)N; a.G = (int)Lq.G;
   a.out_f32 = out_f32 ? 1 : 0;
-  return dbg ? launch_decode_m<false, true>(a, st) : launch_decode_m<false, false>(a, st);
+  return dbg ? launch_decode_m<false, true>(a, false, st) : launch_decode_m<false, false>(a, pdl, st);
 }
 
 cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* asum, int64_t M,
                               int64_t K, const void* packed, int64_t N, void* out, bool out_f32,
-                              int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+                              int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                              cudaStream_t st) {
   const Q4kLayout Lq(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
   DecodeArgs a{};
@@ -490,7 +534,7 @@ cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* 
   a.out = out; a.ldo = ldo; a.dbg = dbg; a.err = err;
   a.M = (int)M; a.K = (int)K; a.N = (int)N; a.G = (int)Lq.G;
   a.out_f32 = out_f32 ? 1 : 0;
-  return dbg ? launch_decode_m<true, true>(a, st) : launch_decode_m<true, false>(a, st);
+  return dbg ? launch_decode_m<true, true>(a, false, st) : launch_decode_m<true, false>(a, pdl, st);
 }
 
 }  // namespace qg

@@ -422,6 +422,50 @@ __device__ __forceinline__ float4 ldg_f32x4_pinned(const float* p) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on its stream still
+// runs; griddep_wait() returns once that kernel has completed and its memory
+// writes are visible (immediately when the launch was an ordinary one).
+// griddep_launch_dependents() lets the next such kernel start early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Per-token activation quantization arithmetic (the quantize kernels).
+// ---------------------------------------------------------------------------
+// s = absmax / 127, one correctly rounded division
+__device__ __forceinline__ float act_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+
+// The reciprocal qround multiplies by: 1/s rounded once when s is normal (then
+// finite and exact to 2^-24), else 0, which makes qround divide exactly.
+__device__ __forceinline__ float act_scale_rcp(float s) {
+  if (!(s >= 1.17549435e-38f)) return 0.0f;
+  const float inv = __frcp_rn(s);
+  return isinf(inv) ? 0.0f : inv;
+}
+
+// rint(x / s) with the IEEE-rounded quotient, returned as a float.
+// r = x * rcp_rn(s) differs from the exact quotient by at most 2^-16 for
+// |x/s| <= 128 (two roundings of relative size 2^-24 each), and the rounded
+// quotient by at most 2^-16 + 2^-17 < 2^-15. rint() of the two can only
+// differ when a half-integer lies within 2^-15 of r; those rare elements take
+// the exact division.
+// inv = 0 selects the exact division for every element (used when s is
+// subnormal, where the reciprocal loses precision or overflows).
+__device__ __forceinline__ float qround(float x, float s, float inv) {
+  const float r = x * inv;
+  const float q0 = rintf(r);
+  if (__builtin_expect(inv == 0.0f || fabsf(r - q0) >= 0.5f - 3.0517578125e-05f, 0))
+    return rintf(__fdiv_rn(x, s));
+  return q0;
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);

@@ -37,22 +37,6 @@ __device__ __forceinline__ void load_chunk(const void* row, int64_t c, float (&v
   }
 }
 
-// rint(x / s) with the IEEE-rounded quotient, returned as a float.
-// r = x * rcp_rn(s) differs from the exact quotient by at most 2^-16 for
-// |x/s| <= 128 (two roundings of relative size 2^-24 each), and the rounded
-// quotient by at most 2^-16 + 2^-17 < 2^-15. rint() of the two can only
-// differ when a half-integer lies within 2^-15 of r; those rare elements take
-// the exact division.
-// inv = 0 selects the exact division for every element (used when s is
-// subnormal, where the reciprocal loses precision or overflows).
-__device__ __forceinline__ float qround(float x, float s, float inv) {
-  const float r = x * inv;
-  const float q0 = rintf(r);
-  if (__builtin_expect(inv == 0.0f || fabsf(r - q0) >= 0.5f - 3.0517578125e-05f, 0))
-    return rintf(__fdiv_rn(x, s));
-  return q0;
-}
-
 // kStatic: the scale is given (s_in[m * s_stride], e.g. calibrated once) and
 // not computed; values beyond it saturate at +-127.
 template <bool kBf16, int kQThreads, int kRegChunks, bool kStatic>
@@ -60,6 +44,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
     const void* __restrict__ x, int64_t ldx, int K, int8_t* __restrict__ q,
     float* __restrict__ scale, int32_t* __restrict__ bsum, __half* __restrict__ q16,
     const float* __restrict__ s_in, int64_t s_stride) {
+  // a GEMM launched after this kernel with programmatic stream serialization
+  // may start now (its weight streaming overlaps this kernel; it waits for
+  // this grid's completion before it reads the activations)
+  griddep_launch_dependents();
   const int64_t m = blockIdx.x;
   const int tid = threadIdx.x;
   const int nchunks = K / 8;
@@ -104,14 +92,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_act_kernel(
     amax = red[0];
 #pragma unroll
     for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    s = __fdiv_rn(amax, 127.0f);
+    s = act_scale(amax);
   }
   const bool zero_row = kStatic ? (s == 0.0f) : (amax == 0.0f);
-  float inv = 0.0f;
-  if (!zero_row && s >= 1.17549435e-38f) {  // normal s: 1/s is finite and exact to 2^-24
-    inv = __frcp_rn(s);
-    if (isinf(inv)) inv = 0.0f;
-  }
+  const float inv = zero_row ? 0.0f : act_scale_rcp(s);
   if (!kStatic && tid == 0) scale[m] = s;
 
   int8_t* qrow = q ? q + m * (int64_t)K : nullptr;

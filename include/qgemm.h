@@ -188,6 +188,40 @@ qg_status qg_gemm_w4a8_q4k_ex(const int8_t* q, const uint16_t* q16, const float*
                               int64_t ldo, qg_path path, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The whole layer in one call: x in, y out. qg_quantize_act (the dynamic    */
+/* per-token scales) into the caller's workspace, then the GEMM (AUTO), with */
+/* the bits of those two calls made separately.                              */
+/*   M <= qg_small_m_max(): the decode GEMM is launched as a programmatic    */
+/*     dependent of the quantize kernel: its CTAs start while the rows are   */
+/*     quantized, request their first weight stages, and copy activations   */
+/*     only after the quantize grid has completed.                           */
+/*   x          [M][ldx] of x_dtype, 16-byte aligned, ldx >= K,              */
+/*              ldx*elem_size % 16 == 0.                                      */
+/*   w_packed   from qg_pack_q8_0 / qg_pack_q4k with the same N, K.          */
+/*   out        [M][ldo] of out_dtype, 16-byte aligned, ldo >= N.             */
+/*   scale_out  [M] fp32: receives the row scales s[m] (else they stay in    */
+/*              the workspace), or NULL.                                      */
+/*   workspace  device memory of at least qg_linear_workspace_bytes(kind, M, */
+/*              K) bytes, 256-byte aligned, owned by the caller: the row      */
+/*              scales, the quantized activations (int8 for the decode        */
+/*              kernel, fp16 for the prefill kernel) and, for W4A8, the       */
+/*              block sums.                                                   */
+/* K as for the GEMM (multiple of 32; of 256 for Q4_K), M >= 1.               */
+/* ------------------------------------------------------------------------ */
+/* Workspace bytes for qg_linear_w8a8_q8_0 (weights_kind 0) or               */
+/* qg_linear_w4a8_q4k (weights_kind 1) with these sizes; 0 if the sizes are  */
+/* invalid. Host-only. */
+size_t qg_linear_workspace_bytes(int weights_kind, int64_t M, int64_t K);
+qg_status qg_linear_w8a8_q8_0(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
+                              const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                              int64_t ldo, float* scale_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t K, int64_t ldx,
+                             const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
+                             int64_t ldo, float* scale_out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Test support: the exact per-block integer sums as the chosen kernel sees   */
 /* them, isum[m][n][b] (int32, [M][N][K/32]), taken from the same kernels     */
 /* (decode: the int8 MMA accumulators; prefill: the tensor-memory block       */

@@ -130,3 +130,48 @@ def test_gemm_launch_count_host_rules(L):
     assert L.qg_gemm_launch_count(1, 8, 4096 + 32, 17408, 0) == 0  # K not a multiple of 256
     assert L.qg_gemm_launch_count(2, 8, 5120, 17408, 0) == 0
     assert L.qg_gemm_launch_count(0, 8, 5120, 17408, 7) == 0
+
+
+def _align(v, a=256):
+    return (v + a - 1) // a * a
+
+
+def test_linear_workspace_layout(L):
+    # the documented layout: row scales, then the int8 activations (decode
+    # kernel, M <= 16) or their fp16 copy (prefill kernel), then (W4A8) the
+    # block sums, each part 256-byte aligned
+    for M, K in [(1, 256), (8, 5120), (16, 17408), (17, 256), (2048, 2560), (4096, 5120)]:
+        act = M * K if M <= 16 else 2 * M * K
+        base = _align(M * 4) + act
+        assert L.qg_linear_workspace_bytes(0, M, K) == _align(base)
+        assert L.qg_linear_workspace_bytes(1, M, K) == _align(_align(base) + M * (K // 32) * 4)
+    assert L.qg_linear_workspace_bytes(2, 9, 256) == 0      # unknown weights kind
+    assert L.qg_linear_workspace_bytes(0, 9, 48) == 0       # K not a multiple of 32
+    assert L.qg_linear_workspace_bytes(1, 9, 288) == 0      # K not a multiple of 256
+    assert L.qg_linear_workspace_bytes(0, 0, 256) == 0
+    assert qg.linear_workspace_bytes("q8_0", 17, 256) == L.qg_linear_workspace_bytes(0, 17, 256)
+
+
+def _linear(L, kind=0, x=FAKE, xdt=0, M=4, K=256, ldx=256, w=FAKE, N=16, out=FAKE, odt=0,
+            ldo=16, sc=None, ws=None, wsb=0):
+    fn = L.qg_linear_w8a8_q8_0 if kind == 0 else L.qg_linear_w4a8_q4k
+    return fn(P(x), xdt, M, K, ldx, P(w), N, P(out), odt, ldo,
+              None if sc is None else P(sc), None if ws is None else P(ws), wsb, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=0), _lib.QG_EINVAL), (dict(w=0), _lib.QG_EINVAL), (dict(out=0), _lib.QG_EINVAL),
+    (dict(xdt=3), _lib.QG_EINVAL), (dict(odt=3), _lib.QG_EINVAL), (dict(M=0), _lib.QG_EINVAL),
+    (dict(N=0), _lib.QG_EINVAL), (dict(K=48, ldx=48), _lib.QG_EINVAL),
+    (dict(kind=1, K=288, ldx=288), _lib.QG_EINVAL), (dict(ldx=128), _lib.QG_EINVAL),
+    (dict(ldo=8), _lib.QG_EINVAL),
+    (dict(x=FAKE + 8), _lib.QG_EALIGN), (dict(ldx=260), _lib.QG_EALIGN),
+    (dict(xdt=1, ldx=258), _lib.QG_EALIGN), (dict(out=FAKE + 2), _lib.QG_EALIGN),
+    (dict(w=FAKE + 16), _lib.QG_EALIGN), (dict(sc=FAKE + 2), _lib.QG_EALIGN),
+    # a workspace of the reported size is required
+    (dict(M=1), _lib.QG_EINVAL), (dict(M=9, ws=FAKE, wsb=1024), _lib.QG_EINVAL),
+    (dict(M=17, ws=FAKE + 128, wsb=1 << 20), _lib.QG_EALIGN),
+])
+def test_linear_argument_validation(L, kw, status):
+    assert _linear(L, **kw) == status
+    assert L.qg_last_error().decode()

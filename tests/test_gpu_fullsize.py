@@ -154,3 +154,24 @@ def test_launch_plan_of_the_benchmark_step():
     assert qg.gemm_launch_count("q8_0", 8192, 5120, 17408) == 1
     assert qg.gemm_launch_count("q4k", 4096, 5120, 17408) == 1
     assert qg.gemm_launch_count("q8_0", 8, 5120, 17408) == 1
+
+
+@pytest.mark.parametrize("kind,K,N", [("q8_0", 5120, 17408), ("q8_0", 17408, 5120),
+                                      ("q4k", 5120, 17408)])
+def test_linear_decode_full_size(kind, K, N):
+    # the whole layer (x in, y out) at decode sizes (the decode GEMM overlaps
+    # the quantize kernel); every output element compared
+    name = "decode_w8a8" if kind == "q8_0" else "w4a8_q4k"
+    w = synth.config_weights(name, N, K)
+    packed = qg.pack_q8_0(to_dev(w), N, K) if kind == "q8_0" else qg.pack_q4k(to_dev(w), N, K)
+    fn = qg.linear_w8a8_q8_0 if kind == "q8_0" else qg.linear_w4a8_q4k
+    gemm = oracle.gemm_w8a8_q8_0 if kind == "q8_0" else oracle.gemm_w4a8_q4k
+    for M in (1, 8, 16):
+        x, bits = synth.config_activations(name, M, K)
+        xd = to_dev(bits.view(np.int16)).view(torch.bfloat16)
+        out = fn(xd, packed, N)
+        torch.cuda.synchronize()
+        qg.check_device_error()
+        oq, os_ = oracle.quantize_act(bits)
+        _, ob = gemm(oq, os_, w)
+        assert np.array_equal(bits_of(out), ob), (kind, M, K, N)
