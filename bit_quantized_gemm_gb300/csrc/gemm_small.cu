@@ -27,6 +27,9 @@
 //     paths give identical bits -- and hands the stage back to the producer.
 // K-parallel compute with a sequential fp32 chain keeps ten warps busy per
 // 16-row group, which small N (few groups) needs to reach HBM rate.
+// As the GEMM of the layer call the kernel is a programmatic dependent of the
+// quantize kernel: it starts while the rows are quantized, requests its first
+// weight stages, and copies activations only once the quantize grid is done.
 #include "qg_common.cuh"
 
 namespace qg {
