@@ -175,3 +175,23 @@ def _linear(L, kind=0, x=FAKE, xdt=0, M=4, K=256, ldx=256, w=FAKE, N=16, out=FAK
 def test_linear_argument_validation(L, kw, status):
     assert _linear(L, **kw) == status
     assert L.qg_last_error().decode()
+
+
+def test_plain_c_client_links_and_runs(L, tmp_path):
+    # the boundary is a C ABI: a C program built with gcc against the header
+    # and linked to the library runs its host-only checks (no GPU needed)
+    import os
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    libdir = os.path.dirname(_lib.SO_PATH)
+    exe = str(tmp_path / "abi_host_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(here, "c", "abi_host_check.c"), "-L", libdir, "-lqgemm",
+                    "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "0 failure(s)" in r.stdout
