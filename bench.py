@@ -109,10 +109,15 @@ class ClockSampler:
 
 
 def source_sha(path):
-    """git blob id of a file (identifies the kernel source a capture was taken on)."""
+    """Hash of a kernel source's code: comments removed and whitespace
+    collapsed, so that a capture stays attached to the code it was taken on
+    (a comment edit keeps it, any code edit drops it)."""
     import hashlib
-    data = open(path, "rb").read()
-    return hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha1(" ".join(text.split()).encode()).hexdigest()
 
 
 def sources_sha(paths):

@@ -19,7 +19,8 @@
 //   * one producer warp (lane 0) runs the ring; the compute warps hand each
 //     stage back per thread (no warp-wide operation on the path);
 //   * weight scales: d[n][b] from the fp32 scale rows, a stage's two blocks
-//     per 8-byte load, fetched one stage ahead.
+//     per 8-byte load, fetched three stages ahead through a short register
+//     pipeline (one stage ahead left the loads' latency exposed).
 #include <cuda.h>
 
 #include <type_traits>
