@@ -1,0 +1,45 @@
+"""CPU checks of bench.py: the JSON line of the reference arm (the CPU oracle
+timed on the host on a bounded sample of the benchmark step) and the hash
+that ties the committed DRAM-traffic capture to the kernel code."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["unit"] == "TOPS" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "prefill_4b_w8a8"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_capture_hash_follows_code_not_comments(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("int f(int x) { return x + 1; }  // one more\n/* a block\n comment */\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// header comment\nint f(int x) {\n  return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.source_sha(str(a)) == bench.source_sha(str(b))
+    assert bench.source_sha(str(a)) != bench.source_sha(str(c))
+    assert bench.sources_sha([str(a), str(c)]) != bench.sources_sha([str(c), str(a)])
