@@ -2,7 +2,7 @@
  * libqgemm.so and exercises the calls that need no GPU -- version, sizes,
  * workspace and launch-count queries, and argument validation, which rejects
  * bad requests on the host before any launch. Prints one line per check and
- * returns the number of failures. */
+ * returns the number of failures. Valid C99 and C++. */
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
@@ -37,7 +37,8 @@ int main(void) {
             QG_EINVAL,
         "qg_gemm_w8a8_q8_0 rejects a null scale");
   check(strlen(qg_last_error()) > 0, "qg_last_error holds a reason");
-  check(qg_quantize_act(fake, QG_BF16, 4, 64, 68, fake, fake, NULL, NULL, NULL) == QG_EALIGN,
+  check(qg_quantize_act(fake, QG_BF16, 4, 64, 68, (int8_t*)fake, (float*)fake, NULL, NULL,
+                        NULL) == QG_EALIGN,
         "qg_quantize_act rejects a row stride that is not a multiple of 16 bytes");
   check(qg_linear_w8a8_q8_0(fake, QG_BF16, 4, 256, 256, fake, 16, fake, QG_BF16, 16, NULL,
                             NULL, 0, NULL) == QG_EINVAL,

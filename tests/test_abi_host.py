@@ -195,3 +195,13 @@ def test_plain_c_client_links_and_runs(L, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "0 failure(s)" in r.stdout
+    # the same client as C++: the header's extern "C" block gives unmangled names
+    gxx = shutil.which("g++")
+    if gxx is not None:
+        exe_cc = str(tmp_path / "abi_host_check_cc")
+        subprocess.run([gxx, "-x", "c++", "-std=c++17", "-Wall", "-Werror",
+                        "-I", os.path.join(root, "include"),
+                        os.path.join(here, "c", "abi_host_check.c"), "-x", "none", "-L", libdir,
+                        "-lqgemm", "-Wl,-rpath," + libdir, "-o", exe_cc], check=True)
+        r = subprocess.run([exe_cc], capture_output=True, text=True)
+        assert r.returncode == 0 and "0 failure(s)" in r.stdout, r.stdout + r.stderr
