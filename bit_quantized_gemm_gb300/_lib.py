@@ -59,6 +59,7 @@ def load():
         "qg_debug_wait_timeout": ([ctypes.c_uint32, P], I),
         "qg_gemm_launch_count": ([I, I64, I64, I64, I], I),
         "qg_linear_workspace_bytes": ([I, I64, I64], SZ),
+        "qg_debug_prefill_plan_q8_0": ([I64, I64, I, P, P, P], I),
         "qg_linear_w8a8_q8_0": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w4a8_q4k": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
     }
@@ -251,3 +252,14 @@ def linear_w4a8_q4k(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=
                     workspace=None, stream=None):
     """As linear_w8a8_q8_0, with Q4_K weights."""
     return _linear("q4k", x, packed, N, out, out_dtype, scale_out, workspace, stream)
+
+
+def prefill_plan(M, N, sms):
+    """The W8A8 prefill wave plan on `sms` SMs: (rows of the 256-token launch,
+    narrow-part kind: None / "tensor" / "16-row", its token-tile width)."""
+    rows = ctypes.c_int64()
+    kind = ctypes.c_int()
+    tokens = ctypes.c_int()
+    _check(load().qg_debug_prefill_plan_q8_0(M, N, sms, ctypes.byref(rows), ctypes.byref(kind),
+                                             ctypes.byref(tokens)))
+    return rows.value, {0: None, 1: "tensor", 2: "16-row"}[kind.value], tokens.value

@@ -34,6 +34,8 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
                                 const void* packed, int64_t N, void* out, bool out_f32,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
 int prefill_launches_q8_0(int64_t M, int64_t N);
+void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* narrow_kind,
+                       int* narrow_tokens);
 
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
@@ -234,6 +236,16 @@ int qg_gemm_launch_count(int weights_kind, int64_t M, int64_t K, int64_t N, qg_p
   const bool large = (path == QG_PATH_LARGE) || (path == QG_PATH_AUTO && M > kSmallMMax);
   if (!large) return (int)ceil_div(M, kDecodeRows);
   return weights_kind ? 1 : prefill_launches_q8_0(M, N);
+}
+
+qg_status qg_debug_prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide,
+                                     int* narrow_kind, int* narrow_tokens) {
+  if (!rows_wide || !narrow_kind || !narrow_tokens) return fail(QG_EINVAL, "null pointer argument");
+  if (M < 1 || M > kMaxM || N < 1 || N > kMaxN)
+    return fail(QG_EINVAL, "M, N out of range [1, 2^24]");
+  if (sms < 1 || sms > 4096) return fail(QG_EINVAL, "sms=%d out of range [1, 4096]", sms);
+  prefill_plan_q8_0(M, N, sms, rows_wide, narrow_kind, narrow_tokens);
+  return QG_OK;
 }
 
 qg_status qg_check_device_error(void* stream) {

@@ -719,6 +719,26 @@ cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, 
                                void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
                                cudaStream_t st);
 
+// The plan for M x N on `sms` SMs, as launch_prefill_q8_0 carries it out
+// (host only): the weight rows of the 256-token launch, then the remaining
+// rows' kind (0 none, 1 tensor-memory tiles, 2 16-row tiles) and token width.
+void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* narrow_kind,
+                       int* narrow_tokens) {
+  const PrefillPlan p = plan_prefill_w8a8(M, N, sms);
+  const int64_t n0 = (int64_t)p.nt_wide * kBN;
+  *rows_wide = n0 < N ? n0 : N;
+  *narrow_kind = 0;
+  *narrow_tokens = 0;
+  if (n0 >= N) return;
+  if (p.bm_tail == 0) {
+    *narrow_kind = 2;
+    *narrow_tokens = skinny_tb(M, N - n0, sms);
+  } else {
+    *narrow_kind = 1;
+    *narrow_tokens = p.bm_tail;
+  }
+}
+
 int prefill_launches_q8_0(int64_t M, int64_t N) {
   const PrefillPlan p = QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM}
                                     : plan_prefill_w8a8(M, N, num_sms());

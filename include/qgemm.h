@@ -235,6 +235,18 @@ qg_status qg_debug_block_sums_q4k(const int8_t* q, const uint16_t* q16, int64_t 
                                   const void* w_packed, int64_t N, int32_t* isum,
                                   qg_path path, void* stream);
 
+/* Test support: the wave plan of the W8A8 prefill kernel for an M x N GEMM on
+ * a GPU of `sms` SMs, as qg_gemm_w8a8_q8_0 carries it out there (M above
+ * qg_small_m_max(), AUTO). Host-only; launches nothing.
+ *   rows_wide      weight rows [0, rows_wide) run as 256-token tiles in one
+ *                  launch (N: the whole GEMM is that launch);
+ *   narrow_kind    the remaining rows, all tokens, in a second launch: 0 none,
+ *                  1 tensor-memory tiles, 2 16-row tiles (legacy fp16 MMA);
+ *   narrow_tokens  that launch's token-tile width (0 when there is none).
+ * The plan never changes a bit of the result. */
+qg_status qg_debug_prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide,
+                                     int* narrow_kind, int* narrow_tokens);
+
 /* Test support for failure detection: launches one bounded wait on a
  * barrier that nothing completes; after `polls` polls (1 .. 2^20) it records
  * a timeout in the device error word and returns, leaving the context usable.

@@ -205,3 +205,33 @@ def test_plain_c_client_links_and_runs(L, tmp_path):
                         "-lqgemm", "-Wl,-rpath," + libdir, "-o", exe_cc], check=True)
         r = subprocess.run([exe_cc], capture_output=True, text=True)
         assert r.returncode == 0 and "0 failure(s)" in r.stdout, r.stdout + r.stderr
+
+
+def test_prefill_wave_plan_on_152_sms(L):
+    # the plans the benchmark's and the workloads' shapes get on GB300 (152 SMs)
+    plan = _lib.prefill_plan
+    assert plan(2048, 9728, 152) == (9728, None, 0)        # 4B gate/up: 4 whole waves
+    assert plan(2048, 2560, 152) == (2432, "16-row", 64)   # 4B down: 1 wave + 128-row tail
+    assert plan(8192, 17408, 152) == (17408, None, 0)      # 27B gate/up
+    assert plan(32, 5120, 152) == (0, "16-row", 32)        # narrow prefill: 16-row tiles
+    assert plan(64, 17408, 152) == (0, "tensor", 64)       # 64-token tensor-memory tiles
+
+
+def test_prefill_wave_plan_invariants(L):
+    import random
+    rng = random.Random(5)
+    for _ in range(400):
+        M = rng.choice([17, 33, 64, 100, 256, 300, 1000, 2048, 4096, 8192])
+        N = rng.choice([16, 130, 520, 1000, 2560, 5120, 9728, 17408]) + rng.choice([0, 0, 7])
+        sms = rng.choice([1, 8, 132, 148, 152, 160])
+        rows, kind, tokens = _lib.prefill_plan(M, N, sms)
+        assert 0 <= rows <= N
+        assert rows == N or rows % 128 == 0        # whole 128-row tiles, or everything
+        assert (kind is None) == (rows == N)       # a second launch only for leftover rows
+        assert tokens == 0 if kind is None else tokens in (32, 64, 128)
+        launches = 1 if kind is None or rows == 0 else 2
+        assert launches in (1, 2)
+    with pytest.raises(qg.QGError):
+        _lib.prefill_plan(0, 128, 152)
+    with pytest.raises(qg.QGError):
+        _lib.prefill_plan(64, 128, 0)
