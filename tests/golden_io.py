@@ -84,3 +84,52 @@ def q4k_case():
         elif key == "w":
             c["w"] = _kv(rest, float)
     return c
+
+
+def _kv_ranges(text, conv):
+    """index=value or first-last=value tokens -> {index: value}."""
+    out = {}
+    for tok in text.split():
+        k, v = tok.split("=")
+        lo, _, hi = k.partition("-")
+        for i in range(int(lo), int(hi or lo) + 1):
+            out[i] = conv(v)
+    return out
+
+
+def gemm_q4k_cases():
+    """Cases of gemm_q4k_small.txt: K, x, per-row super-block bytes, y, bf16."""
+    cases, cur = [], None
+    for line in _lines("gemm_q4k_small.txt"):
+        if line.startswith("case "):
+            cur = {"name": line[5:].strip(), "sb": {}, "y": {}, "bf16": {}}
+            cases.append(cur)
+            continue
+        key, _, rest = line.partition(":")
+        rest = rest.strip()
+        if key == "K":
+            cur["K"] = int(rest)
+        elif key == "x":
+            cur["x"] = _kv_ranges(rest, float)
+        elif key.startswith("sb"):
+            cur["sb"][int(key[2:])] = _kv_ranges(rest, lambda h: int(h, 16))
+        elif key.startswith("y"):
+            cur["y"][int(key[1:])] = float(rest)
+        elif key.startswith("bf16_"):
+            cur["bf16"][int(key[5:])] = int(rest, 16)
+    return cases
+
+
+def q4k_case_arrays(case):
+    """(x fp32 [1, K], sblocks uint8 [N, K/256, 144]) of a gemm_q4k_small.txt case."""
+    import numpy as np
+    K = case["K"]
+    x = np.zeros((1, K), np.float32)
+    for k, v in case["x"].items():
+        x[0, k] = v
+    N = len(case["sb"])
+    sb = np.zeros((N, K // 256 * 144), np.uint8)
+    for n, bytes_ in case["sb"].items():
+        for i, v in bytes_.items():
+            sb[n, i] = v
+    return x, sb.reshape(N, K // 256, 144)

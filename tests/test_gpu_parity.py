@@ -242,6 +242,28 @@ def test_w4a8_matches_oracle(M, K, N, path):
 
 
 @pytest.mark.parametrize("path", ["small", "large"])
+def test_w4a8_golden_epilogue_order(path):
+    """The hand-derived cases of tests/golden/gemm_q4k_small.txt on both
+    kernels: exact value 0, chain result +2^-9 only with the isum term
+    before the min term, fused, sub-blocks ascending. Each case row sits
+    among seeded rows (rows are independent)."""
+    import golden_io
+    for case in golden_io.gemm_q4k_cases():
+        x, sblocks = golden_io.q4k_case_arrays(case)
+        K, N = x.shape[1], sblocks.shape[0]
+        _, rnd = synth.activations(K + 5, 3, K, dtype="bf16", outlier_frac=0.01)
+        xb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        bits = np.concatenate([rnd[:1], xb, rnd[1:]], axis=0)
+        out, _ = gpu_w4a8(bits, sblocks, N, path, out_dtype=torch.float32)
+        got = out.cpu().numpy()
+        for n, v in case["y"].items():
+            assert got[1, n].view(np.uint32) == np.float32(v).view(np.uint32), (case["name"], got[1, n])
+        outb, _ = gpu_w4a8(bits, sblocks, N, path)
+        for n, v in case["bf16"].items():
+            assert out_bits(outb)[1, n] == v
+
+
+@pytest.mark.parametrize("path", ["small", "large"])
 def test_w4a8_block_sums_exact(path):
     M, K, N = 33, 512, 40
     x, bits = synth.activations(9, M, K, dtype="bf16", outlier_frac=0.05)

@@ -262,6 +262,27 @@ def test_q4k_golden_superblock():
     assert np.array_equal(packed[0, 0], sb)
 
 
+@pytest.mark.parametrize("case", golden_io.gemm_q4k_cases(), ids=lambda c: c["name"])
+def test_gemm_q4k_golden(case):
+    """Hand-derived epilogue cases: the isum term before the min term, one
+    fused multiply-add each, sub-blocks ascending (the alternatives give
+    -2^-9 or 0, derivations in the fixture)."""
+    x, sblocks = golden_io.q4k_case_arrays(case)
+    qa, sa, bs = oracle.quantize_act(x, bsum=True)
+    assert sa[0] == np.float32(1.0)
+    assert np.array_equal(qa[0].astype(np.float32), x[0])
+    y, out = oracle.gemm_w4a8_q4k(qa, sa, sblocks)
+    for n, v in case["y"].items():
+        assert y[0, n].view(np.uint32) == np.float32(v).view(np.uint32), (n, y[0, n], v)
+        assert out[0, n] == case["bf16"][n]
+    # the exact value of every case is 0 (fp64 dot product with the decoded
+    # weights): what the chain leaves is the rounding of its first product
+    for n in range(sblocks.shape[0]):
+        w = np.concatenate([oracle.q4k_decode(sblocks[n, j])["w"]
+                            for j in range(sblocks.shape[1])])
+        assert float(qa[0].astype(np.float64) @ w) == 0.0
+
+
 def _decode_q4k_all(sblocks):
     N, J, _ = sblocks.shape
     ds = np.zeros((N, J * 8))
