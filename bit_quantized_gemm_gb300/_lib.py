@@ -62,6 +62,7 @@ def load():
         "qg_debug_prefill_plan_q8_0": ([I64, I64, I, P, P, P], I),
         "qg_linear_w8a8_q8_0": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w4a8_q4k": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
+        "qg_linear_w8a8_q8_0_noalloc": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P], I),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -252,6 +253,29 @@ def linear_w4a8_q4k(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=
                     workspace=None, stream=None):
     """As linear_w8a8_q8_0, with Q4_K weights."""
     return _linear("q4k", x, packed, N, out, out_dtype, scale_out, workspace, stream)
+
+
+def linear_noalloc_scratch_bytes():
+    """QG_LINEAR_NOALLOC_SCRATCH_BYTES, read from include/qgemm.h."""
+    m = re.search(r"#define\s+QG_LINEAR_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)",
+                  open(HEADER).read())
+    return int(m.group(1)) << int(m.group(2))
+
+
+def linear_w8a8_q8_0_noalloc(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=None,
+                             stream=None):
+    """As linear_w8a8_q8_0, with the library's static scratch in place of a
+    workspace: the library call allocates nothing (`out` is allocated here
+    when not given). Sizes are limited to linear_noalloc_scratch_bytes() of
+    scratch; calls that overlap on the GPU share the scratch and race."""
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _check(load().qg_linear_w8a8_q8_0_noalloc(
+        _ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(packed), N, _ptr(out),
+        _dtype_code(out.dtype), out.stride(0), _ptr(scale_out), _stream(stream)))
+    return out
 
 
 def prefill_plan(M, N, sms):

@@ -49,6 +49,12 @@ using namespace qg;
 // memory, not allocated by any call).
 static __device__ uint32_t g_error_word_dev;
 
+// Scratch of qg_linear_w8a8_q8_0_noalloc: module-scope device memory, one
+// copy on every device that loads the library, never allocated by a call.
+// In host code its name is only a stand-in: the device address comes from
+// cudaGetSymbolAddress, per device.
+static __device__ __align__(256) uint8_t g_linear_scratch[QG_LINEAR_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kVersion = 10000;        // 1.0.0
@@ -206,6 +212,23 @@ qg_status linear(bool q4k, const void* x, qg_dtype xdt, int64_t M, int64_t K, in
                        : launch_decode_q8_0(q, scale, M, K, w, N, out, f32, ldo, nullptr,
                                             error_word(), true, st),
                    "decode GEMM launch");
+}
+
+// Device address of g_linear_scratch on the current device, looked up once
+// per device (with that device current) and cached; nullptr if the lookup
+// fails.
+void* linear_scratch() {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_linear_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
 }
 
 }  // namespace
@@ -427,6 +450,28 @@ qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t
                              size_t workspace_bytes, void* stream) {
   return linear(true, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out,
                 workspace, workspace_bytes, stream);
+}
+
+qg_status qg_linear_w8a8_q8_0_noalloc(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                                      int64_t ldx, const void* w_packed, int64_t N, void* out,
+                                      qg_dtype out_dtype, int64_t ldo, float* scale_out,
+                                      void* stream) {
+  // 0 when M or K is invalid: linear() then reports which, before any use of
+  // the workspace
+  const size_t need = qg_linear_workspace_bytes(0, M, K);
+  if (need > QG_LINEAR_NOALLOC_SCRATCH_BYTES)
+    return fail(QG_EINVAL,
+                "M=%lld, K=%lld need %llu bytes of scratch, more than the %llu of the static "
+                "scratch; call qg_linear_w8a8_q8_0 with a workspace",
+                (long long)M, (long long)K, (unsigned long long)need,
+                (unsigned long long)QG_LINEAR_NOALLOC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  if (need > 0) {
+    ws = linear_scratch();
+    if (!ws) return fail(QG_ECUDA, "no device address for the static scratch on this device");
+  }
+  return linear(false, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out, ws,
+                ws ? QG_LINEAR_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 
 // A single bounded wait on a barrier that nothing arrives at: after `polls`

@@ -222,6 +222,37 @@ qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t
                              size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The W8A8 layer call without a workspace argument and without allocating   */
+/* (the pages have no counterpart: this is a convenience of this library).   */
+/* For callers that cannot call cudaMalloc: a host that hands a plug-in only  */
+/* its input and output buffers across a C interface, or a latency-critical   */
+/* loop where an allocation (cudaMalloc and cudaFree synchronize the device)  */
+/* is not acceptable. The scratch that qg_linear_w8a8_q8_0 takes from its     */
+/* caller lives here in one module-scope device array of                     */
+/* QG_LINEAR_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the     */
+/* library holds until the process exits.                                    */
+/*   Arguments, results and bits as for qg_linear_w8a8_q8_0 (scale_out may   */
+/*   be NULL).                                                               */
+/*   Limit: qg_linear_workspace_bytes(0, M, K) <= QG_LINEAR_NOALLOC_SCRATCH_  */
+/*   BYTES (every M <= qg_small_m_max() at any K; larger M while M*K*2 plus  */
+/*   the row scales fit); larger sizes return QG_EINVAL and launch nothing.  */
+/*   The first call on a device looks the array's device address up for that */
+/*   device (the device current at the call); make that first call before   */
+/*   any stream capture. It returns QG_ECUDA if the lookup fails.            */
+/*   Every call on a device shares the one array, and it keeps the last      */
+/*   call's contents: nothing in it needs to start at zero (the quantize     */
+/*   kernel writes every byte the GEMM then reads). Calls whose work overlaps */
+/*   on the GPU (other streams, other threads) race on it and give wrong     */
+/*   results; order them on one stream or use qg_linear_w8a8_q8_0 with a     */
+/*   workspace each.                                                         */
+/* ------------------------------------------------------------------------ */
+#define QG_LINEAR_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+qg_status qg_linear_w8a8_q8_0_noalloc(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                                      int64_t ldx, const void* w_packed, int64_t N, void* out,
+                                      qg_dtype out_dtype, int64_t ldo, float* scale_out,
+                                      void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Test support: the exact per-block integer sums as the chosen kernel sees   */
 /* them, isum[m][n][b] (int32, [M][N][K/32]), taken from the same kernels     */
 /* (decode: the int8 MMA accumulators; prefill: the tensor-memory block       */
