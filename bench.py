@@ -1,20 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the exact int8 (W8A8) / W4A8 quantized linear layer on GB300.
 
-One step = the whole hot path over one batch of the 4B-class prefill
+One step = the whole hot path over one batch of the 27B-class prefill
 workload: per-token int8 quantization of the activations, then the W8A8
-(Q8_0) GEMM, for both projections of that workload (gate/up: M=2048, K=2560,
-N=9728; down: M=2048, K=9728, N=2560). Inputs are seeded synthetic (bf16
-N(0,1) activations with 1% outlier channels x20 and right-padded rows;
-weights N(0,0.02) encoded as Q8_0), resident in HBM when the timed region
-starts; L2 is flushed (a 512 MiB write) between timed steps, outside the
-per-step CUDA events.
+(Q8_0) GEMM, for both projections of that workload (gate/up: M=8192, K=5120,
+N=17408; down: M=8192, K=17408, N=5120). Inputs are seeded synthetic (bf16
+N(0,1) activations with 1% outlier channels x20; weights N(0,0.02) encoded
+as Q8_0), resident in HBM when the timed region starts; L2 is flushed (a
+512 MiB write) between timed steps, outside the per-step CUDA events.
 
 `value` = int8 GEMM tera-operations per second (2*M*N*K per GEMM, both
 projections, quantization time included). The `rows` object adds the other
 workloads of the layer, each timed per launch with an L2 flush in between:
-decode (M = 1, 8, 64) as weight-streaming GB/s, the 27B-class prefill and
-the W4A8 (Q4_K) shapes. `--impl reference` times the CPU oracle on a bounded
+decode (M = 1, 8, 64) as weight-streaming GB/s, the 4B-class prefill, the
+W4A8 (Q4_K) shapes and the activation quantizer alone (HBM GB/s). `--impl reference` times the CPU oracle on a bounded
 sample of the same step instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -36,8 +35,10 @@ sys.path.insert(0, ROOT)
 from bit_quantized_gemm_gb300 import synth  # noqa: E402
 
 METRIC = "int8 GEMM TOPS (large M) & weight HBM GB/s (M<=64), % of GB300 roofline"
-WORKLOAD = "prefill_4b_w8a8"
-STEP_SHAPES = [(2048, 2560, 9728), (2048, 9728, 2560)]  # (M, K, N): gate/up, down
+WORKLOAD = "prefill_27b_w8a8"
+STEP_SHAPES = [tuple(s) for s in synth.CONFIGS[WORKLOAD]["shapes"]]  # (M, K, N): gate/up, down
+CPU_SAMPLE_ROWS = 4096  # rows of the step the CPU baseline runs (about 10 s on 16 cores)
+REF_SAMPLE_ROWS = 64    # rows per step of --impl reference
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -133,7 +134,7 @@ def measured_traffic():
     """DRAM bytes per GEMM call (one or two launches) on this workload, mean
     over the two projections, from the committed ncu summary -- None when a
     kernel source it was taken on changed since."""
-    p = os.path.join(ROOT, "profiles", "prefill_traffic_4b_step.json")
+    p = os.path.join(ROOT, "profiles", "prefill_traffic_27b_step.json")
     try:
         with open(p) as f:
             d = json.load(f)
@@ -163,7 +164,7 @@ def job_value(ops_per_rank, world, ms_max):
 
 
 def make_step_inputs(dev):
-    """Seeded inputs of the 4B-class prefill step (x bf16, packed Q8_0 weights)."""
+    """Seeded inputs of the 27B-class prefill step (x bf16, packed Q8_0 weights)."""
     import bit_quantized_gemm_gb300 as qg
     layers = []
     for i, (M, K, N) in enumerate(STEP_SHAPES):
@@ -180,6 +181,23 @@ def make_step_inputs(dev):
                            s=s, h=h, out=out))
     torch.cuda.synchronize()
     return layers
+
+
+def step_kernels(dev):
+    """The kernels the step's GEMM calls launch (the wave plan on this GPU)."""
+    from bit_quantized_gemm_gb300 import _lib
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    parts = []
+    for (M, K, N) in STEP_SHAPES:
+        rows, kind, tokens = _lib.prefill_plan(M, N, sms)
+        d = "%dx%dx%d: prefill_gemm_kernel 256-token tiles (tcgen05 kind::f16 on integer-valued " \
+            "operands) for weight rows [0, %d)" % (M, K, N, rows)
+        if kind == "tensor":
+            d += ", rows [%d, %d) as %d-token tiles" % (rows, N, tokens)
+        elif kind == "16-row":
+            d += ", rows [%d, %d) as skinny_gemm_kernel %d-token 16-row tiles" % (rows, N, tokens)
+        parts.append(d)
+    return "; ".join(parts)
 
 
 def step_ops():
@@ -303,7 +321,9 @@ def bench_rows(dev, flush, hbm, tf_burst, quick):
 
     w8a8_rows("decode_w8a8", synth.CONFIGS["decode_w8a8"]["shapes"])
     torch.cuda.empty_cache()
-    w8a8_rows("prefill_27b_w8a8", synth.CONFIGS["prefill_27b_w8a8"]["shapes"])
+    w8a8_rows("prefill_4b_w8a8", synth.CONFIGS["prefill_4b_w8a8"]["shapes"])
+    torch.cuda.empty_cache()
+    rows.update(quantize_rows(dev, flush, hbm, reps))
     torch.cuda.empty_cache()
     # W4A8
     name = "w4a8_q4k"
@@ -335,6 +355,32 @@ def bench_rows(dev, flush, hbm, tf_burst, quick):
     del packs
     torch.cuda.empty_cache()
     rows.update(layer_rows(dev, hbm))
+    return rows
+
+
+def quantize_rows(dev, flush, hbm, reps):
+    """The activation quantizer alone on the prefill shapes, per launch after
+    an L2 flush, as the benchmark step calls it (fp16 copy of q only, the
+    prefill GEMM's operand). HBM bytes = bf16 x read + fp16 q16 written +
+    the fp32 row scales; `frac_int8_contract` uses the 3 B per element of an
+    int8 output instead (bf16 in, int8 out)."""
+    import bit_quantized_gemm_gb300 as qg
+    rows = {}
+    shapes = [(8192, 5120), (8192, 17408), (2048, 2560), (2048, 9728)]
+    for (M, K) in shapes:
+        x, bits = synth.activations(11, M, K, dtype="bf16", outlier_frac=0.01)
+        xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+        h = torch.empty((M, K), dtype=torch.float16, device=dev)
+        fn = lambda: qg.quantize_act(xd, q16=True, out=(None, s, None, h))
+        fn()
+        t = statistics.median(timed_launches(fn, reps, flush))
+        nbytes = M * K * 2 + M * K * 2 + M * 4
+        gbs = nbytes / t / 1e6
+        rows["quantize_M%d_K%d" % (M, K)] = {
+            "ms": round(t, 5), "gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / hbm, 4),
+            "frac_int8_contract": round((3 * M * K + 4 * M) / t / 1e6 / hbm, 4)}
+        del xd, h
     return rows
 
 
@@ -394,15 +440,22 @@ def layer_rows(dev, hbm):
     return rows
 
 
-def oracle_step_data(rows_sample):
-    """Seeded inputs for a `rows_sample`-row slice of the step (the same
-    generators as the GPU arm; rows are independent, so a slice is a fair sample)."""
-    data = []
+def oracle_step_data(layers, rows_sample):
+    """Host inputs of a `rows_sample`-row slice of the step (the seeded bf16
+    activations and Q8_0 blocks the GPU arm uploaded; rows are independent,
+    so a slice is a fair sample)."""
+    return [(np.ascontiguousarray(L["bits"][:rows_sample]), L["blocks"], L["N"], L["K"])
+            for L in layers]
+
+
+def host_step_inputs():
+    """The step's seeded host inputs, without a GPU (the --impl reference arm)."""
+    layers = []
     for i, (M, K, N) in enumerate(STEP_SHAPES):
-        x, bits = synth.config_activations(WORKLOAD, M, K, seed_offset=i)
+        _, bits = synth.config_activations(WORKLOAD, M, K, seed_offset=i)
         blocks = synth.config_weights(WORKLOAD, N, K, seed_offset=i)
-        data.append((np.ascontiguousarray(bits[:rows_sample]), blocks, N, K))
-    return data
+        layers.append(dict(M=M, K=K, N=N, bits=bits, blocks=blocks))
+    return layers
 
 
 def oracle_step(data):
@@ -412,20 +465,21 @@ def oracle_step(data):
         oracle.gemm_w8a8_q8_0(q, s, blocks)
 
 
-def cpu_baseline(rows_sample=1024):
+def cpu_baseline(layers, rows_sample=CPU_SAMPLE_ROWS):
     """The oracle, as it stands, timed on a bounded sample of the step:
-    `rows_sample` of the 2048 rows of both projections (quantize + GEMM), on
+    `rows_sample` of the 8192 rows of both projections (quantize + GEMM), on
     all host cores (input generation excluded)."""
     import oracle
     oracle.build()
-    data = oracle_step_data(rows_sample)
+    data = oracle_step_data(layers, rows_sample)
     t0 = time.perf_counter()
     oracle_step(data)
     dt = time.perf_counter() - t0
     ops = sum(2.0 * rows_sample * N * K for (_, _, N, K) in data)
     return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "%d of 2048 rows of both projections (quantize + W8A8 GEMM)" % rows_sample}
+            "sample": "%d of %d rows of both projections (quantize + W8A8 GEMM)"
+                      % (rows_sample, STEP_SHAPES[0][0])}
 
 
 # Token-row chunks per projection in the end-to-end step: chunk i's input
@@ -565,11 +619,11 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # The CPU oracle on a bounded sample of the same step (64 rows per step).
+        # The CPU oracle on a bounded sample of the same step (REF_SAMPLE_ROWS per step).
         import oracle
         oracle.build()
-        rows_sample = 64
-        data = oracle_step_data(rows_sample)
+        rows_sample = REF_SAMPLE_ROWS
+        data = oracle_step_data(host_step_inputs(), rows_sample)
 
         def ref_step():
             oracle_step(data)
@@ -588,7 +642,8 @@ def main():
                 "config": {"workload": WORKLOAD, "shapes": STEP_SHAPES, "sample_rows": rows_sample},
                 "cpu_baseline": {"value": round(v, 6), "unit": "TOPS", "cores": oracle.num_threads(),
                                  "kind": "oracle",
-                                 "sample": "%d of 2048 rows of both projections per step" % rows_sample},
+                                 "sample": "%d of %d rows of both projections per step"
+                                           % (rows_sample, STEP_SHAPES[0][0])},
                 "e2e": {"value": round(v, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -652,12 +707,16 @@ def main():
                 "traffic": measured_traffic(),
                 "peak_source": "%s bf16 dense burst (same rate as the fp16 kind the kernel uses)"
                                % peak_src,
-                "kernel": "prefill_gemm_kernel (tcgen05 kind::f16 on integer-valued operands); "
-                          "the down projection's last weight-row tile: skinny_gemm_kernel",
+                "kernel": step_kernels(dev),
+                "algorithmic_bytes_per_call": int(sum(
+                    N * K + N * (K // 32) * 2 + M * K + 2 * M * N for (M, K, N) in STEP_SHAPES)
+                    / len(STEP_SHAPES)),
                 "per": "GEMM call (one or two launches of the kernel): achieved = 2*M*N*K of "
                        "the step's two calls / their CUDA-event time; traffic = DRAM bytes "
                        "of one call, mean of the two",
-                "gemm_ms_per_step": round(gemm_tot, 4)}
+                "gemm_ms_per_step": round(gemm_tot, 4),
+                "gemm_ms": [round(sum(g[i] for g in gemm_ms) / len(gemm_ms), 4)
+                            for i in range(len(STEP_SHAPES))]}
 
     # end to end through the public API with host buffers
     e2e = None
@@ -679,10 +738,11 @@ def main():
         e2e = {"value": round(world * ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
+    host = [dict(bits=L["bits"], blocks=L["blocks"], N=L["N"], K=L["K"]) for L in layers]
     rows = None
+    del layers
+    torch.cuda.empty_cache()
     if not args.no_rows:
-        del layers
-        torch.cuda.empty_cache()
         rows = bench_rows(dev, flush, hbm, tf_burst, quick=True)
 
     # one quantize launch per projection, plus the GEMM's own launches (the
@@ -690,7 +750,7 @@ def main():
     launches_per_step = sum(1 + qg.gemm_launch_count("q8_0", M, K, N) for (M, K, N) in STEP_SHAPES)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline()
+        cpu = cpu_baseline(host)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world,

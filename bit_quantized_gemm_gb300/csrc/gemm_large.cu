@@ -134,7 +134,9 @@ struct LargeSmem {
   uint64_t full[kStages], empty[kStages];
   uint64_t tfull[LargeCfg<BM>::kTBufs], tempty[LargeCfg<BM>::kTBufs];
   uint64_t afull[kAsumRing], aempty[kAsumRing];
+  uint64_t mdrain[2];    // per MMA issuer: completion of its MMAs after a wait gave up
   uint32_t tmem_base;
+  uint32_t tmem_busy;    // nonzero: an issuer's MMAs did not complete; tensor memory stays allocated
 };
 template <bool kQ4K, int BM>
 constexpr size_t large_smem_bytes() { return sizeof(LargeSmem<kQ4K, BM>) + 1024; }  // + alignment slack
@@ -205,6 +207,9 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
       mbar_init(&S.afull[i], 32);
       mbar_init(&S.aempty[i], kEpiWarps * 32);
     }
+    mbar_init(&S.mdrain[0], 1);
+    mbar_init(&S.mdrain[1], 1);
+    S.tmem_busy = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     int aslot = 0;
     uint32_t aphase = 0;
     bool ok = true;
+    uint32_t loaded = 0, load_par = 0;  // per stage: a load was issued; parity of the last one
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, MT, NT, args.tile_group, mt, nt);
@@ -234,6 +240,8 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
         if (lane == 0) {
           ok = mbar_wait(&S.empty[stage], phase ^ 1, args.err);
           if (ok) {
+            loaded |= 1u << stage;
+            load_par = (load_par & ~(1u << stage)) | (phase << stage);
             mbar_arrive_expect_tx(&S.full[stage], kStageABytes + kStageBBytes);
             tma_load_2d(S.a[stage], &tmA, &S.full[stage], s * kBK, nt * kBN);
             tma_load_2d(S.b[stage], &tmB, &S.full[stage], s * kBK, mt * kBM);
@@ -266,6 +274,13 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
         if (!mbar_wait(&S.empty[stage], phase ^ 1, args.err)) break;
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
+    }
+    // Every TMA load this thread issued has landed before the CTA exits, also
+    // after a wait gave up (a bounded wait on each stage's last load; at
+    // once when it was consumed).
+    if (lane == 0) {
+      for (int i = 0; i < kStages; ++i)
+        if ((loaded >> i) & 1u) mbar_wait(&S.full[i], (load_par >> i) & 1u, args.err);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
@@ -319,6 +334,13 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           mma_commit(&S.empty[stage]);  // arrives once this issuer's MMAs are done
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+      }
+      if (!ok) {
+        // a wait gave up: the MMAs this thread issued may still run; wait
+        // (bounded) for all of them before tensor memory is freed. If even
+        // that wait gives up, the tensor memory is left allocated.
+        mma_commit(&S.mdrain[par]);
+        if (!mbar_wait(&S.mdrain[par], 0, args.err)) atomicExch(&S.tmem_busy, 1u);
       }
     }
     __syncwarp();
@@ -548,7 +570,7 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && S.tmem_busy == 0) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -636,12 +658,10 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, cons
   // ~0.5 % faster than 8); measured on GB300
   args.tile_group = ceil_div(a.M, BM) <= 8 ? 2 : 16;
   auto kern = prefill_gemm_kernel<kQ4K, kDebug, BM>;
-  static bool configured = false;  // once per process (idempotent if raced)
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  static std::atomic<uint64_t> attr_set{0};
+  {
+    const cudaError_t e = smem_attr_once_per_device(kern, (int)kSmem, attr_set);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
   const int slots = num_sms() * kCtasPerSm;
@@ -713,6 +733,17 @@ static PrefillPlan plan_prefill_w8a8(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+// The plan a launch carries out: the wave plan, or the one the tuning
+// switches of this build force (QG_FORCE_BM: every W8A8 GEMM as one launch of
+// that width; QG_SKINNY 1: the narrow part as 16-row tiles, 2: the whole GEMM
+// as 16-row tiles). Launch, launch count and the host query all use it.
+static PrefillPlan plan_as_built(int64_t M, int64_t N, int sms) {
+  if (QG_SKINNY == 2) return PrefillPlan{0, 0};
+  PrefillPlan p = QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM} : plan_prefill_w8a8(M, N, sms);
+  if (QG_SKINNY == 1 && (int64_t)p.nt_wide * kBN < N) p.bm_tail = 0;
+  return p;
+}
+
 // gemm_skinny.cu: 16-weight-row tiles on legacy fp16 MMA
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
@@ -724,7 +755,7 @@ cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, 
 // rows' kind (0 none, 1 tensor-memory tiles, 2 16-row tiles) and token width.
 void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* narrow_kind,
                        int* narrow_tokens) {
-  const PrefillPlan p = plan_prefill_w8a8(M, N, sms);
+  const PrefillPlan p = plan_as_built(M, N, sms);
   const int64_t n0 = (int64_t)p.nt_wide * kBN;
   *rows_wide = n0 < N ? n0 : N;
   *narrow_kind = 0;
@@ -740,8 +771,7 @@ void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* n
 }
 
 int prefill_launches_q8_0(int64_t M, int64_t N) {
-  const PrefillPlan p = QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM}
-                                    : plan_prefill_w8a8(M, N, num_sms());
+  const PrefillPlan p = plan_as_built(M, N, num_sms());
   return (p.nt_wide > 0 && (int64_t)p.nt_wide * kBN < N) ? 2 : 1;
 }
 
@@ -767,11 +797,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
     if (!make_tmap(&ta, wq16, N, K, kBN)) return cudaErrorNotSupported;
     return launch_prefill_t<false, true, 256>(ta, q16, a, st);
   }
-  if (QG_SKINNY == 2)  // tuning: the whole GEMM as 16-row tiles
-    return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16), a.d32, a.ldd,
-                              N, out, out_f32, ldo, skinny_tb(M, N, num_sms()), err, st);
-  const PrefillPlan p =
-      QG_FORCE_BM ? PrefillPlan{0, QG_FORCE_BM} : plan_prefill_w8a8(M, N, num_sms());
+  const PrefillPlan p = plan_as_built(M, N, num_sms());
   const int64_t n0 = (int64_t)p.nt_wide * kBN;  // first weight row of the narrow part
   if (n0 > 0) {
     LargeArgs aw = a;
@@ -786,7 +812,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   an.d32 = a.d32 + n0 * a.ldd;
   an.out = out_f32 ? (void*)(reinterpret_cast<float*>(out) + n0)
                    : (void*)(reinterpret_cast<uint16_t*>(out) + n0);
-  if (p.bm_tail == 0 || QG_SKINNY == 1)  // 16-row tiles (legacy fp16 MMA)
+  if (p.bm_tail == 0)  // 16-row tiles (legacy fp16 MMA)
     return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16 + n0 * K * 2),
                               an.d32, an.ldd, an.N, an.out, out_f32, ldo,
                               skinny_tb(M, an.N, num_sms()), err, st);

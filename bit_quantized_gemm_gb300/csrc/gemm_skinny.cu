@@ -269,12 +269,10 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
   if (!make_tmap(&ta, wq16, a.N, a.K, kSkRows) || !make_tmap(&tb, q16, a.M, a.K, TB))
     return cudaErrorNotSupported;
   auto kern = skinny_gemm_kernel<TB>;
-  static bool configured = false;  // once per process (idempotent if raced)
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  static std::atomic<uint64_t> attr_set{0};
+  {
+    const cudaError_t e = smem_attr_once_per_device(kern, (int)C::kSmem, attr_set);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const dim3 grid((unsigned)ceil_div(a.N, kSkRows), (unsigned)ceil_div(a.M, TB));
   kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tb, a);

@@ -469,13 +469,11 @@ static cudaError_t launch_decode_cfg(const DecodeArgs& a, bool pdl, cudaStream_t
   // two-tile kernels (9..16 rows) carry twice the activation rows and stash
   constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K>();
   auto kern = decode_gemm_kernel<TT, kQ4K, kDebug>;
-  static bool configured = false;  // once per process (idempotent if raced)
-  if (!configured) {
-    // the attribute only caps the launch size; occupancy follows the size passed at launch
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         200 * 1024);
+  // the attribute only caps the launch size; occupancy follows the size passed at launch
+  static std::atomic<uint64_t> attr_set{0};
+  {
+    const cudaError_t e = smem_attr_once_per_device(kern, 200 * 1024, attr_set);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   DecodeArgs b = a;
   const int mrows = a.M < TT * 8 ? a.M : TT * 8;

@@ -1,10 +1,11 @@
 // qg_common.cuh -- shared device helpers for the quantized linear layer
 // kernels: the packed-weight layout, bounded mbarrier waits, TMA, tcgen05
-// (tensor memory + 5th-generation MMA) and legacy int8 MMA wrappers.
+// (tensor memory + 5th-generation MMA) and legacy fp16 MMA wrappers.
 //
 // Everything here is hand-written inline PTX for sm_103a.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -90,6 +91,21 @@ struct Q4kLayout {
     total = align_up(off_dm32 + N * B * 4, 256);
   }
 };
+
+// cudaFuncAttributeMaxDynamicSharedMemorySize for `kern`, set once per device
+// (the attribute belongs to the function on the current device). `done`
+// holds one bit per device 0..63; devices past 63 set it on every call.
+template <typename Kern>
+inline cudaError_t smem_attr_once_per_device(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Kernels that wait on barriers receive the address of the library's device
 // error word (one per device) and OR a code into it when a wait gives up.
@@ -300,16 +316,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
       : "memory");
 }
 
-// Warp-group register reallocation (all 128 threads of a warp group execute it).
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
 // Bits: [0,14) start>>4, [16,30) leading offset>>4 (unused for swizzled
@@ -366,36 +372,6 @@ __device__ __forceinline__ uint32_t nib_pair_to_f16x2(uint32_t w) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x64006400u));
   return r;
-}
-
-// ---------------------------------------------------------------------------
-// Legacy warp-level int8 MMA (exact int32 accumulate): m16n8k32.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const int (&a)[4], int b0, int b1,
-                                             const int (&c)[4]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%11,%12,%13};"
-      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(c[0]), "r"(c[1]),
-        "r"(c[2]), "r"(c[3]));
-}
-
-// (float)i for |i| < 2^22, exactly, from an int32 accumulator that started at
-// the bit pattern of 1.5*2^23: the integer add lands in the mantissa.
-constexpr int kMagicBits = 0x4B400000;
-constexpr float kMagicF = 12582912.0f;
-__device__ __forceinline__ float magic_to_float(int acc_bits) {
-  return __int_as_float(acc_bits) - kMagicF;
-}
-
-// Streaming 128-bit global load that bypasses L1 allocation.
-__device__ __forceinline__ int4 ldg_stream(const void* p) {
-  int4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 
 // Read-only 4-byte global load as volatile asm: it stays where it is written

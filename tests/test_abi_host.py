@@ -229,8 +229,6 @@ def test_prefill_wave_plan_invariants(L):
         assert rows == N or rows % 128 == 0        # whole 128-row tiles, or everything
         assert (kind is None) == (rows == N)       # a second launch only for leftover rows
         assert tokens == 0 if kind is None else tokens in (32, 64, 128)
-        launches = 1 if kind is None or rows == 0 else 2
-        assert launches in (1, 2)
     with pytest.raises(qg.QGError):
         _lib.prefill_plan(0, 128, 152)
     with pytest.raises(qg.QGError):

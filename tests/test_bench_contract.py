@@ -23,7 +23,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference"
     assert d["unit"] == "TOPS" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "prefill_4b_w8a8"
+    assert d["config"]["workload"] == "prefill_27b_w8a8"
+    assert d["config"]["shapes"] == [[8192, 5120, 17408], [8192, 17408, 5120]]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
     assert cb["value"] == d["value"] and cb["unit"] == d["unit"]

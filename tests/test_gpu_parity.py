@@ -214,6 +214,20 @@ def test_w8a8_batch_invariance_and_paths():
     assert np.array_equal(full_s, full_l)
 
 
+def test_launch_count_follows_the_wave_plan():
+    """qg_gemm_launch_count on this GPU equals the launches of the plan the
+    host query gives for its SM count (two when a narrow part follows a wide
+    launch)."""
+    from bit_quantized_gemm_gb300 import _lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for M, K, N in [(8192, 5120, 17408), (8192, 17408, 5120), (2048, 2560, 9728),
+                    (2048, 9728, 2560), (64, 5120, 17408), (300, 640, 520), (4096, 5120, 17408)]:
+        rows, kind, _ = _lib.prefill_plan(M, N, sms)
+        want = 2 if (kind is not None and rows > 0) else 1
+        assert qg.gemm_launch_count("q8_0", M, K, N) == want, (M, K, N)
+        assert qg.gemm_launch_count("q8_0", M, K, N, path="small") == -(-M // 16)
+
+
 # --------------------------------------------------------------------- W4A8
 def gpu_w4a8(bits, sblocks, N, path, out_dtype=torch.bfloat16):
     K = bits.shape[1]
