@@ -80,11 +80,17 @@ namespace qg {
 #ifndef QG_CHUNK
 #define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
 #endif
+#ifndef QG_WARP_ARRIVE
+#define QG_WARP_ARRIVE 0  // 1: epilogue hand-backs as one arrival per warp (after a warp sync)
+#endif
+constexpr uint32_t kEpiArrivalsPerWarp = QG_WARP_ARRIVE ? 1 : 32;
 constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 64;       // K per stage
-constexpr int kEpiWarps = QG_EPI_WARPS;  // multiple of 4 (tensor-memory lane quarters)
 constexpr int kFirstEpiWarp = 3;         // warp 0 producer, warps 1-2 MMA issuers
-constexpr int kLThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+// Epilogue warps of a tile width (a multiple of 4: tensor-memory lane
+// quarters); QG_EPI_WARPS applies to tiles of 128 tokens and more.
+__host__ __device__ constexpr int epi_warps_for(int bm) { return bm >= 128 ? QG_EPI_WARPS : 8; }
+__host__ __device__ constexpr int threads_for(int bm) { return 32 * (kFirstEpiWarp + epi_warps_for(bm)); }
 constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
 constexpr int kCtasPerSm = QG_CTAS_PER_SM;  // CTAs sharing an SM (and its tensor memory)
 constexpr uint32_t kTmemCols = 512 / kCtasPerSm;
@@ -97,6 +103,8 @@ template <int BM>
 struct LargeCfg {
   static_assert(BM % 16 == 0 && BM >= 32 && BM <= 256 && kTmemCols % BM == 0, "tile width");
   static constexpr int kBM = BM;
+  static constexpr int kEpiWarps = epi_warps_for(BM);
+  static constexpr int kThreads = threads_for(BM);
   // per-block accumulators in this CTA's tensor memory (at most 8)
   static constexpr int kTBufs = kTmemCols / BM < 8 ? kTmemCols / BM : 8;
   static constexpr uint32_t kStageBBytes = BM * kBK * 2;
@@ -111,7 +119,9 @@ struct LargeCfg {
 template <bool kQ4K, int BM>
 __host__ __device__ constexpr int stages_for() {
   constexpr int kCols = LargeCfg<BM>::kColsPerThread;
-  constexpr int kFixed = (QG_TMA_OUT ? 2 * kCols * kBN * 2 : 16) + (kQ4K ? kAsumRing : 1) * BM * 4 +
+  constexpr int kEpiWarps = LargeCfg<BM>::kEpiWarps;
+  constexpr int kFixed = (QG_TMA_OUT ? (kEpiWarps / 4) * kCols * kBN * 2 : 16) +
+                         (kQ4K ? kAsumRing : 1) * BM * 4 +
                          kEpiWarps * kCols * 4 + 2048;  // + barriers and alignment slack
   constexpr int kPer = (int)kStageABytes + BM * kBK * 2;
   constexpr int n = (226 * 1024 - kFixed) / kPer;
@@ -122,13 +132,15 @@ __host__ __device__ constexpr int stages_for() {
 
 template <bool kQ4K, int BM>
 struct LargeSmem {
+  static constexpr int kEpiWarps = LargeCfg<BM>::kEpiWarps;
   static constexpr int kStages = stages_for<kQ4K, BM>();
   static constexpr int kCols = LargeCfg<BM>::kColsPerThread;
   uint8_t a[kStages][kStageABytes];
   uint8_t b[kStages][LargeCfg<BM>::kStageBBytes];
-  // bf16 output tile staged for the TMA store: per epilogue half, kCols token
-  // rows x 128 weight rows (row-major, the store's box)
-  uint16_t ostage[QG_TMA_OUT ? 2 : 1][QG_TMA_OUT ? kCols * kBN : 8];
+  // bf16 output tile staged for the TMA store: per group of four epilogue
+  // warps (a column slice of the tile), kCols token rows x 128 weight rows
+  // (row-major, the store's box)
+  uint16_t ostage[QG_TMA_OUT ? kEpiWarps / 4 : 1][QG_TMA_OUT ? kCols * kBN : 8];
   float asum[kQ4K ? kAsumRing : 1][BM];
   float sa_stage[kEpiWarps][kCols];  // per epilogue warp: its tile's activation scales
   uint64_t full[kStages], empty[kStages];
@@ -173,11 +185,12 @@ __device__ __forceinline__ void tile_coords(int tile, int MT, int NT, int kGroup
 }
 
 template <bool kQ4K, bool kDebug, int BM>
-__global__ void __launch_bounds__(kLThreads, kCtasPerSm)
+__global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const LargeArgs args) {
   using C = LargeCfg<BM>;
+  constexpr int kEpiWarps = C::kEpiWarps;
   constexpr int kStages = stages_for<kQ4K, BM>();
   constexpr bool kStageMode = C::kTBufs % 4 == 0;
   constexpr int kBM = C::kBM;
@@ -201,11 +214,11 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
     }
     for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpiWarps * 32);  // every epilogue thread hands back its loads
+      mbar_init(&S.tempty[i], kEpiWarps * kEpiArrivalsPerWarp);  // epilogue hand-backs
     }
     for (int i = 0; i < kAsumRing; ++i) {
       mbar_init(&S.afull[i], 32);
-      mbar_init(&S.aempty[i], kEpiWarps * 32);
+      mbar_init(&S.aempty[i], kEpiWarps * kEpiArrivalsPerWarp);
     }
     mbar_init(&S.mdrain[0], 1);
     mbar_init(&S.mdrain[1], 1);
@@ -457,7 +470,12 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
             // all of this thread's columns of the block are in registers:
             // each thread hands its part of the buffer back (no warp sync)
             tc_fence_before();
-            mbar_arrive(&S.tempty[tb]);
+            if (QG_WARP_ARRIVE) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&S.tempty[tb]);
+            } else {
+              mbar_arrive(&S.tempty[tb]);
+            }
           }
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
@@ -487,7 +505,12 @@ __global__ void __launch_bounds__(kLThreads, kCtasPerSm)
           }
         }
         if (kQ4K) {
-          mbar_arrive(&S.aempty[aslot]);  // this thread's reads of the slot are done
+          if (QG_WARP_ARRIVE) {  // the warp's reads of the slot are done
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.aempty[aslot]);
+          } else {
+            mbar_arrive(&S.aempty[aslot]);  // this thread's reads of the slot are done
+          }
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
       }
@@ -666,7 +689,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, cons
   const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
   const int slots = num_sms() * kCtasPerSm;
   const int grid = tiles < slots ? tiles : slots;
-  kern<<<grid, kLThreads, kSmem, st>>>(ta, tb, to, args);
+  kern<<<grid, LargeCfg<BM>::kThreads, kSmem, st>>>(ta, tb, to, args);
   return cudaGetLastError();
 }
 
