@@ -653,17 +653,6 @@ static bool make_out_tmap(CUtensorMap* map, void* base, int64_t M, int64_t N, in
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int num_sms() {
-  static int cached[64] = {};
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  n = n > 0 ? n : 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
-}
-
 template <bool kQ4K, bool kDebug, int BM>
 static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, const LargeArgs& a,
                                    cudaStream_t st) {

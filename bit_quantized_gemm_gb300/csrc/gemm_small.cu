@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   const int B4 = (B + 3) & ~3;
   const int J = B / 8;
   const int nstages = (B + kSBlk - 1) / kSBlk;
-  const int64_t g = blockIdx.x;
   const int M = a.M;
   const int gr = lane >> 2, c = lane & 3;
 
@@ -211,9 +210,15 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     // requested, and stage 0's activations would queue behind them. An
     // ordinary launch requests each stage's activations right after its
     // weights.
+    // The CTA's groups are g = blockIdx.x, + gridDim.x, ... (grid capped at
+    // the resident CTAs): the ring streams from one group into the next
+    // without draining. The activation slices are the same for every group.
     const int P = a.pdl ? min(min(nstages, NW), 3) : 1;
     int st = 0;
     uint32_t ph = 0;
+    bool ok = true;
+    bool first = true;
+    for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x, first = false) {
     for (int s = 0; s < nstages; ++s) {
       const int blk0 = s * kSBlk;
       const int nb = min(kSBlk, B - blk0);
@@ -221,7 +226,6 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       uint32_t bytes = !kQ4K ? nb * 512 + ((nb + 3) / 4) * 128 : nb * 256 + (nb / 8) * 256;
       bytes += mrows * nb * 32;
       if (kQ4K) bytes += mrows * nb * 4;
-      bool ok = true;
       if (lane == 0) {
         ok = mbar_wait(&empty[st], ph ^ 1, a.err);
         if (ok) {
@@ -239,14 +243,15 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (s + 1 == P) {
-        // the first P stages are slots 0..P-1 of the first round
+      if (first && s + 1 == P) {
+        // the first group's first P stages are slots 0..P-1 of the first round
         if (a.pdl) griddep_wait();
         for (int r = 0; r < P; ++r) copy_acts(r, r);
-      } else if (s >= P) {
+      } else if (!first || s >= P) {
         copy_acts(s, st);
       }
       if (++st == NW) { st = 0; ph ^= 1; }
+    }
     }
     // drain: every stage released before the CTA exits
     if (lane == 0) {
@@ -264,11 +269,13 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     int st = 0, xs = 0;
     uint32_t ph = 0, xph = 0;
+    bool ok = true;
+    for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x) {
     for (int s = 0; s < nstages; ++s) {
       const int blk0 = s * kSBlk;
       const int nb = min(kSBlk, B - blk0);
-      if (!mbar_wait(&full[st], ph, a.err)) break;
-      if (!mbar_wait(&xempty[xs], xph ^ 1, a.err)) break;
+      ok = mbar_wait(&full[st], ph, a.err) && mbar_wait(&xempty[xs], xph ^ 1, a.err);
+      if (!ok) break;
       const uint8_t* base = smem + st * SBY;
       float* stash = stash_base + xs * (L::kSlotBytes / 4);
       // this warp's blocks: fragments of all of them first (rows past nb
@@ -352,17 +359,19 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       if (++st == NW) { st = 0; ph ^= 1; }
       if (++xs == 2) { xs = 0; xph ^= 1; }
     }
+    }
     return;
   }
 
   // ----------------------------------------------------------- chain warp
+  bool ok = true;
+  int st = 0, xs = 0;
+  uint32_t ph = 0, xph = 0;
+  for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x) {
   const int n0 = (int)(16 * g + gr), n1 = n0 + 8;
   float2 acc[TT][2];  // [tile][row n0 / n1]: tokens 8t+2c, 8t+2c+1
 #pragma unroll
   for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
-  bool ok = true;
-  int st = 0, xs = 0;
-  uint32_t ph = 0, xph = 0;
   for (int s = 0; s < nstages && ok; ++s) {
     const int blk0 = s * kSBlk;
     const int nb = min(kSBlk, B - blk0);
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     if (++xs == 2) { xs = 0; xph ^= 1; }
   }
 
-  if (kDebug || !ok) return;
+  if (kDebug || !ok) continue;
   griddep_wait();  // the activation scales come from the preceding quantize kernel
 #pragma unroll
   for (int t = 0; t < TT; ++t) {
@@ -460,6 +469,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
           reinterpret_cast<uint16_t*>(a.out)[(int64_t)m * a.ldo + n] = f32_to_bf16_rne(y);
       }
     }
+  }
   }
 }
 
@@ -479,7 +489,10 @@ static cudaError_t launch_decode_cfg(const DecodeArgs& a, bool pdl, cudaStream_t
   const int mrows = a.M < TT * 8 ? a.M : TT * 8;
   b.nw = L::num_stages(mrows, kBudget);
   b.pdl = pdl ? 1 : 0;
-  dim3 grid((unsigned)a.G), block(32 * (kCompWarps + 2));
+  // persistent: at most the CTAs that are resident at once; each walks
+  // groups blockIdx.x, + gridDim.x, ...
+  const int64_t slots = (int64_t)num_sms() * dec_ctas<kQ4K>();
+  dim3 grid((unsigned)(a.G < slots ? a.G : slots)), block(32 * (kCompWarps + 2));
   if (!pdl) {
     kern<<<grid, block, L::total(mrows, b.nw), st>>>(b);
     return cudaGetLastError();

@@ -92,6 +92,21 @@ struct Q4kLayout {
   }
 };
 
+// SM count of the current device (cached per device)
+inline int num_sms() {
+  static std::atomic<int> cached[64] = {};
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 // cudaFuncAttributeMaxDynamicSharedMemorySize for `kern`, set once per device
 // (the attribute belongs to the function on the current device). `done`
 // holds one bit per device 0..63; devices past 63 set it on every call.
