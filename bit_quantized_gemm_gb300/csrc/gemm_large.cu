@@ -80,6 +80,9 @@ namespace qg {
 #ifndef QG_CHUNK
 #define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
 #endif
+#ifndef QG_DQ_AHEAD
+#define QG_DQ_AHEAD 0  // W8A8: 0 = scalar scales one block ahead (quads measured 15-55 % slower); W4A8 uses quads, max(this, 1) ahead
+#endif
 #ifndef QG_WARP_ARRIVE
 #define QG_WARP_ARRIVE 0  // 1: epilogue hand-backs as one arrival per warp (after a warp sync)
 #endif
@@ -396,35 +399,41 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
       }
 
       // Weight scales are prefetched; the loads are volatile so the compiler
-      // keeps them where they are written. W8A8: one block ahead (a quad
-      // scheme measured ~15 % slower there: the main loop is sensitive to
-      // its code shape). W4A8: four blocks at a time (one 16-byte load of
-      // d*sc and of dmin*m; rows are 16-byte aligned, K a multiple of 256),
-      // the next quad fetched while the current one is used (+7 %).
+      // keeps them where they are written. kQA > 0: four blocks per 16-byte
+      // load (rows are 16-byte aligned: whole quads of blocks), kQA quads
+      // ahead of their use; W4A8 loads d*sc and dmin*m alike. kQA = 0 (W8A8
+      // only): one scalar load one block ahead.
+      constexpr int kQA = (kQ4K && QG_DQ_AHEAD < 1) ? 1 : QG_DQ_AHEAD;  // W4A8: quads always
+      constexpr int kQR = kQA > 0 ? kQA + 1 : 1;
       float d_next = 0.0f;
-      float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f), m4 = d4, d4n = d4, m4n = d4;
-      if (nvalid) {
-        if (kQ4K) {
-          d4n = ldg_f32x4_pinned(drow);
-          m4n = ldg_f32x4_pinned(mrow);
-        } else {
-          d_next = ldg_f32_pinned(drow);
+      float4 dq[kQR], mq[kQR];
+#pragma unroll
+      for (int i = 0; i < kQR; ++i) {
+        dq[i] = mq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kQA > 0 && nvalid && 4 * i < NB) {
+          dq[i] = ldg_f32x4_pinned(drow + 4 * i);
+          if (kQ4K) mq[i] = ldg_f32x4_pinned(mrow + 4 * i);
         }
       }
+      if (kQA == 0 && nvalid) d_next = ldg_f32_pinned(drow);
       for (int blk = 0; blk < NB && ok; ++blk) {
         float dw, ndm = 0.0f;
-        if (kQ4K) {
-          if ((blk & 3) == 0) {
-            d4 = d4n;
-            m4 = m4n;
-            if (blk + 4 < NB && nvalid) {
-              d4n = ldg_f32x4_pinned(drow + blk + 4);
-              m4n = ldg_f32x4_pinned(mrow + blk + 4);
+        if (kQA > 0) {
+          if ((blk & 3) == 0 && blk > 0) {
+#pragma unroll
+            for (int i = 0; i + 1 < kQR; ++i) {
+              dq[i] = dq[i + 1];
+              if (kQ4K) mq[i] = mq[i + 1];
+            }
+            const int nxt = blk + 4 * kQA;
+            if (nxt < NB && nvalid) {
+              dq[kQR - 1] = ldg_f32x4_pinned(drow + nxt);
+              if (kQ4K) mq[kQR - 1] = ldg_f32x4_pinned(mrow + nxt);
             }
           }
           const int q = blk & 3;
-          dw = q == 0 ? d4.x : q == 1 ? d4.y : q == 2 ? d4.z : d4.w;
-          ndm = -(q == 0 ? m4.x : q == 1 ? m4.y : q == 2 ? m4.z : m4.w);
+          dw = q == 0 ? dq[0].x : q == 1 ? dq[0].y : q == 2 ? dq[0].z : dq[0].w;
+          if (kQ4K) ndm = -(q == 0 ? mq[0].x : q == 1 ? mq[0].y : q == 2 ? mq[0].z : mq[0].w);
         } else {
           dw = d_next;
           if (blk + 1 < NB && nvalid) d_next = ldg_f32_pinned(drow + blk + 1);

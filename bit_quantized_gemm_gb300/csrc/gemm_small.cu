@@ -69,6 +69,9 @@ __host__ __device__ constexpr int dec_hbatch() { return kQ4K ? QG_DEC_HB_Q4K : 4
 #ifndef QG_DEC_BUDGET_TT2_KB
 #define QG_DEC_BUDGET_TT2_KB 70
 #endif
+#ifndef QG_DEC_CHAIN_UNROLL
+#define QG_DEC_CHAIN_UNROLL 1  // chain warp: a full stage's block quads unrolled
+#endif
 #ifndef QG_DEC_SBLK_Q4K
 #define QG_DEC_SBLK_Q4K 16
 #endif
@@ -382,9 +385,10 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::bsum_off(mrows));
     const float* stash = stash_base + xs * (L::kSlotBytes / 4);
     const float2* scs = reinterpret_cast<const float2*>(stash + L::kXBytes / 4);  // [block][row]
-    // blocks in groups of kG (a quad of Q8_0 scales)
+    // blocks in groups of kG (a quad of Q8_0 scales); a full stage's quads
+    // are unrolled so that later quads' shared loads overlap earlier FMAs
     constexpr int kG = 4;
-    for (int j0 = 0; j0 < nb; j0 += kG) {
+    auto quad = [&](const int j0) {
       float dA[kG], dB[kG], mA[kG], mB[kG];
       if (!kQ4K) {
         const uint4 sc = *reinterpret_cast<const uint4*>(sb + (j0 >> 2) * 128 + gr * 16);
@@ -443,6 +447,13 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
           }
         }
       }
+    
+    };
+    if (QG_DEC_CHAIN_UNROLL && nb == kSBlk) {
+#pragma unroll
+      for (int j0 = 0; j0 < kSBlk; j0 += kG) quad(j0);
+    } else {
+      for (int j0 = 0; j0 < nb; j0 += kG) quad(j0);
     }
     __syncwarp();
     if (lane == 0) {
