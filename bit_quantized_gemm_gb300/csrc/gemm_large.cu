@@ -80,13 +80,6 @@ namespace qg {
 #ifndef QG_CHUNK
 #define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
 #endif
-#ifndef QG_DQ_AHEAD
-#define QG_DQ_AHEAD 0  // W8A8: 0 = scalar scales one block ahead (quads measured 15-55 % slower); W4A8 uses quads, max(this, 1) ahead
-#endif
-#ifndef QG_WARP_ARRIVE
-#define QG_WARP_ARRIVE 0  // 1: epilogue hand-backs as one arrival per warp (after a warp sync)
-#endif
-constexpr uint32_t kEpiArrivalsPerWarp = QG_WARP_ARRIVE ? 1 : 32;
 constexpr int kBN = 128;      // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 64;       // K per stage
 constexpr int kFirstEpiWarp = 3;         // warp 0 producer, warps 1-2 MMA issuers
@@ -217,11 +210,11 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
     }
     for (int i = 0; i < kTBufs; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpiWarps * kEpiArrivalsPerWarp);  // epilogue hand-backs
+      mbar_init(&S.tempty[i], kEpiWarps * 32);  // every epilogue thread hands back its loads
     }
     for (int i = 0; i < kAsumRing; ++i) {
       mbar_init(&S.afull[i], 32);
-      mbar_init(&S.aempty[i], kEpiWarps * kEpiArrivalsPerWarp);
+      mbar_init(&S.aempty[i], kEpiWarps * 32);
     }
     mbar_init(&S.mdrain[0], 1);
     mbar_init(&S.mdrain[1], 1);
@@ -399,11 +392,12 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
       }
 
       // Weight scales are prefetched; the loads are volatile so the compiler
-      // keeps them where they are written. kQA > 0: four blocks per 16-byte
-      // load (rows are 16-byte aligned: whole quads of blocks), kQA quads
-      // ahead of their use; W4A8 loads d*sc and dmin*m alike. kQA = 0 (W8A8
-      // only): one scalar load one block ahead.
-      constexpr int kQA = (kQ4K && QG_DQ_AHEAD < 1) ? 1 : QG_DQ_AHEAD;  // W4A8: quads always
+      // keeps them where they are written. W8A8: one scalar load one block
+      // ahead (quads of four blocks one to three quads ahead, or scalars two
+      // blocks ahead, measured 3-55 % slower: the epilogue loop is tight on
+      // registers). W4A8: four blocks per 16-byte load of d*sc and of dmin*m
+      // (rows are 16-byte aligned: whole quads), one quad ahead of its use.
+      constexpr int kQA = kQ4K ? 1 : 0;
       constexpr int kQR = kQA > 0 ? kQA + 1 : 1;
       float d_next = 0.0f;
       float4 dq[kQR], mq[kQR];
@@ -479,12 +473,7 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
             // all of this thread's columns of the block are in registers:
             // each thread hands its part of the buffer back (no warp sync)
             tc_fence_before();
-            if (QG_WARP_ARRIVE) {
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&S.tempty[tb]);
-            } else {
-              mbar_arrive(&S.tempty[tb]);
-            }
+            mbar_arrive(&S.tempty[tb]);
           }
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
@@ -514,12 +503,7 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           }
         }
         if (kQ4K) {
-          if (QG_WARP_ARRIVE) {  // the warp's reads of the slot are done
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.aempty[aslot]);
-          } else {
-            mbar_arrive(&S.aempty[aslot]);  // this thread's reads of the slot are done
-          }
+          mbar_arrive(&S.aempty[aslot]);  // this thread's reads of the slot are done
           if (++aslot == kAsumRing) { aslot = 0; aphase ^= 1; }
         }
       }
