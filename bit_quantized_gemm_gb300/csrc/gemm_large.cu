@@ -242,6 +242,21 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
     uint32_t aphase = 0;
     bool ok = true;
     uint32_t loaded = 0, load_par = 0;  // per stage: a load was issued; parity of the last one
+    // W4A8: activation block sums of eight blocks for this lane's tokens
+    int4 bs_cur[kQ4K ? kBM / 32 : 1][2], bs_nxt[kQ4K ? kBM / 32 : 1][2];
+    auto load_bs8 = [&](int mt, int blk8, int4 (&dst)[kQ4K ? kBM / 32 : 1][2]) {
+#pragma unroll
+      for (int i = 0; i < kBM / 32; ++i) {
+        const int m = mt * kBM + i * 32 + lane;
+        if (m < M) {
+          const int4* p = reinterpret_cast<const int4*>(args.bsum + (int64_t)m * NB + blk8);
+          dst[i][0] = __ldg(p);
+          dst[i][1] = __ldg(p + 1);
+        } else {
+          dst[i][0] = dst[i][1] = make_int4(0, 0, 0, 0);
+        }
+      }
+    };
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, MT, NT, args.tile_group, mt, nt);
@@ -262,12 +277,25 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           for (int j = 0; j < 2; ++j) {
             const int blk = 2 * s + j;
             if (blk >= NB) break;
+            // the tile's activation block sums come eight blocks per load
+            // round (two 16-byte loads per token: NB and the block index are
+            // multiples of 8), the next eight requested while these are used,
+            // so each round's latency is hidden behind eight blocks
+            if ((blk & 7) == 0) {
+              if (blk == 0) load_bs8(mt, 0, bs_cur);
+              else {
+#pragma unroll
+                for (int i = 0; i < kBM / 32; ++i) { bs_cur[i][0] = bs_nxt[i][0]; bs_cur[i][1] = bs_nxt[i][1]; }
+              }
+              if (blk + 8 < NB) load_bs8(mt, blk + 8, bs_nxt);
+            }
             ok = mbar_wait(&S.aempty[aslot], aphase ^ 1, args.err);
             if (!ok) break;
+            const int q = blk & 7;
 #pragma unroll
             for (int i = 0; i < kBM / 32; ++i) {
-              const int m = mt * kBM + i * 32 + lane;
-              const int v = (m < M) ? __ldg(args.bsum + (int64_t)m * NB + blk) : 0;
+              const int4 w = (q < 4) ? bs_cur[i][0] : bs_cur[i][1];
+              const int v = (q & 3) == 0 ? w.x : (q & 3) == 1 ? w.y : (q & 3) == 2 ? w.z : w.w;
               S.asum[aslot][i * 32 + lane] = (float)v;  // exact: |v| <= 4064
             }
             mbar_arrive(&S.afull[aslot]);
