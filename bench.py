@@ -58,27 +58,29 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 25 ms, each sample
+    timestamped so that the summary can keep those inside a window (the timed
+    region); start it before the warm-up so it is already sampling then."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -88,25 +90,45 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        if not getattr(self, "lines", None):
-            return None
-        sm, smax, reasons = [], 0.0, set()
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    def summary(self, window=None):
+        """Median SM clock, max clock and the throttle reasons seen; samples
+        inside `window` = (t0, t1) (host time.time()) when at least 3 fall in
+        it, else all samples (the warm-up runs the same work)."""
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             try:
-                sm.append(float(f[1]))
-                smax = max(smax, float(f[2]))
+                rows.append((self._when(f[0]), float(f[2]), float(f[3]), f[6:10]))
             except (ValueError, IndexError):
                 continue
-            for name, val in zip(names, f[5:9]):
+        if not rows:
+            return None
+        scope = "timed region"
+        if window is not None:
+            inside = [r for r in rows if r[0] is not None and window[0] <= r[0] <= window[1]]
+            if len(inside) >= 3:
+                rows = inside
+            else:
+                scope = "warm-up and timed region (%d samples inside the timed region)" % len(inside)
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[3]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in rows),
+                "sm_max_mhz": max(r[2] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "window": scope}
 
 
 def source_sha(path):
@@ -668,9 +690,6 @@ def main():
         flush_buf.fill_(1)
 
     layers = make_step_inputs(dev)
-    for _ in range(max(args.warmup, 3)):
-        run_step(layers)
-    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
@@ -678,9 +697,13 @@ def main():
         torch.cuda.synchronize()
 
     step_ms, gemm_ms = [], []
-    barrier()
     with ClockSampler(local) as clk:
+        for _ in range(max(args.warmup, 3)):
+            run_step(layers)
+        torch.cuda.synchronize()
+        barrier()
         t_wall0 = time.perf_counter()
+        t_unix0 = time.time()
         for _ in range(args.steps):
             flush()
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -694,7 +717,8 @@ def main():
             gemm_ms.append([e0.elapsed_time(e1) for e0, e1 in ev])
         barrier()
         t_wall = time.perf_counter() - t_wall0
-    clocks = clk.summary()
+        t_unix1 = time.time()
+    clocks = clk.summary((t_unix0, t_unix1))
     ms = reduce_max(sum(step_ms) / len(step_ms), world)
     ops = step_ops()
     value = job_value(ops, world, ms)

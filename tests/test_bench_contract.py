@@ -44,3 +44,26 @@ def test_capture_hash_follows_code_not_comments(tmp_path):
     assert bench.source_sha(str(a)) == bench.source_sha(str(b))
     assert bench.source_sha(str(a)) != bench.source_sha(str(c))
     assert bench.sources_sha([str(a), str(c)]) != bench.sources_sha([str(c), str(a)])
+
+
+def test_clock_summary_keeps_the_timed_window():
+    """The clock record keeps the samples inside the timed region when there
+    are enough of them, reports throttle reasons seen there, and falls back
+    to all samples (warm-up included) otherwise."""
+    import bench
+    import datetime
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5).timestamp()
+
+    def line(dt, mhz, power_cap):
+        stamp = datetime.datetime.fromtimestamp(t0 + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        cap = "Active" if power_cap else "Not Active"
+        return "%s, 0, %d, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, %s" % (stamp, mhz, cap)
+
+    c = bench.ClockSampler(0)
+    c.lines = [line(0.00, 1500, True), line(0.10, 2000, False), line(0.15, 2010, False),
+               line(0.20, 2020, False), line(0.50, 1400, True)]
+    s = c.summary((t0 + 0.05, t0 + 0.3))
+    assert s["samples"] == 3 and s["sm_mhz"] == 2010 and s["reasons"] == []
+    assert s["window"] == "timed region"
+    s = c.summary((t0 + 0.05, t0 + 0.12))          # one sample inside: all samples
+    assert s["samples"] == 5 and "sw_power_cap" in s["reasons"]
