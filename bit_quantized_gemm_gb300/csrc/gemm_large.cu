@@ -465,9 +465,6 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
         }
         const int tb = kStageMode ? (2 * (ti * NS + (blk >> 1)) + (blk & 1)) % kTBufs
                                   : blk % kTBufs;
-        // `ok` is uniform across the warp without a vote: every lane runs the
-        // same polling loop on the same barrier and sees the same answers (a
-        // per-block warp vote or shuffle here costs about 9 % of the time)
         if (kStageMode && kQ4K && QG_PAIR_WAIT) {
           // one issuer commits both blocks of a stage, and the second commit
           // arrives only after all of that issuer's earlier MMAs: a wait on
@@ -481,12 +478,17 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
             ok = mbar_wait(&S.tfull[tw], (tph >> tw) & 1u, args.err);
             tph ^= (1u << tb) | (pair ? (1u << tw) : 0u);
           }
+          if (ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
+          if (!ok) break;
         } else {
+          // `ok` is uniform across the warp without a vote: every lane runs the
+          // same polling loop on the same barrier and sees the same answers (a
+          // per-block warp vote or shuffle here costs about 9 % of the time)
           ok = mbar_wait(&S.tfull[tb], (tph >> tb) & 1u, args.err);
+          if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
+          if (!ok) break;
           tph ^= 1u << tb;
         }
-        if (kQ4K && ok) ok = mbar_wait(&S.afull[aslot], aphase, args.err);
-        if (!ok) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(tb * kBM + half * kColsPerThread);
