@@ -302,6 +302,15 @@ def timed_graph(fns, reps, batches=5):
     return times
 
 
+def graph_fields(fns, algo_bytes, hbm):
+    """The same back-to-back launches replayed from a CUDA graph, as a decode
+    loop would issue them: without the stream's per-launch gap (~2 us on
+    this GPU between eagerly launched kernels)."""
+    t = statistics.median(timed_graph(fns, 40))
+    gbs = algo_bytes / t / 1e6
+    return {"ms_graph": round(t, 5), "gbs_graph": round(gbs, 1), "frac_graph": round(gbs / hbm, 4)}
+
+
 def bench_rows(dev, flush, hbm, tf_burst, quick):
     """The other workloads of the layer, per launch (GEMM kernel only)."""
     import bit_quantized_gemm_gb300 as qg
@@ -336,6 +345,7 @@ def bench_rows(dev, flush, hbm, tf_burst, quick):
                 algo = wbytes + M * K + 4 * M + 2 * M * N
                 gbs = algo / t / 1e6
                 r.update({"gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / hbm, 4)})
+                r.update(graph_fields(fns, algo, hbm))
             else:
                 r.update({"bound": "tensor", "frac": round(ops / t / 1e9 / tf_burst, 4)})
             rows[key] = r
@@ -371,6 +381,7 @@ def bench_rows(dev, flush, hbm, tf_burst, quick):
             algo = N * K // 256 * 144 + M * K + 4 * M + 4 * M * (K // 32) + 2 * M * N
             gbs = algo / t / 1e6
             r.update({"gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / hbm, 4)})
+            r.update(graph_fields(fns, algo, hbm))
         else:
             r.update({"bound": "tensor", "frac": round(ops / t / 1e9 / tf_burst, 4)})
         rows["%s_M%d_K%d_N%d" % (name, M, K, N)] = r

@@ -7,20 +7,22 @@
 //
 // Design. For M <= 16 the layer is bound by reading the weights from HBM
 // (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). A CTA owns one group
-// of 16 weight rows and all of K; K is cut into stages of 16 blocks.
+// of 16 weight rows and all of K; K is cut into stages of 16 or 32 blocks.
+// Two kernels share that frame:
 //   * warp 0 (one thread) streams each stage -- the group's contiguous
-//     fragment-order weights and scales, the activation rows (and for W4A8
-//     their block sums) -- into a shared-memory ring with 1-D bulk copies
+//     weights and scales, the activation rows (and for W4A8 their block
+//     sums) -- into a shared-memory ring with 1-D bulk copies
 //     (cp.async.bulk + mbarrier transaction counts);
-//   * warps 1..8 split the stage's blocks (two each): per block one 16-byte
-//     shared load gives the A fragments of two m16n8k16 fp16 MMAs (biased
-//     int8 bytes widened to exact fp16 by byte permutes and one packed
-//     subtract; Q4_K nibbles by shift-and-mask), one 8-byte load per 8-token
-//     tile the token fragment (int8 rows padded to 544 bytes:
-//     conflict-free), and the two MMAs sum the block exactly in fp32 from
-//     zero (|sum| < 2^20). The exact block sums go to a shared stash. (This
-//     GPU runs legacy fp16 MMAs at 4x the rate of legacy int8 MMAs, which
-//     are no faster than dp4a, so int8 values travel as fp16 here);
+//   * warps 1..8 compute the stage's exact block sums into a shared stash:
+//     - up to 4 rows, decode_dp4a_kernel: one lane per
+//       weight row and block, eight dp4a per token on the row's 32 int8
+//       values (W4A8: its 32 nibbles masked into low and high bytes), no
+//       widening; the W4A8 lane also decodes its row's d*sc and dmin*m;
+//     - more rows, decode_gemm_kernel: two m16n8k16 fp16 MMAs per block and
+//       8-token tile (int8 widened to exact fp16 by byte permutes and one
+//       packed subtract; nibbles by mask-or and one packed subtract or
+//       multiply-add); legacy fp16 MMAs run at 4x the legacy int8 MMA rate,
+//       which is that of dp4a; every sum is below 2^20, exact in fp32;
 //   * warp 9 applies acc = fmaf(isum, d, acc) (Q4_K: then
 //     fmaf(-asum, dmin*m, acc)) over the stage's blocks in ascending order
 //     with packed f32x2 FMAs -- the same chain as the prefill kernel, so both
@@ -36,51 +38,69 @@ namespace qg {
 
 constexpr int kCompWarps = 8;      // compute warps per CTA
 
-// K blocks per pipeline stage: 16 for both formats (8 KB of Q8_0 weights,
-// 4 KB of Q4_K nibbles per 16-row group). Q4_K once took 32 to halve the
-// per-stage overhead, but its stash then left room for two stages in
-// flight: 16 blocks measured 43 % faster at 16 rows, equal at 1 and 8.
+// K blocks per pipeline stage. MMA tiles: 16 for both formats (8 KB of Q8_0
+// weights, 4 KB of Q4_K nibbles per 16-row group); Q4_K once took 32, but
+// its stash then left room for two stages in flight (16 measured 43 %
+// faster at 16 rows, equal at 1 and 8). Integer dot products: 16 for Q8_0,
+// 32 for Q4_K, whose 4 KB stages are otherwise too short for the fixed
+// per-stage work (barrier waits, hand-over) of every warp.
 #ifndef QG_DEC_SBLK_Q8
 #define QG_DEC_SBLK_Q8 16
 #endif
+#ifndef QG_DEC_SBLK_Q4K
+#define QG_DEC_SBLK_Q4K 16
+#endif
+#ifndef QG_DEC_SBLK_DP4A_Q8
+#define QG_DEC_SBLK_DP4A_Q8 16
+#endif
+#ifndef QG_DEC_SBLK_DP4A_Q4K
+#define QG_DEC_SBLK_DP4A_Q4K 32
+#endif
+template <bool kQ4K, bool kDp4a>
+__host__ __device__ constexpr int sblk() {
+  return kDp4a ? (kQ4K ? QG_DEC_SBLK_DP4A_Q4K : QG_DEC_SBLK_DP4A_Q8)
+               : (kQ4K ? QG_DEC_SBLK_Q4K : QG_DEC_SBLK_Q8);
+}
 // CTAs of 320 threads resident per SM (registers and shared memory are
 // budgeted for it)
 #ifndef QG_DEC_CTAS_Q4K
 #define QG_DEC_CTAS_Q4K 3
 #endif
-template <bool kQ4K>
-__host__ __device__ constexpr int dec_ctas() { return kQ4K ? QG_DEC_CTAS_Q4K : 3; }
-template <bool kQ4K>
-constexpr int dec_smem_budget() { return dec_ctas<kQ4K>() == 2 ? 110 * 1024 : 70 * 1024; }
-// Blocks a compute warp converts before their MMAs, and blocks whose sums the
-// chain warp loads before their FMAs: all of a warp's blocks / 4 for Q8_0,
-// one at a time for Q4_K (whose conversions and sub-block terms need the
-// registers; batching measured slower there).
-#ifndef QG_DEC_CB_Q4K
-#define QG_DEC_CB_Q4K 1
+#ifndef QG_DEC_CTAS_Q8
+#define QG_DEC_CTAS_Q8 3
 #endif
 template <bool kQ4K>
-__host__ __device__ constexpr int dec_cbatch() { return kQ4K ? QG_DEC_CB_Q4K : 32; }
+__host__ __device__ constexpr int dec_ctas() { return kQ4K ? QG_DEC_CTAS_Q4K : QG_DEC_CTAS_Q8; }
+template <bool kQ4K>
+constexpr int dec_smem_budget() { return dec_ctas<kQ4K>() == 2 ? 110 * 1024 : 70 * 1024; }
+// MMA tiles: blocks whose sums the chain warp loads before their FMAs: 4 for
+// Q8_0, one at a time for Q4_K (whose sub-block terms need the registers).
 #ifndef QG_DEC_HB_Q4K
 #define QG_DEC_HB_Q4K 1
 #endif
 template <bool kQ4K>
 __host__ __device__ constexpr int dec_hbatch() { return kQ4K ? QG_DEC_HB_Q4K : 4; }
+// Rows up to which the integer dot-product kernel runs (one lane per weight
+// row; each token's 32 activation bytes of a block are loaded by every row's
+// lane) rather than fp16 MMA tiles (weights widened once per 8-token tile,
+// activations loaded once per tile); at most kDp4aMaxM.
+constexpr int kDp4aMaxM = 4;
+#ifndef QG_DEC_DP4A_MAX_Q8
+#define QG_DEC_DP4A_MAX_Q8 4
+#endif
+#ifndef QG_DEC_DP4A_MAX_Q4K
+#define QG_DEC_DP4A_MAX_Q4K 4
+#endif
+template <bool kQ4K>
+constexpr int dec_dp4a_max_m() { return kQ4K ? QG_DEC_DP4A_MAX_Q4K : QG_DEC_DP4A_MAX_Q8; }
+static_assert(QG_DEC_DP4A_MAX_Q8 <= kDp4aMaxM && QG_DEC_DP4A_MAX_Q4K <= kDp4aMaxM,
+              "the integer kernel's stash and chain hold at most four tokens");
 #ifndef QG_DEC_BUDGET_TT2_KB
 #define QG_DEC_BUDGET_TT2_KB 70
 #endif
 #ifndef QG_DEC_CHAIN_UNROLL
 #define QG_DEC_CHAIN_UNROLL 1  // chain warp: a full stage's block quads unrolled
 #endif
-#ifndef QG_DEC_SBLK_Q4K
-#define QG_DEC_SBLK_Q4K 16
-#endif
-template <bool kQ4K>
-__host__ __device__ constexpr int sblk() { return kQ4K ? QG_DEC_SBLK_Q4K : QG_DEC_SBLK_Q8; }
-// bytes per activation row in a stage: 32 per block + 32 of padding, so the
-// eight rows one 8-byte load touches fall in distinct banks
-template <bool kQ4K>
-__host__ __device__ constexpr int arow() { return sblk<kQ4K>() * 32 + 32; }
 
 __device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -94,19 +114,27 @@ __device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint3
 // Shared-memory layout (offsets depend on M, fixed at launch):
 //   NW weight stages, each: weights | scales | M activation rows | (W4A8) M
 //   block-sum rows -- released by the chain warp;
-//   2 stash slots of exact block sums between compute and chain warps;
+//   2 stash slots between compute and chain warps: exact block sums, and for
+//   W4A8 the rows' d*sc, dmin*m (and, integer kernel, -asum per token);
 //   barriers full[NW], empty[NW], xfull[2], xempty[2].
-template <int TT, bool kQ4K>
+// Stash sums: MMA tiles keep an m16n8 accumulator fragment per block and
+// 8-token tile ([block][tile][lane][4], W4A8 scales [block][row]); the
+// integer kernel keeps, per block, token pair and row, the two sums (W8A8)
+// or the two sums with the row's d*sc and dmin*m (W4A8, one 16-byte load
+// for the chain), and for W4A8 -asum per block and token.
+template <int TT, bool kQ4K, bool kDp4a, int kPairs = 2>
 struct DecodeSmem {
-  static constexpr int kSBlk = sblk<kQ4K>();
-  static constexpr int kARow = arow<kQ4K>();
+  static constexpr int kSBlk = sblk<kQ4K, kDp4a>();
+  // bytes per activation row in a stage: 32 per block + 32 of padding, so the
+  // eight rows one 8-byte load touches fall in distinct banks
+  static constexpr int kARow = kSBlk * 32 + 32;
   static constexpr int kWBytes = kSBlk * (kQ4K ? 256 : 512);  // weights per stage
   static constexpr int kSBytes = kQ4K ? kSBlk / 8 * 256 : kSBlk / 4 * 128;  // scales / headers
-  static constexpr int kXBytes = kSBlk * TT * 32 * 16;          // exact sums of a stash slot
-  // Q4_K: the exact sub-block scales (d*sc, dmin*m) of the 16 rows, per block,
-  // decoded by the compute warps so the chain warp only loads them
-  static constexpr int kScBytes = kQ4K ? kSBlk * 16 * 8 : 0;
-  static constexpr int kSlotBytes = kXBytes + kScBytes;
+  static constexpr int kXBytes =
+      kDp4a ? kSBlk * kPairs * 16 * (kQ4K ? 16 : 8) : kSBlk * TT * 32 * 16;
+  static constexpr int kScBytes = (kQ4K && !kDp4a) ? kSBlk * 16 * 8 : 0;
+  static constexpr int kAsBytes = (kQ4K && kDp4a) ? kSBlk * kDp4aMaxM * 4 : 0;
+  static constexpr int kSlotBytes = kXBytes + kScBytes + kAsBytes;
   static constexpr int kMaxNw = 8;
   static __host__ __device__ int stage_bytes(int mrows) {
     return (int)align_up(kWBytes + kSBytes + mrows * kARow + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
@@ -124,17 +152,65 @@ struct DecodeSmem {
   }
 };
 
-// 6-bit field f (0..15: sc_0..7 then m_0..7) of a Q4_K super-block header
-// held as 16 bytes (d, dmin, then a 96-bit little-endian string of fields in
-// words y, z, w), as a float (exact)
-__device__ __forceinline__ float q4k_field(const uint4& H, int f) {
-  const uint64_t lo = (uint64_t)H.y | ((uint64_t)H.z << 32);
-  const int pos = 6 * f;
-  uint32_t v;
-  if (pos + 6 <= 64) v = (uint32_t)(lo >> pos);
-  else if (pos >= 64) v = H.w >> (pos - 64);
-  else v = (uint32_t)(lo >> pos) | (H.w << (64 - pos));
-  return (float)(v & 63u);
+// Exact integer dot products of four byte pairs (dp4a): both operands signed,
+// or unsigned weights with signed activations.
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Sub-block i's scales of a packed Q4_K row header (d, dmin, then 12-bit
+// units sc_i | m_i << 6 at bits [12i, 12i+12) of words y, z, w): d*sc_i and
+// dmin*m_i, exact products.
+// A 6-bit field f enters as the float 2^23 + f (its bits or'ed into the
+// mantissa of 2^23); fmaf(d, 2^23 + f, -d * 2^23) rounds the exact value d*f,
+// which fits in fp32 (11 + 6 significant bits), so it is d*f exactly.
+__device__ __forceinline__ float2 q4k_scales(const uint4& H, int i) {
+  const uint32_t lo = i < 3 ? H.y : (i < 6 ? H.z : H.w);
+  const uint32_t hi = i < 3 ? H.z : H.w;
+  const uint32_t u = __funnelshift_r(lo, hi, (12 * i) & 31);
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&H.x));
+  const float sc = __uint_as_float((u & 63u) | 0x4B000000u);
+  const float mn = __uint_as_float(((u >> 6) & 63u) | 0x4B000000u);
+  return make_float2(fmaf(dd.x, sc, dd.x * -8388608.0f), fmaf(dd.y, mn, dd.y * -8388608.0f));
+}
+
+// An integer of magnitude below 2^22 as fp32 (exact): added to the bits of
+// 1.5 * 2^23 it lands in the mantissa, and subtracting 1.5 * 2^23 leaves it.
+__device__ __forceinline__ float small_int_to_f32(int v) {
+  return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+// Eight 4-bit values of a packed Q4_K word (byte e: low nibble k = e, high
+// nibble k = 4 + e) as exact fp16 pairs: p0 = (k0, k2), p8 = (k1, k3), p4 =
+// (k4, k6), p12 = (k5, k7). A nibble or'ed into the mantissa of 1024 gives
+// 1024 + q (minus 1024); one in mantissa bits 4..7 gives 1024 + 16q, which
+// one fused multiply-add by 1/16 minus 64 brings back to q.
+__device__ __forceinline__ void nib_word_to_f16(uint32_t w, uint32_t& p0, uint32_t& p8,
+                                                uint32_t& p4, uint32_t& p12) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t l0 = (w & 0x000F000Fu) | 0x64006400u, h0 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t l8 = (w8 & 0x000F000Fu) | 0x64006400u, h8 = (w8 & 0x00F000F0u) | 0x64006400u;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p0) : "r"(l0), "r"(0x64006400u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p8) : "r"(l8), "r"(0x64006400u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p4) : "r"(h0), "r"(0x2C002C00u), "r"(0xD400D400u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p12) : "r"(h8), "r"(0x2C002C00u), "r"(0xD400D400u));
+}
+
+// Four biased bytes (q + 128) as exact fp16 pairs of bytes (0, 2) and (1, 3).
+__device__ __forceinline__ void biased_u8x4_to_f16x4_even_odd(uint32_t u, uint32_t& lo,
+                                                              uint32_t& hi) {
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4240;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4341;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
 struct DecodeArgs {
@@ -153,9 +229,99 @@ struct DecodeArgs {
   int pdl;          // launched as a programmatic dependent of the quantize kernel
 };
 
+// Warp 0 of a decode CTA: streams stage after stage of the CTA's groups into
+// the ring (weights and scales, then the activation rows and, for W4A8,
+// their block sums), and at the end waits until the chain warp has released
+// every stage.
+template <class L, bool kQ4K>
+__device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* smem, int SBY,
+                                               int mrows, uint64_t* full, uint64_t* empty,
+                                               int lane) {
+  constexpr int kSBlk = L::kSBlk;
+  constexpr int kARow = L::kARow;
+  const int NW = a.nw;
+  const int B = a.K / kBlk;
+  const int B4 = (B + 3) & ~3;
+  const int J = B / 8;
+  const int nstages = (B + kSBlk - 1) / kSBlk;
+  // The activation rows (and W4A8 block sums) of stage r into ring slot `slot`.
+  auto copy_acts = [&](int r, int slot) {
+    const int blk0 = r * kSBlk;
+    const int nb = min(kSBlk, B - blk0);
+    uint8_t* base = smem + slot * SBY;
+    for (int m = lane; m < mrows; m += 32) {
+      bulk_copy(base + L::act_off() + m * kARow,
+                a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[slot]);
+      if (kQ4K)
+        bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
+                  nb * 4, &full[slot]);
+    }
+  };
+  // Launched as a programmatic dependent, the weights and scales of the
+  // first P stages are requested before any activation: the quantize kernel
+  // may still be writing the activations, and griddep_wait() returns once it
+  // has completed. P is at most 3: every CTA's first three stages are ~1 us
+  // of HBM time, about what a decode-sized quantize lasts; more would still
+  // be arriving when the activations are requested, and stage 0's
+  // activations would queue behind them. An ordinary launch requests each
+  // stage's activations right after its weights.
+  // The CTA's groups are g = blockIdx.x, + gridDim.x, ... (grid capped at the
+  // resident CTAs): the ring streams from one group into the next without
+  // draining. The activation slices are the same for every group.
+  const int P = a.pdl ? min(min(nstages, NW), 3) : 1;
+  int st = 0;
+  uint32_t ph = 0;
+  bool ok = true;
+  bool first = true;
+  for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x, first = false) {
+    for (int s = 0; s < nstages; ++s) {
+      const int blk0 = s * kSBlk;
+      const int nb = min(kSBlk, B - blk0);
+      uint8_t* base = smem + st * SBY;
+      uint32_t bytes = !kQ4K ? nb * 512 + ((nb + 3) / 4) * 128 : nb * 256 + (nb / 8) * 256;
+      bytes += mrows * nb * 32;
+      if (kQ4K) bytes += mrows * nb * 4;
+      if (lane == 0) {
+        ok = mbar_wait(&empty[st], ph ^ 1, a.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&full[st], bytes);
+          if (!kQ4K) {
+            bulk_copy(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
+            bulk_copy(base + L::kWBytes, a.wscale + (g * (B4 / 4) + blk0 / 4) * 128,
+                      ((nb + 3) / 4) * 128, &full[st]);
+          } else {
+            bulk_copy(base, a.wstream + (g * B + blk0) * 256, nb * 256, &full[st]);
+            bulk_copy(base + L::kWBytes, a.wscale + (g * J + blk0 / 8) * 256, (nb / 8) * 256,
+                      &full[st]);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (first && s + 1 == P) {
+        // the first group's first P stages are slots 0..P-1 of the first round
+        if (a.pdl) griddep_wait();
+        for (int r = 0; r < P; ++r) copy_acts(r, r);
+      } else if (!first || s >= P) {
+        copy_acts(s, st);
+      }
+      if (++st == NW) { st = 0; ph ^= 1; }
+    }
+  }
+  // drain: every stage released before the CTA exits
+  if (lane == 0) {
+    for (int i = 0; i < NW; ++i) {
+      if (!mbar_wait(&empty[st], ph ^ 1, a.err)) break;
+      if (++st == NW) { st = 0; ph ^= 1; }
+    }
+  }
+}
+
+// Decode GEMM on fp16 MMA tiles: 8-token tiles (TT of them), weights
+// widened to fp16 once per tile.
 template <int TT, bool kQ4K, bool kDebug>
 __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const DecodeArgs a) {
-  using L = DecodeSmem<TT, kQ4K>;
+  using L = DecodeSmem<TT, kQ4K, false>;
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
   constexpr int kBlkPerWarp = kSBlk / kCompWarps;
@@ -170,8 +336,6 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.K / kBlk;
-  const int B4 = (B + 3) & ~3;
-  const int J = B / 8;
   const int nstages = (B + kSBlk - 1) / kSBlk;
   const int M = a.M;
   const int gr = lane >> 2, c = lane & 3;
@@ -190,86 +354,13 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   __syncthreads();
 
   if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    // The activation rows (and W4A8 block sums) of stage r into ring slot `slot`.
-    auto copy_acts = [&](int r, int slot) {
-      const int blk0 = r * kSBlk;
-      const int nb = min(kSBlk, B - blk0);
-      uint8_t* base = smem + slot * SBY;
-      for (int m = lane; m < mrows; m += 32) {
-        bulk_copy(base + L::act_off() + m * kARow,
-                  a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[slot]);
-        if (kQ4K)
-          bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
-                    nb * 4, &full[slot]);
-      }
-    };
-    // Launched as a programmatic dependent, the weights and scales of the
-    // first P stages are requested before any activation: the quantize
-    // kernel may still be writing the activations, and griddep_wait()
-    // returns once it has completed. P is at most 3: every CTA's first three
-    // stages are ~1 us of HBM time, about what a decode-sized quantize
-    // lasts; more would still be arriving when the activations are
-    // requested, and stage 0's activations would queue behind them. An
-    // ordinary launch requests each stage's activations right after its
-    // weights.
-    // The CTA's groups are g = blockIdx.x, + gridDim.x, ... (grid capped at
-    // the resident CTAs): the ring streams from one group into the next
-    // without draining. The activation slices are the same for every group.
-    const int P = a.pdl ? min(min(nstages, NW), 3) : 1;
-    int st = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    bool first = true;
-    for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x, first = false) {
-    for (int s = 0; s < nstages; ++s) {
-      const int blk0 = s * kSBlk;
-      const int nb = min(kSBlk, B - blk0);
-      uint8_t* base = smem + st * SBY;
-      uint32_t bytes = !kQ4K ? nb * 512 + ((nb + 3) / 4) * 128 : nb * 256 + (nb / 8) * 256;
-      bytes += mrows * nb * 32;
-      if (kQ4K) bytes += mrows * nb * 4;
-      if (lane == 0) {
-        ok = mbar_wait(&empty[st], ph ^ 1, a.err);
-        if (ok) {
-          mbar_arrive_expect_tx(&full[st], bytes);
-          if (!kQ4K) {
-            bulk_copy(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
-            bulk_copy(base + L::kWBytes, a.wscale + (g * (B4 / 4) + blk0 / 4) * 128,
-                      ((nb + 3) / 4) * 128, &full[st]);
-          } else {
-            bulk_copy(base, a.wstream + (g * (B / 2) + blk0 / 2) * 512, nb * 256, &full[st]);
-            bulk_copy(base + L::kWBytes, a.wscale + (g * J + blk0 / 8) * 256, (nb / 8) * 256,
-                      &full[st]);
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (first && s + 1 == P) {
-        // the first group's first P stages are slots 0..P-1 of the first round
-        if (a.pdl) griddep_wait();
-        for (int r = 0; r < P; ++r) copy_acts(r, r);
-      } else if (!first || s >= P) {
-        copy_acts(s, st);
-      }
-      if (++st == NW) { st = 0; ph ^= 1; }
-    }
-    }
-    // drain: every stage released before the CTA exits
-    if (lane == 0) {
-      for (int i = 0; i < NW; ++i) {
-        if (!mbar_wait(&empty[st], ph ^ 1, a.err)) break;
-        if (++st == NW) { st = 0; ph ^= 1; }
-      }
-    }
+    decode_produce<L, kQ4K>(a, smem, SBY, mrows, full, empty, lane);
     return;
   }
 
   if (warp <= kCompWarps) {
     // ------------------------------------------------------ compute warps
     const int cw = warp - 1;
-    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     int st = 0, xs = 0;
     uint32_t ph = 0, xph = 0;
     bool ok = true;
@@ -281,79 +372,80 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       if (!ok) break;
       const uint8_t* base = smem + st * SBY;
       float* stash = stash_base + xs * (L::kSlotBytes / 4);
-      // this warp's blocks: fragments of all of them first (rows past nb
-      // of a short last stage compute unused sums that are never stored),
-      // so the blocks' load and MMA latencies overlap
-      constexpr int kCB = dec_cbatch<kQ4K>() < kBlkPerWarp ? dec_cbatch<kQ4K>() : kBlkPerWarp;
-#pragma unroll
-      for (int u0 = 0; u0 < kBlkPerWarp; u0 += kCB) {
-      uint32_t a0[kCB][4], a1[kCB][4];  // A fragments, k 0-15 / 16-31
-#pragma unroll
-      for (int u = 0; u < kCB; ++u) {
-        const int j = cw * kBlkPerWarp + u0 + u;
-        if (!kQ4K) {
-          const uint4 w = *reinterpret_cast<const uint4*>(base + j * 512 + lane * 16);
-          // x: row n0 k 8c..+3, y: row n1 k 8c..+3, z: n0 k 8c+4..+7, w: n1 k 8c+4..+7
-          biased_u8x4_to_f16x4(w.x, a0[u][0], a0[u][2]);
-          biased_u8x4_to_f16x4(w.y, a0[u][1], a0[u][3]);
-          biased_u8x4_to_f16x4(w.z, a1[u][0], a1[u][2]);
-          biased_u8x4_to_f16x4(w.w, a1[u][1], a1[u][3]);
-        } else {
-          const uint2 w =
-              *reinterpret_cast<const uint2*>(base + (j >> 1) * 512 + lane * 16 + (j & 1) * 8);
-          a0[u][0] = nib_pair_to_f16x2<0>(w.x);
-          a0[u][1] = nib_pair_to_f16x2<4>(w.x);
-          a0[u][2] = nib_pair_to_f16x2<8>(w.x);
-          a0[u][3] = nib_pair_to_f16x2<12>(w.x);
-          a1[u][0] = nib_pair_to_f16x2<0>(w.y);
-          a1[u][1] = nib_pair_to_f16x2<4>(w.y);
-          a1[u][2] = nib_pair_to_f16x2<8>(w.y);
-          a1[u][3] = nib_pair_to_f16x2<12>(w.y);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const int mrow = 8 * t + gr;  // token of this lane's B fragment
-#pragma unroll
-        for (int u = 0; u < kCB; ++u) {
-          const int j = cw * kBlkPerWarp + u0 + u;
-          uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;
-          if (mrow < M) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(
-                base + L::act_off() + mrow * kARow + c * 8 + j * 32);
-            biased_u8x4_to_f16x4(bv.x ^ 0x80808080u, b00, b01);
-            biased_u8x4_to_f16x4(bv.y ^ 0x80808080u, b10, b11);
-          }
-          float d[4];
-          mma_f16_16816(d, a0[u], b00, b01, zero4);
-          mma_f16_16816(d, a1[u], b10, b11, d);
-          // d: (n0, tok 8t+2c), (n0, 8t+2c+1), (n1, 8t+2c), (n1, 8t+2c+1): exact sums
-          if (j < nb)
-            *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
-                make_float4(d[0], d[1], d[2], d[3]);
-          if (kDebug && j < nb) {
-            const int b = blk0 + j;
-            const int n0 = (int)(16 * g + gr), mc0 = 8 * t + 2 * c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int m = mc0 + (i & 1), n = n0 + ((i < 2) ? 0 : 8);
-              if (m < M && n < a.N) a.dbg[((int64_t)m * a.N + n) * B + b] = __float2int_rn(d[i]);
-            }
-          }
-        }
-      }
-      }
-      if (kQ4K && lane < 16) {
-        // this warp's blocks: row `lane`'s d*sc and dmin*m (exact products)
-        float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
+      {
+        // two m16n8k16 fp16 MMAs per block and 8-token tile (this warp's
+        // blocks 2cw, 2cw+1; their fragments first, so the blocks' load and
+        // MMA latencies overlap)
+        const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a0[kBlkPerWarp][4], a1[kBlkPerWarp][4];  // A fragments
 #pragma unroll
         for (int u = 0; u < kBlkPerWarp; ++u) {
           const int j = cw * kBlkPerWarp + u;
+          if (!kQ4K) {
+            // rows gr and gr+8, k 8c .. 8c+7 (chunk c/2 of each row)
+            const int q = c >> 1;
+            const uint8_t* wp = base + j * 512 + 8 * (c & 1);
+            const uint2 xa = *reinterpret_cast<const uint2*>(wp + (q * 16 + (gr ^ (q << 2))) * 16);
+            const uint2 xb =
+                *reinterpret_cast<const uint2*>(wp + (q * 16 + ((gr + 8) ^ (q << 2))) * 16);
+            biased_u8x4_to_f16x4(xa.x ^ 0x80808080u, a0[u][0], a0[u][2]);
+            biased_u8x4_to_f16x4(xb.x ^ 0x80808080u, a0[u][1], a0[u][3]);
+            biased_u8x4_to_f16x4(xa.y ^ 0x80808080u, a1[u][0], a1[u][2]);
+            biased_u8x4_to_f16x4(xb.y ^ 0x80808080u, a1[u][1], a1[u][3]);
+          } else {
+            // word c of rows gr and gr+8: k 8c .. 8c+7; the MMA's k slots
+            // (2c, 2c+1) / (2c+8, 2c+9) take k (8c, 8c+2) / (8c+1, 8c+3) and,
+            // in the second MMA, (8c+4, 8c+6) / (8c+5, 8c+7)
+            const uint8_t* wp = base + j * 256 + 4 * c;
+            nib_word_to_f16(*reinterpret_cast<const uint32_t*>(wp + gr * 16), a0[u][0], a0[u][2],
+                            a1[u][0], a1[u][2]);
+            nib_word_to_f16(*reinterpret_cast<const uint32_t*>(wp + (gr + 8) * 16), a0[u][1],
+                            a0[u][3], a1[u][1], a1[u][3]);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const int mrow = 8 * t + gr;  // token of this lane's B fragment
+#pragma unroll
+          for (int u = 0; u < kBlkPerWarp; ++u) {
+            const int j = cw * kBlkPerWarp + u;
+            uint32_t b00 = 0, b01 = 0, b10 = 0, b11 = 0;
+            if (mrow < M) {
+              const uint2 bv = *reinterpret_cast<const uint2*>(
+                  base + L::act_off() + mrow * kARow + c * 8 + j * 32);
+              if (!kQ4K) {
+                biased_u8x4_to_f16x4(bv.x ^ 0x80808080u, b00, b01);
+                biased_u8x4_to_f16x4(bv.y ^ 0x80808080u, b10, b11);
+              } else {
+                biased_u8x4_to_f16x4_even_odd(bv.x ^ 0x80808080u, b00, b01);
+                biased_u8x4_to_f16x4_even_odd(bv.y ^ 0x80808080u, b10, b11);
+              }
+            }
+            float d[4];
+            mma_f16_16816(d, a0[u], b00, b01, zero4);
+            mma_f16_16816(d, a1[u], b10, b11, d);
+            // d: (n0, tok 8t+2c), (n0, 8t+2c+1), (n1, 8t+2c), (n1, 8t+2c+1): exact sums
+            if (j < nb)
+              *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
+                  make_float4(d[0], d[1], d[2], d[3]);
+            if (kDebug && j < nb) {
+              const int b = blk0 + j;
+              const int n0 = (int)(16 * g + gr), mc0 = 8 * t + 2 * c;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int m = mc0 + (i & 1), n = n0 + ((i < 2) ? 0 : 8);
+                if (m < M && n < a.N) a.dbg[((int64_t)m * a.N + n) * B + b] = __float2int_rn(d[i]);
+              }
+            }
+          }
+        }
+        if (kQ4K) {
+          // lane (r, hh): row r's d*sc and dmin*m of block 2cw + hh
+          const int r = lane & 15, j = cw * kBlkPerWarp + (lane >> 4);
           if (j < nb) {
-            const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 +
-                                                            lane * 16);
-            const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&H.x));
-            scw[j * 16 + lane] = make_float2(dd.x * q4k_field(H, j & 7), dd.y * q4k_field(H, 8 + (j & 7)));
+            const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
+            float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
+            scw[j * 16 + r] = q4k_scales(H, j & 7);
           }
         }
       }
@@ -484,21 +576,249 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   }
 }
 
-template <int TT, bool kQ4K, bool kDebug>
-static cudaError_t launch_decode_cfg(const DecodeArgs& a, bool pdl, cudaStream_t st) {
-  using L = DecodeSmem<TT, kQ4K>;
-  // two-tile kernels (9..16 rows) carry twice the activation rows and stash
-  constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K>();
-  auto kern = decode_gemm_kernel<TT, kQ4K, kDebug>;
+// Decode GEMM for at most four rows on integer dot products. Compute warps:
+// half-warp hh of warp cw takes blocks cw + 8*hh (+ 16, + 32 ... within the
+// stage), one lane per weight row: two 16-byte loads of the row's 32 int8
+// values of the block (W4A8: one load of its 32 nibbles, masked into low
+// and high bytes), two of each token's 32 activation bytes, eight dp4a per
+// token, and the exact int32 sum goes to the stash as fp32 (|sum| < 2^20).
+// For W4A8 the lane also decodes its row's d*sc and dmin*m (exact products;
+// the block's sub-block index is cw for every lane of the warp), and lanes r
+// < M store token r's -asum of the block. No value is widened to fp16 and no
+// lane idles at one token. Chain warp: lane (r, tp) carries weight row r and
+// tokens 2tp, 2tp+1 as one packed pair, applying per block, in ascending
+// order, acc = fmaf(isum, d, acc) (W4A8: fmaf(isum, d*sc, acc) then
+// fmaf(-asum, dmin*m, acc)): the same operations in the same order as the
+// MMA kernel and the prefill kernel.
+template <bool kQ4K, int kM, bool kDebug>
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_dp4a_kernel(const DecodeArgs a) {
+  constexpr int kPairs = (kM + 1) / 2;  // token pairs
+  using L = DecodeSmem<1, kQ4K, true, kPairs>;
+  constexpr int kSBlk = L::kSBlk;
+  constexpr int kARow = L::kARow;
+  constexpr int kPer = kSBlk / (2 * kCompWarps);  // blocks per lane and stage
+  static_assert(kSBlk % (2 * kCompWarps) == 0 && kCompWarps == 8,
+                "a warp's blocks share their sub-block index");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int NW = a.nw;
+  static_assert(kM >= 1 && kM <= kDp4aMaxM, "rows of the integer kernel");
+  constexpr int M = kM;  // == a.M
+  const int SBY = L::stage_bytes(M);
+  float* stash_base = reinterpret_cast<float*>(smem + NW * SBY);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kSlotBytes);
+  uint64_t* empty = full + NW;    // weight stage consumed by the chain warp
+  uint64_t* xfull = empty + NW;   // stash slot written (count: compute warps)
+  uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = a.K / kBlk;
+  const int nstages = (B + kSBlk - 1) / kSBlk;
+  const int r = lane & 15, hh = lane >> 4;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xfull[i], kCompWarps);
+      mbar_init(&xempty[i], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    decode_produce<L, kQ4K>(a, smem, SBY, M, full, empty, lane);
+    return;
+  }
+
+  if (warp <= kCompWarps) {
+    // ------------------------------------------------------ compute warps
+    const int cw = warp - 1;
+    int st = 0, xs = 0;
+    uint32_t ph = 0, xph = 0;
+    bool ok = true;
+    for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x) {
+      const int64_t n = 16 * g + r;
+      for (int s = 0; s < nstages; ++s) {
+        const int blk0 = s * kSBlk;
+        const int nb = min(kSBlk, B - blk0);
+        ok = mbar_wait(&full[st], ph, a.err) && mbar_wait(&xempty[xs], xph ^ 1, a.err);
+        if (!ok) break;
+        const uint8_t* base = smem + st * SBY;
+        float* xsum = stash_base + xs * (L::kSlotBytes / 4);  // [block][pair][row][2 or 4]
+        float* asn = xsum + L::kXBytes / 4;                    // [block][token]
+        const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::bsum_off(M));
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int j = cw + kCompWarps * hh + 2 * kCompWarps * u;
+          const uint8_t* act = base + L::act_off() + j * 32;
+          int isum[kM];
+          if (!kQ4K) {
+            const uint8_t* wp = base + j * 512;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(wp + r * 16);             // k 0..15
+            const uint4 w1 = *reinterpret_cast<const uint4*>(wp + (16 + (r ^ 4)) * 16);  // k 16..31
+#pragma unroll
+            for (int m = 0; m < kM; ++m) {
+              const uint4 x0 = *reinterpret_cast<const uint4*>(act + m * kARow);
+              const uint4 x1 = *reinterpret_cast<const uint4*>(act + m * kARow + 16);
+              int s0 = dp4a_ss(w0.x, x0.x, 0), s1 = dp4a_ss(w1.x, x1.x, 0);
+              s0 = dp4a_ss(w0.y, x0.y, s0);
+              s1 = dp4a_ss(w1.y, x1.y, s1);
+              s0 = dp4a_ss(w0.z, x0.z, s0);
+              s1 = dp4a_ss(w1.z, x1.z, s1);
+              s0 = dp4a_ss(w0.w, x0.w, s0);
+              s1 = dp4a_ss(w1.w, x1.w, s1);
+              isum[m] = s0 + s1;
+            }
+          } else {
+            // word x of the row: low nibbles k = 8x..8x+3, high nibbles
+            // 8x+4..8x+7; the high nibbles stay in place (16 q), and their
+            // sum is shifted back once (exact: a multiple of 16)
+            const uint4 w = *reinterpret_cast<const uint4*>(base + j * 256 + r * 16);
+            const uint32_t l0 = w.x & 0x0F0F0F0Fu, h0 = w.x & 0xF0F0F0F0u;
+            const uint32_t l1 = w.y & 0x0F0F0F0Fu, h1 = w.y & 0xF0F0F0F0u;
+            const uint32_t l2 = w.z & 0x0F0F0F0Fu, h2 = w.z & 0xF0F0F0F0u;
+            const uint32_t l3 = w.w & 0x0F0F0F0Fu, h3 = w.w & 0xF0F0F0F0u;
+#pragma unroll
+            for (int m = 0; m < kM; ++m) {
+              const uint4 x0 = *reinterpret_cast<const uint4*>(act + m * kARow);       // k 0..15
+              const uint4 x1 = *reinterpret_cast<const uint4*>(act + m * kARow + 16);  // k 16..31
+              int sl = dp4a_us(l0, x0.x, 0), sh = dp4a_us(h0, x0.y, 0);
+              sl = dp4a_us(l1, x0.z, sl);
+              sh = dp4a_us(h1, x0.w, sh);
+              sl = dp4a_us(l2, x1.x, sl);
+              sh = dp4a_us(h2, x1.y, sh);
+              sl = dp4a_us(l3, x1.z, sl);
+              sh = dp4a_us(h3, x1.w, sh);
+              isum[m] = sl + (sh >> 4);
+            }
+          }
+          if (j < nb) {
+            float xf[2 * kPairs];
+#pragma unroll
+            for (int m = 0; m < 2 * kPairs; ++m) {
+              xf[m] = m < kM ? small_int_to_f32(isum[m < kM ? m : 0]) : 0.f;
+              if (kDebug && m < kM && n < a.N)
+                a.dbg[((int64_t)m * a.N + n) * B + blk0 + j] = isum[m < kM ? m : 0];
+            }
+            if (!kQ4K) {
+#pragma unroll
+              for (int p = 0; p < kPairs; ++p)
+                *reinterpret_cast<float2*>(xsum + ((j * kPairs + p) * 16 + r) * 2) =
+                    make_float2(xf[2 * p], xf[2 * p + 1]);
+            } else {
+              const uint4 H =
+                  *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
+              const float2 sc = q4k_scales(H, cw);
+#pragma unroll
+              for (int p = 0; p < kPairs; ++p)
+                *reinterpret_cast<float4*>(xsum + ((j * kPairs + p) * 16 + r) * 4) =
+                    make_float4(xf[2 * p], xf[2 * p + 1], sc.x, sc.y);
+              if (r < M) asn[j * kDp4aMaxM + r] = small_int_to_f32(-bb[r * kSBlk + j]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfull[xs]);
+        if (++st == NW) { st = 0; ph ^= 1; }
+        if (++xs == 2) { xs = 0; xph ^= 1; }
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- chain warp
+  const int tp = hh;                          // tokens 2tp, 2tp+1
+  const int tpc = tp < kPairs ? tp : 0;       // (lanes past the last pair repeat pair 0)
+  bool ok = true;
+  int st = 0, xs = 0;
+  uint32_t ph = 0, xph = 0;
+  for (int64_t g = blockIdx.x; g < a.G && ok; g += gridDim.x) {
+    const int64_t n = 16 * g + r;
+    float2 acc = make_float2(0.f, 0.f);
+    for (int s = 0; s < nstages && ok; ++s) {
+      const int blk0 = s * kSBlk;
+      const int nb = min(kSBlk, B - blk0);
+      ok = mbar_wait(&xfull[xs], xph, a.err);
+      if (!ok) break;
+      const uint8_t* base = smem + st * SBY;
+      const float* xsum = stash_base + xs * (L::kSlotBytes / 4);
+      const float* asn = xsum + L::kXBytes / 4;
+      // four blocks at a time: their operands are loaded before their FMAs
+      auto quad = [&](const int j0) {
+        if (!kQ4K) {
+          float2 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            x[u] = *reinterpret_cast<const float2*>(xsum + (((j0 + u) * kPairs + tpc) * 16 + r) * 2);
+          // fp16 scales of rows r&7 and (r&7)+8 for blocks j0..j0+3
+          const uint2 dq = *reinterpret_cast<const uint2*>(base + L::kWBytes + (j0 >> 2) * 128 +
+                                                           (r & 7) * 16 + (r >> 3) * 8);
+          const float2 d01 = __half22float2(*reinterpret_cast<const __half2*>(&dq.x));
+          const float2 d23 = __half22float2(*reinterpret_cast<const __half2*>(&dq.y));
+          const float d[4] = {d01.x, d01.y, d23.x, d23.y};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (j0 + u < nb) acc = __ffma2_rn(x[u], make_float2(d[u], d[u]), acc);
+        } else {
+          float4 v[4];
+          float2 as[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            v[u] = *reinterpret_cast<const float4*>(xsum + (((j0 + u) * kPairs + tpc) * 16 + r) * 4);
+            as[u] = *reinterpret_cast<const float2*>(asn + (j0 + u) * kDp4aMaxM + 2 * tpc);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (j0 + u < nb) {
+              acc = __ffma2_rn(make_float2(v[u].x, v[u].y), make_float2(v[u].z, v[u].z), acc);
+              acc = __ffma2_rn(as[u], make_float2(v[u].w, v[u].w), acc);
+            }
+          }
+        }
+      };
+      if (nb == kSBlk) {
+#pragma unroll
+        for (int j0 = 0; j0 < kSBlk; j0 += 4) quad(j0);
+      } else {
+        for (int j0 = 0; j0 < nb; j0 += 4) quad(j0);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&xempty[xs]);
+        mbar_arrive(&empty[st]);
+      }
+      if (++st == NW) { st = 0; ph ^= 1; }
+      if (++xs == 2) { xs = 0; xph ^= 1; }
+    }
+    if (kDebug || !ok) continue;
+    griddep_wait();  // the activation scales come from the preceding quantize kernel
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int m = 2 * tp + i;
+      if (m < M && n < a.N) {
+        const float y = (i ? acc.y : acc.x) * __ldg(a.sa + m);
+        if (a.out_f32)
+          reinterpret_cast<float*>(a.out)[(int64_t)m * a.ldo + n] = y;
+        else
+          reinterpret_cast<uint16_t*>(a.out)[(int64_t)m * a.ldo + n] = f32_to_bf16_rne(y);
+      }
+    }
+  }
+}
+
+// Launch of either decode kernel with layout L over `mrows` activation rows.
+template <class L, bool kQ4K, class Kern>
+static cudaError_t launch_decode(Kern kern, std::atomic<uint64_t>& attr_set, const DecodeArgs& a,
+                                 int mrows, int budget, bool pdl, cudaStream_t st) {
   // the attribute only caps the launch size; occupancy follows the size passed at launch
-  static std::atomic<uint64_t> attr_set{0};
   {
     const cudaError_t e = smem_attr_once_per_device(kern, 200 * 1024, attr_set);
     if (e != cudaSuccess) return e;
   }
   DecodeArgs b = a;
-  const int mrows = a.M < TT * 8 ? a.M : TT * 8;
-  b.nw = L::num_stages(mrows, kBudget);
+  b.nw = L::num_stages(mrows, budget);
   b.pdl = pdl ? 1 : 0;
   // persistent: at most the CTAs that are resident at once; each walks
   // groups blockIdx.x, + gridDim.x, ...
@@ -524,10 +844,40 @@ static cudaError_t launch_decode_cfg(const DecodeArgs& a, bool pdl, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, b);
 }
 
+template <int TT, bool kQ4K, bool kDebug>
+static cudaError_t launch_decode_mma(const DecodeArgs& a, bool pdl, cudaStream_t st) {
+  using L = DecodeSmem<TT, kQ4K, false>;
+  // two-tile kernels (9..16 rows) carry twice the activation rows and stash
+  constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K>();
+  static std::atomic<uint64_t> attr_set{0};
+  return launch_decode<L, kQ4K>(decode_gemm_kernel<TT, kQ4K, kDebug>, attr_set, a,
+                                a.M < TT * 8 ? a.M : TT * 8, kBudget, pdl, st);
+}
+
+template <bool kQ4K, int kM, bool kDebug>
+static cudaError_t launch_decode_dp4a_m(const DecodeArgs& a, bool pdl, cudaStream_t st) {
+  using L = DecodeSmem<1, kQ4K, true, (kM + 1) / 2>;
+  static std::atomic<uint64_t> attr_set{0};
+  return launch_decode<L, kQ4K>(decode_dp4a_kernel<kQ4K, kM, kDebug>, attr_set, a, kM,
+                                dec_smem_budget<kQ4K>(), pdl, st);
+}
+
+template <bool kQ4K, bool kDebug>
+static cudaError_t launch_decode_dp4a(const DecodeArgs& a, bool pdl, cudaStream_t st) {
+  static_assert(kDp4aMaxM == 4, "one instantiation per row count");
+  switch (a.M) {
+    case 1: return launch_decode_dp4a_m<kQ4K, 1, kDebug>(a, pdl, st);
+    case 2: return launch_decode_dp4a_m<kQ4K, 2, kDebug>(a, pdl, st);
+    case 3: return launch_decode_dp4a_m<kQ4K, 3, kDebug>(a, pdl, st);
+    default: return launch_decode_dp4a_m<kQ4K, 4, kDebug>(a, pdl, st);
+  }
+}
+
 template <bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_m(const DecodeArgs& a, bool pdl, cudaStream_t st) {
-  if (a.M <= 8) return launch_decode_cfg<1, kQ4K, kDebug>(a, pdl, st);
-  return launch_decode_cfg<2, kQ4K, kDebug>(a, pdl, st);
+  if (a.M <= dec_dp4a_max_m<kQ4K>()) return launch_decode_dp4a<kQ4K, kDebug>(a, pdl, st);
+  if (a.M <= 8) return launch_decode_mma<1, kQ4K, kDebug>(a, pdl, st);
+  return launch_decode_mma<2, kQ4K, kDebug>(a, pdl, st);
 }
 
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,

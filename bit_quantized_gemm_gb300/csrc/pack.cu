@@ -20,31 +20,25 @@ __device__ __forceinline__ uint16_t q8_dbits(const uint8_t* blocks, int64_t B, i
   return (uint16_t)(p[0] | (p[1] << 8));
 }
 
-// one thread per (group g, block b, lane t): the 16 A-fragment bytes of the
-// decode kernel's two fp16 MMAs for this block, stored biased (q + 128 as an
-// unsigned byte) so that two byte permutes and one packed subtract turn four
-// of them into exact fp16 values
+// one thread per (group g, block b, chunk t): 16 of the block's int8 values
+// as signed bytes. Chunk t = 16*h + (r ^ 4h) holds q[16g+r][32b+16h ..
+// +15]: the decode kernel's integer dot products read a row's 32 values as
+// chunks (0, r) and (1, r); its 16-row fp16 MMA tiles read 8 bytes of rows
+// r and r+8, and the XOR keeps those half-warp reads free of bank conflicts.
 __global__ void pack_q8_0_stream(const uint8_t* __restrict__ blocks, int64_t N, int64_t B,
                                  int64_t G, uint8_t* __restrict__ out) {
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= G * B * 32) return;
   const int t = (int)(i % 32);
   const int64_t b = (i / 32) % B, g = i / 32 / B;
-  const int r = t / 4, c = t % 4;
-  const int64_t n0 = 16 * g + r, n1 = n0 + 8, k0 = 32 * b + 8 * c;
-  uint8_t v[16];
-  for (int j = 0; j < 4; ++j) {
-    v[j] = (uint8_t)(q8_val(blocks, B, N, n0, k0 + j) + 128);
-    v[4 + j] = (uint8_t)(q8_val(blocks, B, N, n1, k0 + j) + 128);
-    v[8 + j] = (uint8_t)(q8_val(blocks, B, N, n0, k0 + 4 + j) + 128);
-    v[12 + j] = (uint8_t)(q8_val(blocks, B, N, n1, k0 + 4 + j) + 128);
+  const int h = t >> 4, r = (t & 15) ^ (h << 2);
+  const int64_t n = 16 * g + r, k0 = 32 * b + 16 * h;
+  uint32_t w[4];
+  for (int x = 0; x < 4; ++x) {
+    w[x] = 0;
+    for (int e = 0; e < 4; ++e) w[x] |= (uint32_t)(uint8_t)q8_val(blocks, B, N, n, k0 + 4 * x + e) << (8 * e);
   }
-  uint4 w;
-  w.x = v[0] | (v[1] << 8) | (v[2] << 16) | ((uint32_t)v[3] << 24);
-  w.y = v[4] | (v[5] << 8) | (v[6] << 16) | ((uint32_t)v[7] << 24);
-  w.z = v[8] | (v[9] << 8) | (v[10] << 16) | ((uint32_t)v[11] << 24);
-  w.w = v[12] | (v[13] << 8) | (v[14] << 16) | ((uint32_t)v[15] << 24);
-  reinterpret_cast<uint4*>(out)[i] = w;
+  reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // one thread per (group g, block quad p, row r in 0..7)
@@ -93,36 +87,35 @@ __device__ __forceinline__ int q4_field(const uint8_t* p, int f) {
   return (int)((v >> sh) & 63u);
 }
 
-// one thread per (group g, block b, lane t): two words of nibbles, one per
-// 16-wide half h of the block's 32 k (k = 32b + 8c + 4h + j, j = 0..3): rows
-// r and r+8 interleaved so that shift-and-mask yields fp16 pairs directly:
-//   bits 0-3 q[r][j0], 16-19 q[r][j1], 4-7 q[r+8][j0], 20-23 q[r+8][j1],
-//   8-11 q[r][j2], 24-27 q[r][j3], 12-15 q[r+8][j2], 28-31 q[r+8][j3]
+// one thread per (group g, block b, row r): the row's 32 values of the block
+// in 16 bytes, [g][b][r][16 B]. Word x (0..3) holds k = 32b + 8x .. 8x+7:
+// byte e's low nibble is q[k = 32b + 8x + e], its high nibble q[32b + 8x + 4
+// + e], so masking a word with 0x0F0F0F0F / 0xF0F0F0F0 gives four bytes that
+// pair with four consecutive activation bytes in an integer dot product.
 __global__ void pack_q4k_stream(const uint8_t* __restrict__ sb, int64_t N, int64_t J,
                                 int64_t B, int64_t G, uint8_t* __restrict__ out) {
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i >= G * B * 32) return;
-  const int t = (int)(i % 32);
-  const int64_t b = (i / 32) % B, g = i / 32 / B;
-  const int r = t / 4, c = t % 4;
-  const int64_t n0 = 16 * g + r, n1 = n0 + 8;
-  uint32_t w[2];
-  for (int h = 0; h < 2; ++h) {
-    const int64_t k = 32 * b + 8 * c + 4 * h;
-    uint32_t a[4], e[4];
-    for (int j = 0; j < 4; ++j) {
-      a[j] = (uint32_t)q4_nib(sb, J, N, n0, k + j);
-      e[j] = (uint32_t)q4_nib(sb, J, N, n1, k + j);
+  if (i >= G * B * 16) return;
+  const int r = (int)(i % 16);
+  const int64_t b = (i / 16) % B, g = i / 16 / B;
+  const int64_t n = 16 * g + r;
+  uint32_t w[4];
+  for (int x = 0; x < 4; ++x) {
+    w[x] = 0;
+    for (int e = 0; e < 4; ++e) {
+      const int64_t k = 32 * b + 8 * x + e;
+      const uint32_t lo = (uint32_t)q4_nib(sb, J, N, n, k), hi = (uint32_t)q4_nib(sb, J, N, n, k + 4);
+      w[x] |= (lo | (hi << 4)) << (8 * e);
     }
-    w[h] = a[0] | (a[1] << 16) | (e[0] << 4) | (e[1] << 20) | (a[2] << 8) | (a[3] << 24) |
-           (e[2] << 12) | (e[3] << 28);
   }
-  // [g][b/2][lane][16 B]: block 2p in bytes 0-7, block 2p+1 in bytes 8-15
-  const int64_t off = (((g * (B / 2) + b / 2) * 32 + t) * 16) + (b & 1) * 8;
-  *reinterpret_cast<uint2*>(out + off) = make_uint2(w[0], w[1]);
+  reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// one thread per (group g, super-block j, row r in 0..15): the 16-byte header
+// one thread per (group g, super-block j, row r in 0..15): a 16-byte header,
+// [G][J][16 rows][16 B]: d and dmin (bytes 0-3, as in the super-block), then
+// a 96-bit little-endian string of eight 12-bit units, unit i at bits [12i,
+// 12i+12) = sc_i | m_i << 6, so that one funnel shift brings a sub-block's
+// two fields together.
 __global__ void pack_q4k_shdr(const uint8_t* __restrict__ sb, int64_t N, int64_t J, int64_t G,
                               uint8_t* __restrict__ out) {
   int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -130,7 +123,28 @@ __global__ void pack_q4k_shdr(const uint8_t* __restrict__ sb, int64_t N, int64_t
   const int r = (int)(i % 16);
   const int64_t j = (i / 16) % J, g = i / 16 / J;
   const int64_t n = 16 * g + r;
-  for (int x = 0; x < 16; ++x) out[i * 16 + x] = (n < N) ? sb[(n * J + j) * kQ4kBytes + x] : 0;
+  uint8_t h[16] = {};
+  if (n < N) {
+    const uint8_t* p = sb + (n * J + j) * kQ4kBytes;
+    for (int x = 0; x < 4; ++x) h[x] = p[x];
+    uint64_t lo = 0;  // units 0..4 (bits 0..59) and the low 4 bits of unit 5
+    uint32_t hi = 0;  // bits 64..95
+    for (int u = 0; u < 8; ++u) {
+      const uint64_t unit = (uint64_t)(q4_field(p + 4, u) | (q4_field(p + 4, 8 + u) << 6));
+      const int pos = 12 * u;
+      if (pos + 12 <= 64) {
+        lo |= unit << pos;
+      } else if (pos >= 64) {
+        hi |= (uint32_t)(unit << (pos - 64));
+      } else {
+        lo |= unit << pos;
+        hi |= (uint32_t)(unit >> (64 - pos));
+      }
+    }
+    for (int x = 0; x < 8; ++x) h[4 + x] = (uint8_t)(lo >> (8 * x));
+    for (int x = 0; x < 4; ++x) h[12 + x] = (uint8_t)(hi >> (8 * x));
+  }
+  for (int x = 0; x < 16; ++x) out[i * 16 + x] = h[x];
 }
 
 // one thread per (n, b): fp16 copy of the sub-block's 4-bit values, d*sc, dmin*m
@@ -173,7 +187,7 @@ cudaError_t launch_pack_q4k(const void* sblocks, int64_t N, int64_t K, void* pac
   const Q4kLayout L(N, K);
   auto* base = reinterpret_cast<uint8_t*>(packed);
   const auto* in = reinterpret_cast<const uint8_t*>(sblocks);
-  pack_q4k_stream<<<grid_for(L.G * L.B * 32, 256), 256, 0, st>>>(in, N, L.J, L.B, L.G,
+  pack_q4k_stream<<<grid_for(L.G * L.B * 16, 256), 256, 0, st>>>(in, N, L.J, L.B, L.G,
                                                                    base + L.off_stream);
   pack_q4k_shdr<<<grid_for(L.G * L.J * 16, 256), 256, 0, st>>>(in, N, L.J, L.G,
                                                                 base + L.off_shdr);

@@ -36,14 +36,11 @@ __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a
 // Packed weight layout (opaque to callers; sized by qg_*_packed_bytes).
 //
 // Q8_0, for N rows, K columns, B = K/32 blocks, G = ceil(N/16) row groups:
-//  stream  G*B*512 B   weights in the decode kernel's fragment order, as
-//                       biased bytes q+128: for group g, block b, lane t
-//                       (r = t/4, c = t%4) the 16 bytes are q[16g+r][32b+8c
-//                       .. +3], q[16g+r+8][32b+8c .. +3], q[16g+r][32b+8c+4
-//                       .. +7], q[16g+r+8][32b+8c+4 .. +7] -- the A operands
-//                       of the block's two m16n8k16 fp16 MMAs (K permuted the
-//                       same way on both operands; integer sums do not
-//                       depend on the order).
+//  stream  G*B*512 B   weights of group g, block b as 32 chunks of 16
+//                       signed bytes: chunk 16h + (r ^ 4h) holds q[16g+r]
+//                       [32b+16h .. +15] (a dot-product lane reads its row as
+//                       chunks (0, r), (1, r); an MMA lane reads 8 bytes of
+//                       rows r and r+8, free of bank conflicts).
 //  dsc     G*(B4/4)*128 B  fp16 scales for the decode kernel: for group g,
 //                       block quad p, row r (0..7): 16 bytes =
 //                       d[16g+r][4p .. 4p+3], d[16g+r+8][4p .. 4p+3].
@@ -51,12 +48,12 @@ __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a
 //                       (operand A of the prefill tensor-core kernel).
 //  d32     N*B4*4 B    scales as fp32, [N][B4] (B4 = B rounded up to 4).
 // Q4_K, with J = K/256 super-blocks per row:
-//  stream  G*B*256 B   nibbles in fragment order: for group g, block pair p,
-//                       lane t: 8 bytes for block 2p then 8 for block 2p+1;
-//                       for one block two words, one per 16-wide half
-//                       (bit layout in pack.cu: fp16 pairs by shift-and-mask).
-//  shdr    G*J*256 B   the first 16 bytes (d, dmin, 6-bit fields) of each
-//                       super-block, [G][J][16 rows][16 B].
+//  stream  G*B*256 B   nibbles of group g, block b, row r in 16 bytes,
+//                       [G][B][16][16 B]: word x holds k = 8x..8x+3 in the
+//                       low nibbles of its bytes, 8x+4..8x+7 in the high ones.
+//  shdr    G*J*256 B   per row and super-block, [G][J][16 rows][16 B]: d,
+//                       dmin (fp16), then eight 12-bit units sc_i | m_i << 6
+//                       at bits [12i, 12i+12) of a 96-bit little-endian string.
 //  q16     N*K*2 B     q (0..15) as fp16, row-major [N][K].
 //  ds32    N*B*4 B     d*sc_b as fp32 (exact), [N][B].
 //  dm32    N*B*4 B     dmin*m_b as fp32 (exact), [N][B].
@@ -378,15 +375,6 @@ __device__ __forceinline__ void biased_u8x4_to_f16x4(uint32_t u, uint32_t& lo, u
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
-
-// Two 4-bit values at bits [s, s+4) and [s+16, s+20) -> an fp16 pair.
-template <int kShift>
-__device__ __forceinline__ uint32_t nib_pair_to_f16x2(uint32_t w) {
-  uint32_t a = ((w >> kShift) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x64006400u));
-  return r;
 }
 
 // Read-only 4-byte global load as volatile asm: it stays where it is written

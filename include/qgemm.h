@@ -132,7 +132,7 @@ qg_status qg_quantize_act_static(const void* x, qg_dtype x_dtype, int64_t M, int
 /* row-major over (n, b): {fp16 d (little endian); int8 q[32]}, weight =     */
 /* d*q. qg_pack_q8_0 rearranges them once into the library's opaque packed   */
 /* buffer (qg_q8_0_packed_bytes(N, K) bytes, 256-byte aligned, caller-owned), */
-/* which holds the int8 values in the decode kernel's fragment order, the     */
+/* which holds the int8 values in the decode kernels' order, the            */
 /* scales, and an fp16 copy of the values for the prefill kernel. The values  */
 /* are never changed: d and q reach the arithmetic bit for bit.              */
 /*   blocks  device, [N][K/32][34] bytes (no alignment needed).              */
