@@ -102,14 +102,6 @@ static_assert(QG_DEC_DP4A_MAX_Q8 <= kDp4aMaxM && QG_DEC_DP4A_MAX_Q4K <= kDp4aMax
 #define QG_DEC_CHAIN_UNROLL 1  // chain warp: a full stage's block quads unrolled
 #endif
 
-__device__ __forceinline__ void bulk_copy(void* smem_dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Shared-memory layout (offsets depend on M, fixed at launch):
 //   NW weight stages, each: weights | scales | M activation rows | (W4A8) M
@@ -250,10 +242,10 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
     const int nb = min(kSBlk, B - blk0);
     uint8_t* base = smem + slot * SBY;
     for (int m = lane; m < mrows; m += 32) {
-      bulk_copy(base + L::act_off() + m * kARow,
+      bulk_copy_g2s(base + L::act_off() + m * kARow,
                 a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[slot]);
       if (kQ4K)
-        bulk_copy(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
+        bulk_copy_g2s(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
                   nb * 4, &full[slot]);
     }
   };
@@ -286,12 +278,12 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
         if (ok) {
           mbar_arrive_expect_tx(&full[st], bytes);
           if (!kQ4K) {
-            bulk_copy(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
-            bulk_copy(base + L::kWBytes, a.wscale + (g * (B4 / 4) + blk0 / 4) * 128,
+            bulk_copy_g2s(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);
+            bulk_copy_g2s(base + L::kWBytes, a.wscale + (g * (B4 / 4) + blk0 / 4) * 128,
                       ((nb + 3) / 4) * 128, &full[st]);
           } else {
-            bulk_copy(base, a.wstream + (g * B + blk0) * 256, nb * 256, &full[st]);
-            bulk_copy(base + L::kWBytes, a.wscale + (g * J + blk0 / 8) * 256, (nb / 8) * 256,
+            bulk_copy_g2s(base, a.wstream + (g * B + blk0) * 256, nb * 256, &full[st]);
+            bulk_copy_g2s(base + L::kWBytes, a.wscale + (g * J + blk0 / 8) * 256, (nb / 8) * 256,
                       &full[st]);
           }
         }
