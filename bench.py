@@ -418,8 +418,9 @@ def quantize_rows(dev, flush, hbm, reps):
 
 
 def layer_rows(dev, hbm):
-    """The whole layer (x in, y out) at decode sizes through qg_linear_* (the
-    decode GEMM launched as a programmatic dependent of the quantize kernel)
+    """The whole layer (x in, y out) at decode sizes (1 and 8 rows: the decode
+    GEMM) and 64 rows (the prefill kernels) through qg_linear_* (the GEMM
+    launched as a programmatic dependent of the quantize kernel)
     against qg_quantize_act and the GEMM called separately, per call, cycling
     through four weight copies like the decode rows. Each is timed as issued
     (one host call per layer against two) and replayed from a CUDA graph
@@ -434,7 +435,7 @@ def layer_rows(dev, hbm):
         packs = [pack(wts, N, K) for _ in range(ROTATE_COPIES)]
         del wts
         lin = qg.linear_w4a8_q4k if q4k else qg.linear_w8a8_q8_0
-        for M in (1, 8):
+        for M in (1, 8, 64):
             x, bits = synth.config_activations(name, M, K)
             xd = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -443,13 +444,15 @@ def layer_rows(dev, hbm):
             q = torch.empty((M, K), dtype=torch.int8, device=dev)
             s = torch.empty((M,), dtype=torch.float32, device=dev)
             bs = torch.empty((M, K // 32), dtype=torch.int32, device=dev) if q4k else None
+            wide = M > qg.small_m_max()  # the prefill kernels read the fp16 copy
+            h = torch.empty((M, K), dtype=torch.float16, device=dev) if wide else None
 
             def two(p):
-                qg.quantize_act(xd, block_sums=q4k, out=(q, s, bs, None))
+                qg.quantize_act(xd, block_sums=q4k, q16=wide, out=(q, s, bs, h))
                 if q4k:
-                    qg.gemm_w4a8_q4k(q, None, s, bs, p, N, out=out)
+                    qg.gemm_w4a8_q4k(q, h, s, bs, p, N, out=out)
                 else:
-                    qg.gemm_w8a8_q8_0(q, None, s, p, N, out=out)
+                    qg.gemm_w8a8_q8_0(q, h, s, p, N, out=out)
 
             layer = [lambda p=p: lin(xd, p, N, out=out, workspace=ws) for p in packs]
             separate = [lambda p=p: two(p) for p in packs]
@@ -465,7 +468,8 @@ def layer_rows(dev, hbm):
             wbytes = N * K // 256 * 144 if q4k else N * K + N * (K // 32) * 2
             algo = wbytes + 2 * M * K + 2 * M * N  # weights, bf16 x, bf16 out
             gbs = algo / r["ms"] / 1e6
-            r.update({"launches": 2, "gbs": round(gbs, 1), "bound": "hbm",
+            r.update({"launches": 1 + qg.gemm_launch_count(kind, M, K, N), "gbs": round(gbs, 1),
+                      "bound": "hbm",
                       "frac": round(gbs / hbm, 4)})
             rows["layer_%s_M%d_K%d_N%d" % (name, M, K, N)] = r
         del packs

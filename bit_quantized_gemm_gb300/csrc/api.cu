@@ -32,7 +32,8 @@ cudaError_t launch_decode_q4k(const int8_t* qa, const float* sa, const int32_t* 
                               cudaStream_t st);
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
-                                int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st);
+                                int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                                cudaStream_t st);
 int prefill_launches_q8_0(int64_t M, int64_t N);
 void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* narrow_kind,
                        int* narrow_tokens);
@@ -40,7 +41,7 @@ void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* n
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
                                bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err,
-                               cudaStream_t st);
+                               bool pdl, cudaStream_t st);
 }  // namespace qg
 
 using namespace qg;
@@ -198,15 +199,15 @@ qg_status linear(bool q4k, const void* x, qg_dtype xdt, int64_t M, int64_t K, in
   s = from_cuda(launch_quantize_act(x, xdt == QG_BF16, M, K, ldx, q, scale, bsum, q16, st),
                 "quantize launch");
   if (s != QG_OK) return s;
+  // The GEMM's first launch (decode or prefill kernel) is a programmatic dependent of the
+  // quantize kernel: its CTAs start, and request their first weight stages,
+  // while the activations are quantized
   if (large)
     return from_cuda(q4k ? launch_prefill_q4k(q16, scale, bsum, M, K, w, N, out, f32, ldo, nullptr,
-                                              error_word(), st)
+                                              error_word(), true, st)
                          : launch_prefill_q8_0(q16, scale, M, K, w, N, out, f32, ldo, nullptr,
-                                               error_word(), st),
+                                               error_word(), true, st),
                      "prefill GEMM launch");
-  // M <= kSmallMMax (one decode launch): the GEMM is a programmatic
-  // dependent of the quantize kernel, so its CTAs stream their first weight
-  // stages while the activations are quantized
   return from_cuda(q4k ? launch_decode_q4k(q, scale, bsum, M, K, w, N, out, f32, ldo, nullptr,
                                            error_word(), true, st)
                        : launch_decode_q8_0(q, scale, M, K, w, N, out, f32, ldo, nullptr,
@@ -369,7 +370,7 @@ static qg_status gemm_q8_0(const int8_t* q, const uint16_t* q16, const float* sc
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool f32 = odt == QG_F32;
   if (large)
-    return from_cuda(launch_prefill_q8_0(q16, scale, M, K, w, N, out, f32, ldo, dbg, error_word(), st),
+    return from_cuda(launch_prefill_q8_0(q16, scale, M, K, w, N, out, f32, ldo, dbg, error_word(), false, st),
                      "prefill GEMM launch");
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,
                        [&](int64_t m0, int64_t mc, void* o, int32_t* d) {
@@ -392,7 +393,7 @@ static qg_status gemm_q4k(const int8_t* q, const uint16_t* q16, const float* sca
   const bool f32 = odt == QG_F32;
   if (large)
     return from_cuda(
-        launch_prefill_q4k(q16, scale, bsum, M, K, w, N, out, f32, ldo, dbg, error_word(), st),
+        launch_prefill_q4k(q16, scale, bsum, M, K, w, N, out, f32, ldo, dbg, error_word(), false, st),
         "prefill GEMM launch");
   const int64_t B = K / kBlk;
   return decode_chunks(M, K, N, ldo, f32 ? 4 : 2, out, dbg,

@@ -166,6 +166,7 @@ struct LargeArgs {
   int out_f32;
   int tma_out;           // 1: bf16 outputs leave through the TMA store (tmO)
   int tile_group;        // token tiles per group of the persistent tile order
+  int pdl;               // launched as a programmatic dependent of the quantize kernel
   int32_t* dbg;          // [M][N][B] isum export (debug) or null
   uint32_t* err;
 };
@@ -260,7 +261,14 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
         }
       }
     };
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    // As a programmatic dependent of the quantize kernel (W8A8): the weight
+    // tiles of the first P stages are requested before the wait for its
+    // grid, their activation tiles after it. W4A8 reads activation block
+    // sums in this warp as well: it waits before anything.
+    const int P = (args.pdl && !kQ4K) ? min(min(NS, kStages), 3) : 0;
+    if (args.pdl && kQ4K) griddep_wait();
+    bool first = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, first = false) {
       int mt, nt;
       tile_coords(tile, MT, NT, args.tile_group, mt, nt);
       for (int s = 0; s < NS && ok; ++s) {
@@ -271,7 +279,14 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
             load_par = (load_par & ~(1u << stage)) | (phase << stage);
             mbar_arrive_expect_tx(&S.full[stage], kStageABytes + kStageBBytes);
             tma_load_2d(S.a[stage], &tmA, &S.full[stage], s * kBK, nt * kBN);
-            tma_load_2d(S.b[stage], &tmB, &S.full[stage], s * kBK, mt * kBM);
+            if (!(first && s < P))
+              tma_load_2d(S.b[stage], &tmB, &S.full[stage], s * kBK, mt * kBM);
+            if (first && s + 1 == P) {
+              // the first tile's first P stages are ring slots 0..P-1
+              griddep_wait();
+              for (int r = 0; r < P; ++r)
+                tma_load_2d(S.b[r], &tmB, &S.full[r], r * kBK, mt * kBM);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -390,6 +405,9 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
     const int half = (warp - kFirstEpiWarp) >> 2;
     uint32_t tph = 0;  // bit b: phase of the next wait on tfull[b]
     const bool ostore = args.tma_out && quarter == 0 && lane == 0;  // issues this half's stores
+    // the activation scales come from the quantize kernel, and the output may
+    // be what the kernel before it read
+    if (args.pdl) griddep_wait();
     int aslot = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -719,8 +737,8 @@ static cudaError_t launch_prefill_t(const CUtensorMap& ta, const void* q16, cons
   const int tiles = (int)(ceil_div(a.M, BM) * ceil_div(a.N, kBN));
   const int slots = num_sms() * kCtasPerSm;
   const int grid = tiles < slots ? tiles : slots;
-  kern<<<grid, LargeCfg<BM>::kThreads, kSmem, st>>>(ta, tb, to, args);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(LargeCfg<BM>::kThreads), kSmem, st, a.pdl != 0, ta,
+                       tb, to, args);
 }
 
 // Cycles of one 32-block step of one tile (measured on GB300 with forced
@@ -801,7 +819,7 @@ static PrefillPlan plan_as_built(int64_t M, int64_t N, int sms) {
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
                                void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
-                               cudaStream_t st);
+                               bool pdl, cudaStream_t st);
 
 // The plan for M x N on `sms` SMs, as launch_prefill_q8_0 carries it out
 // (host only): the weight rows of the 256-token launch, then the remaining
@@ -828,10 +846,13 @@ int prefill_launches_q8_0(int64_t M, int64_t N) {
   return (p.nt_wide > 0 && (int64_t)p.nt_wide * kBN < N) ? 2 : 1;
 }
 
-// returns cudaErrorNotSupported when the tensor-map encoder is unavailable
+// returns cudaErrorNotSupported when the tensor-map encoder is unavailable;
+// pdl: the first launch is a programmatic dependent of the quantize kernel
+// before it on the stream (a second launch follows the first in stream order)
 cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                 const void* packed, int64_t N, void* out, bool out_f32,
-                                int64_t ldo, int32_t* dbg, uint32_t* err, cudaStream_t st) {
+                                int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
+                                cudaStream_t st) {
   const Q8Layout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
   LargeArgs a{};
@@ -855,6 +876,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   if (n0 > 0) {
     LargeArgs aw = a;
     aw.N = (int)(n0 < N ? n0 : N);
+    aw.pdl = pdl ? 1 : 0;
     if (!make_tmap(&ta, wq16, aw.N, K, kBN)) return cudaErrorNotSupported;
     const cudaError_t e = launch_prefill_t<false, false, 256>(ta, q16, aw, st);
     if (e != cudaSuccess || n0 >= N) return e;
@@ -862,13 +884,14 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   // weight rows [n0, N) over all tokens, as narrow tiles
   LargeArgs an = a;
   an.N = (int)(N - n0);
+  an.pdl = (pdl && n0 == 0) ? 1 : 0;
   an.d32 = a.d32 + n0 * a.ldd;
   an.out = out_f32 ? (void*)(reinterpret_cast<float*>(out) + n0)
                    : (void*)(reinterpret_cast<uint16_t*>(out) + n0);
   if (p.bm_tail == 0)  // 16-row tiles (legacy fp16 MMA)
     return launch_skinny_q8_0(q16, sa, M, K, reinterpret_cast<const uint16_t*>(wq16 + n0 * K * 2),
                               an.d32, an.ldd, an.N, an.out, out_f32, ldo,
-                              skinny_tb(M, an.N, num_sms()), err, st);
+                              skinny_tb(M, an.N, num_sms()), err, an.pdl != 0, st);
   if (!make_tmap(&ta, wq16 + n0 * K * 2, an.N, K, kBN)) return cudaErrorNotSupported;
   switch (p.bm_tail) {
     case 128: return launch_prefill_t<false, false, 128>(ta, q16, an, st);
@@ -880,7 +903,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
 
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
-                               bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err,
+                               bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
                                cudaStream_t st) {
   const Q4kLayout L(N, K);
   const auto* base = reinterpret_cast<const uint8_t*>(packed);
@@ -898,6 +921,7 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.out_f32 = out_f32 ? 1 : 0;
   a.dbg = dbg;
   a.err = err;
+  a.pdl = (pdl && !dbg) ? 1 : 0;
   constexpr int BM = QG_BM_W4A8;
   if (dbg) return launch_prefill_t<true, true, BM>(ta, q16, a, st);
   // a GEMM of at most 64 tokens fills half of a 128-token tile: 64-token tiles

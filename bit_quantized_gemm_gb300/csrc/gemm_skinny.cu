@@ -62,6 +62,7 @@ struct SkinnyArgs {
   int64_t ldo, ldd;
   int M, N, K;
   int out_f32;
+  int pdl;  // launched as a programmatic dependent of the quantize kernel
   uint32_t* err;
 };
 
@@ -113,13 +114,22 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, 2)
       int st = 0;
       uint32_t ph = 0;
       bool ok = true;
+      // as a programmatic dependent of the quantize kernel: the weight tiles
+      // of the first P stages before the wait for its grid, their activation
+      // tiles after it
+      const int P = args.pdl ? min(min(NS, kS), 3) : 0;
       for (int s = 0; s < NS && ok; ++s) {
         ok = mbar_wait(&empty[st], ph ^ 1, args.err);
         if (!ok) break;
         uint8_t* a_s = sm + st * C::kStageBytes;
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);  // whole boxes (zero-filled edges)
         tma_load_2d(a_s, &tmA, &full[st], s * kSkBK, n0);
-        tma_load_2d(a_s + C::kABytes, &tmB, &full[st], s * kSkBK, m0);
+        if (s >= P) tma_load_2d(a_s + C::kABytes, &tmB, &full[st], s * kSkBK, m0);
+        if (s + 1 == P) {
+          griddep_wait();
+          for (int r = 0; r < P; ++r)
+            tma_load_2d(sm + r * C::kStageBytes + C::kABytes, &tmB, &full[r], r * kSkBK, m0);
+        }
         if (++st == kS) { st = 0; ph ^= 1; }
       }
       // every stage handed back before the CTA exits (no copy in flight)
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, 2)
     }
   }
   if (!ok) return;
+  if (args.pdl) griddep_wait();  // the activation scales come from the quantize kernel
 #pragma unroll
   for (int tt = 0; tt < 2; ++tt) {
 #pragma unroll
@@ -275,8 +286,7 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)ceil_div(a.N, kSkRows), (unsigned)ceil_div(a.M, TB));
-  kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tb, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(C::kThreads), C::kSmem, st, a.pdl != 0, ta, tb, a);
 }
 
 // Weight rows [0, N) of the packed-layout views passed in (the caller offsets
@@ -285,8 +295,9 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
                                void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
-                               cudaStream_t st) {
+                               bool pdl, cudaStream_t st) {
   SkinnyArgs a{};
+  a.pdl = pdl ? 1 : 0;
   a.d32 = d32;
   a.ldd = ldd;
   a.sa = sa;

@@ -815,25 +815,10 @@ static cudaError_t launch_decode(Kern kern, std::atomic<uint64_t>& attr_set, con
   // persistent: at most the CTAs that are resident at once; each walks
   // groups blockIdx.x, + gridDim.x, ...
   const int64_t slots = (int64_t)num_sms() * dec_ctas<kQ4K>();
-  dim3 grid((unsigned)(a.G < slots ? a.G : slots)), block(32 * (kCompWarps + 2));
-  if (!pdl) {
-    kern<<<grid, block, L::total(mrows, b.nw), st>>>(b);
-    return cudaGetLastError();
-  }
-  // programmatic dependent launch: the CTAs may start while the previous
-  // kernel on the stream (the quantize kernel) runs, streaming their first
-  // weight stages meanwhile
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = (size_t)L::total(mrows, b.nw);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, b);
+  // with pdl, the CTAs may start while the previous kernel on the stream
+  // (the quantize kernel) runs, streaming their first weight stages meanwhile
+  const dim3 grid((unsigned)(a.G < slots ? a.G : slots)), block(32 * (kCompWarps + 2));
+  return launch_kernel(kern, grid, block, (size_t)L::total(mrows, b.nw), st, pdl, b);
 }
 
 template <int TT, bool kQ4K, bool kDebug>

@@ -119,6 +119,30 @@ inline cudaError_t smem_attr_once_per_device(Kern kern, int bytes, std::atomic<u
   return e;
 }
 
+// Launch `kern` on `st`; with `pdl`, as a programmatic dependent of the
+// kernel before it on the stream: its CTAs may start while that kernel runs,
+// and every read of that kernel's outputs (and every write of its inputs)
+// in `kern` must follow griddep_wait().
+template <class Kern, class... Args>
+inline cudaError_t launch_kernel(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 bool pdl, const Args&... args) {
+  if (!pdl) {
+    kern<<<grid, block, smem, st>>>(args...);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Kernels that wait on barriers receive the address of the library's device
 // error word (one per device) and OR a code into it when a wait gives up.
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t code) {
