@@ -14,15 +14,17 @@
 //     sums) -- into a shared-memory ring with 1-D bulk copies
 //     (cp.async.bulk + mbarrier transaction counts);
 //   * warps 1..8 compute the stage's exact block sums into a shared stash:
-//     - up to 4 rows, decode_dp4a_kernel: one lane per
+//     - up to 3 (W8A8) or 4 (W4A8) rows, decode_dp4a_kernel: one lane per
 //       weight row and block, eight dp4a per token on the row's 32 int8
 //       values (W4A8: its 32 nibbles masked into low and high bytes), no
 //       widening; the W4A8 lane also decodes its row's d*sc and dmin*m;
-//     - more rows, decode_gemm_kernel: two m16n8k16 fp16 MMAs per block and
-//       8-token tile (int8 widened to exact fp16 by byte permutes and one
-//       packed subtract; nibbles by mask-or and one packed subtract or
-//       multiply-add); legacy fp16 MMAs run at 4x the legacy int8 MMA rate,
-//       which is that of dp4a; every sum is below 2^20, exact in fp32;
+//     - more rows, decode_gemm_kernel: one legacy int8 m16n8k32 MMA per
+//       block and 8-token tile on the stored bytes (nibbles masked into
+//       unsigned bytes). That MMA runs at a quarter of the legacy fp16 rate,
+//       but 16 rows need only ~18 us of it for a 5120 x 17408 matrix, and
+//       nothing is widened (the fp16-MMA variant, which widens weights and
+//       activations in registers, is kept behind a build switch); every sum
+//       is below 2^20, exact in int32 and in fp32;
 //   * warp 9 applies acc = fmaf(isum, d, acc) (Q4_K: then
 //     fmaf(-asum, dmin*m, acc)) over the stage's blocks in ascending order
 //     with packed f32x2 FMAs -- the same chain as the prefill kernel, so both
@@ -37,6 +39,12 @@
 namespace qg {
 
 constexpr int kCompWarps = 8;      // compute warps per CTA
+
+// 5..16 rows: block sums by the legacy int8 MMA on the stored bytes (1) or by
+// fp16 MMAs on weights and activations widened in registers (0)
+#ifndef QG_DEC_IMMA
+#define QG_DEC_IMMA 1
+#endif
 
 // K blocks per pipeline stage. MMA tiles: 16 for both formats (8 KB of Q8_0
 // weights, 4 KB of Q4_K nibbles per 16-row group); Q4_K once took 32, but
@@ -82,11 +90,13 @@ template <bool kQ4K>
 __host__ __device__ constexpr int dec_hbatch() { return kQ4K ? QG_DEC_HB_Q4K : 4; }
 // Rows up to which the integer dot-product kernel runs (one lane per weight
 // row; each token's 32 activation bytes of a block are loaded by every row's
-// lane) rather than fp16 MMA tiles (weights widened once per 8-token tile,
-// activations loaded once per tile); at most kDp4aMaxM.
+// lane) rather than MMA tiles (activations loaded once per 8-token tile); at
+// most kDp4aMaxM. Measured on GB300: W8A8 4 rows tie at 5120 -> 17408 and
+// favour the int8 MMA tiles at 17408 -> 5120 (24.9 vs 26.9 us); W4A8 4 rows
+// favour dp4a (23.0 vs 25.6 us).
 constexpr int kDp4aMaxM = 4;
 #ifndef QG_DEC_DP4A_MAX_Q8
-#define QG_DEC_DP4A_MAX_Q8 4
+#define QG_DEC_DP4A_MAX_Q8 3
 #endif
 #ifndef QG_DEC_DP4A_MAX_Q4K
 #define QG_DEC_DP4A_MAX_Q4K 4
@@ -309,8 +319,9 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
   }
 }
 
-// Decode GEMM on fp16 MMA tiles: 8-token tiles (TT of them), weights
-// widened to fp16 once per tile.
+// Decode GEMM on legacy MMA tiles of 16 weight rows x 8 tokens (TT tiles):
+// int8 m16n8k32 on the stored bytes, or (build switch) fp16 m16n8k16 on
+// values widened in registers.
 template <int TT, bool kQ4K, bool kDebug>
 __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const DecodeArgs a) {
   using L = DecodeSmem<TT, kQ4K, false>;
@@ -364,7 +375,61 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       if (!ok) break;
       const uint8_t* base = smem + st * SBY;
       float* stash = stash_base + xs * (L::kSlotBytes / 4);
-      {
+      if constexpr (QG_DEC_IMMA != 0) {
+        // one int8 m16n8k32 MMA per block and 8-token tile, on the stored
+        // bytes: lane (gr, c) gives k 8c..8c+7 of rows gr and gr+8 (a0/a2,
+        // a1/a3) and of its token (b0/b1), the same k on both operands; Q4_K
+        // nibbles are masked into unsigned bytes (low: k 8c..8c+3, high:
+        // 8c+4..8c+7). The int32 sums are exact; |sum| < 2^20 makes them
+        // exact in fp32 for the chain warp.
+        uint32_t af[kBlkPerWarp][4];
+#pragma unroll
+        for (int u = 0; u < kBlkPerWarp; ++u) {
+          const int j = cw * kBlkPerWarp + u;
+          if (!kQ4K) {
+            const int q = c >> 1;
+            const uint8_t* wp = base + j * 512 + 8 * (c & 1);
+            const uint2 xa = *reinterpret_cast<const uint2*>(wp + (q * 16 + (gr ^ (q << 2))) * 16);
+            const uint2 xb =
+                *reinterpret_cast<const uint2*>(wp + (q * 16 + ((gr + 8) ^ (q << 2))) * 16);
+            af[u][0] = xa.x; af[u][2] = xa.y;
+            af[u][1] = xb.x; af[u][3] = xb.y;
+          } else {
+            const uint8_t* wp = base + j * 256 + 4 * c;
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(wp + gr * 16);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(wp + (gr + 8) * 16);
+            af[u][0] = wa & 0x0F0F0F0Fu; af[u][2] = (wa >> 4) & 0x0F0F0F0Fu;
+            af[u][1] = wb & 0x0F0F0F0Fu; af[u][3] = (wb >> 4) & 0x0F0F0F0Fu;
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const int mrow = 8 * t + gr;  // token of this lane's B fragment
+#pragma unroll
+          for (int u = 0; u < kBlkPerWarp; ++u) {
+            const int j = cw * kBlkPerWarp + u;
+            uint2 bv = make_uint2(0u, 0u);
+            if (mrow < M)
+              bv = *reinterpret_cast<const uint2*>(base + L::act_off() + mrow * kARow + c * 8 + j * 32);
+            int d[4];
+            mma_i8_16832<kQ4K>(d, af[u], bv.x, bv.y);
+            // d: (n0, tok 8t+2c), (n0, 8t+2c+1), (n1, 8t+2c), (n1, 8t+2c+1)
+            if (j < nb)
+              *reinterpret_cast<float4*>(stash + ((j * TT + t) * 32 + lane) * 4) =
+                  make_float4(small_int_to_f32(d[0]), small_int_to_f32(d[1]),
+                              small_int_to_f32(d[2]), small_int_to_f32(d[3]));
+            if (kDebug && j < nb) {
+              const int b = blk0 + j;
+              const int n0 = (int)(16 * g + gr), mc0 = 8 * t + 2 * c;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int m = mc0 + (i & 1), n = n0 + ((i < 2) ? 0 : 8);
+                if (m < M && n < a.N) a.dbg[((int64_t)m * a.N + n) * B + b] = d[i];
+              }
+            }
+          }
+        }
+      } else {
         // two m16n8k16 fp16 MMAs per block and 8-token tile (this warp's
         // blocks 2cw, 2cw+1; their fragments first, so the blocks' load and
         // MMA latencies overlap)
@@ -431,14 +496,14 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
             }
           }
         }
-        if (kQ4K) {
-          // lane (r, hh): row r's d*sc and dmin*m of block 2cw + hh
-          const int r = lane & 15, j = cw * kBlkPerWarp + (lane >> 4);
-          if (j < nb) {
-            const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
-            float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
-            scw[j * 16 + r] = q4k_scales(H, j & 7);
-          }
+      }
+      if (kQ4K) {
+        // lane (r, hh): row r's d*sc and dmin*m of block 2cw + hh
+        const int r = lane & 15, j = cw * kBlkPerWarp + (lane >> 4);
+        if (j < nb) {
+          const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
+          float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
+          scw[j * 16 + r] = q4k_scales(H, j & 7);
         }
       }
       __syncwarp();

@@ -401,6 +401,28 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         "f"(c[2]), "f"(c[3]));
 }
 
+// Legacy int8 tensor-core MMA, m16n8k32, exact int32 sums from zero: A
+// (16 x 32) as signed (kUA = false) or unsigned bytes, B (32 x 8) signed.
+// Fragments: a0/a2 row g, a1/a3 row g+8 (g = lane / 4), k 4t..4t+3 for
+// a0/a1 and 16 + 4t.. for a2/a3 (t = lane % 4); b0 k 4t.., b1 k 16 + 4t..,
+// column g; d as for m16n8k16.
+template <bool kUA>
+__device__ __forceinline__ void mma_i8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  if (kUA)
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
 // Four biased bytes (q + 128) -> two fp16 pairs holding q exactly:
 // the bytes become the low mantissa bits of 1024 + (q + 128), then 1152 is
 // subtracted (all values are integers below 2048, exact in fp16).
