@@ -12,8 +12,8 @@
 // registers between the absmax pass and the quantize pass when it fits
 // (K <= kThreads*8*kRegChunks), else re-read (second read hits L2); threads
 // and register chunks are chosen from K so that several rows per SM are in
-// flight. HBM-bound: per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with
-// q16) written.
+// flight (rows longer than 10240 are re-read: see launch_q_k). HBM-bound:
+// per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with q16) written.
 #include "qg_common.cuh"
 
 namespace qg {
@@ -190,7 +190,12 @@ static void launch_q(const QArgs& a, cudaStream_t st) {
 
 template <bool kBf16, bool kStatic>
 static void launch_q_k(const QArgs& a, cudaStream_t st) {
-  // threads x register chunks x 8 values >= K where possible
+  // Up to K = 10240: threads x register chunks x 8 values >= K, the row held
+  // in registers between its two passes. Longer rows: 256 threads holding
+  // two chunks each, the rest re-read for the second pass (from L2): far
+  // fewer registers, so several times more rows in flight per SM (8192 x
+  // 17408 bf16 rows: 164 against 236 us with the row held in 256 x 9
+  // chunks; at K = 5120 and 9728 the held rows stay faster).
   const int64_t K = a.K;
   if (K <= 128 * 3 * 8)
     launch_q<kBf16, 128, 3, kStatic>(a, st);
@@ -198,10 +203,8 @@ static void launch_q_k(const QArgs& a, cudaStream_t st) {
     launch_q<kBf16, 128, 5, kStatic>(a, st);
   else if (K <= 256 * 5 * 8)
     launch_q<kBf16, 256, 5, kStatic>(a, st);
-  else if (K <= 256 * 9 * 8)
-    launch_q<kBf16, 256, 9, kStatic>(a, st);
   else
-    launch_q<kBf16, 512, 9, kStatic>(a, st);
+    launch_q<kBf16, 256, 2, kStatic>(a, st);
 }
 
 cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
