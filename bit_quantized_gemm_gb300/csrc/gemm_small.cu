@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
   constexpr int kBlkPerWarp = kSBlk / kCompWarps;
+  // (W4A8: each half-warp decodes the scales of one of the warp's blocks)
+  static_assert(!kQ4K || kBlkPerWarp == 2, "two blocks per compute warp and stage");
   extern __shared__ __align__(128) uint8_t smem[];
   const int NW = a.nw;
   const int mrows = min(a.M, TT * 8);
