@@ -521,11 +521,13 @@ def cpu_baseline(layers, rows_sample=CPU_SAMPLE_ROWS):
 
 # Token-row chunks per projection in the end-to-end step: chunk i's input
 # copy, compute and output copy overlap the neighbouring chunks' (rows are
-# batch-invariant, so chunking changes no bit of the output). One chunk per
-# projection measured fastest on GB300: the step is bound by the host copies
-# (both directions at once run at ~150 GB/s each), and smaller GEMMs plus more
-# launches cost more than the overlap gains, eager or as a CUDA graph.
-E2E_CHUNKS = (1, 1)
+# batch-invariant, so chunking changes no bit of the output). The step is
+# bound by the host copies (~210 GB/s host to device, ~190 back, ~160 each
+# when both run); only the first input copy and the last output copy stay
+# outside the overlap. Measured on GB300 for the 8192-token step (ms):
+# (1, 1) 4.42, (2, 1) 4.29, (1, 2) 4.34, (2, 2) 4.21, (4, 2) 4.23, (4, 4)
+# 4.38 -- four chunks' smaller GEMMs cost more than the shorter copies save.
+E2E_CHUNKS = (2, 2)
 
 
 def make_e2e_step(layers, dev, chunks=None):
