@@ -12,7 +12,7 @@
 // registers between the absmax pass and the quantize pass when it fits
 // (K <= kThreads*8*kRegChunks), else re-read (second read hits L2); threads
 // and register chunks are chosen from K so that several rows per SM are in
-// flight (rows longer than 10240 are re-read: see launch_q_k). HBM-bound:
+// flight (many rows, or long ones, are re-read: see launch_q_k). HBM-bound:
 // per element 2 (bf16) or 4 (fp32) bytes read, 1 (+2 with q16) written.
 #include "qg_common.cuh"
 
@@ -190,21 +190,28 @@ static void launch_q(const QArgs& a, cudaStream_t st) {
 
 template <bool kBf16, bool kStatic>
 static void launch_q_k(const QArgs& a, cudaStream_t st) {
-  // Up to K = 10240: threads x register chunks x 8 values >= K, the row held
-  // in registers between its two passes. Longer rows: 256 threads holding
-  // two chunks each, the rest re-read for the second pass (from L2): far
-  // fewer registers, so several times more rows in flight per SM (8192 x
-  // 17408 bf16 rows: 164 against 236 us with the row held in 256 x 9
-  // chunks; at K = 5120 and 9728 the held rows stay faster).
+  // Two regimes, measured on GB300 (bf16 rows, us):
+  // * many rows (M >= 1024, throughput): a thread holds one 8-value chunk and
+  //   re-reads the rest of the row for the quantize pass (from L2), so that
+  //   many rows are in flight per SM: 8192 x 5120 47.8 (row held: 51.8),
+  //   8192 x 17408 144 (held: 236), 2048 x 9728 31.3 (33.4); rows up to 3072
+  //   stay held (2048 x 2560: 15.0 both ways);
+  // * few rows (decode sizes, latency): the row is held in registers between
+  //   its two passes with threads x chunks x 8 >= K (64 x 5120: 8.8 against
+  //   10.9 re-read), and rows longer than 10240 take the 256-thread re-read
+  //   configuration (8 x 17408: 15.0 either way).
   const int64_t K = a.K;
-  if (K <= 128 * 3 * 8)
+  if (K > 256 * 5 * 8 || (a.M >= 1024 && K > 256 * 3 * 8)) {
+    launch_q<kBf16, 256, 1, kStatic>(a, st);
+  } else if (a.M >= 1024 && K > 128 * 3 * 8) {
+    launch_q<kBf16, 128, 1, kStatic>(a, st);
+  } else if (K <= 128 * 3 * 8) {
     launch_q<kBf16, 128, 3, kStatic>(a, st);
-  else if (K <= 128 * 5 * 8)
+  } else if (K <= 128 * 5 * 8) {
     launch_q<kBf16, 128, 5, kStatic>(a, st);
-  else if (K <= 256 * 5 * 8)
+  } else {
     launch_q<kBf16, 256, 5, kStatic>(a, st);
-  else
-    launch_q<kBf16, 256, 2, kStatic>(a, st);
+  }
 }
 
 cudaError_t launch_quantize_act(const void* x, bool bf16, int64_t M, int64_t K, int64_t ldx,
