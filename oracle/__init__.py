@@ -51,6 +51,10 @@ def lib():
         L.orc_q4k_decode.argtypes = [P, P, P, P, P, P, P]
         L.orc_gemm_w4a8_q4k.argtypes = [P, P, I64, I64, P, I64, P, P]
         L.orc_block_sums_q4k.argtypes = [P, I64, I64, P, I64, P, P]
+        L.orc_mxfp4_from_q8_0.argtypes = [P, I64, I64, P, P]
+        L.orc_e2m1_value.argtypes = [I]
+        L.orc_e2m1_value.restype = ctypes.c_double
+        L.orc_gemm_w4a8_mxfp4.argtypes = [P, P, I64, I64, P, P, I64, P, P]
         L.orc_num_threads.restype = I
         _lib = L
     return _lib
@@ -174,3 +178,33 @@ def block_sums_q4k(qa, sblocks):
     asum = np.empty((M, K // 32), np.int32)
     lib().orc_block_sums_q4k(_p(qa), M, K, _p(sblocks), N, _p(isum), _p(asum))
     return isum, asum
+
+
+def mxfp4_from_q8_0(blocks):
+    """Q8_0 blocks uint8 [N, K/32, 34] -> (E2M1 codes uint8 [N, K], exponents uint8 [N, K/32])."""
+    blocks = _c(blocks, np.uint8)
+    N, B, _ = blocks.shape
+    K = B * 32
+    codes = np.empty((N, K), np.uint8)
+    E = np.empty((N, B), np.uint8)
+    lib().orc_mxfp4_from_q8_0(_p(blocks), N, K, _p(codes), _p(E))
+    return codes, E
+
+
+def e2m1_value(code):
+    return lib().orc_e2m1_value(int(code))
+
+
+def gemm_w4a8_mxfp4(qa, sa, codes, E):
+    """qa int8 [M,K], sa fp32 [M], codes uint8 [N,K], E uint8 [N,K/32] -> (y fp32, out bf16 bits)."""
+    qa = _c(qa, np.int8)
+    sa = _c(sa, np.float32)
+    codes = _c(codes, np.uint8)
+    E = _c(E, np.uint8)
+    M, K = qa.shape
+    N = codes.shape[0]
+    assert codes.shape == (N, K) and E.shape == (N, K // 32)
+    y = np.empty((M, N), np.float32)
+    out = np.empty((M, N), np.uint16)
+    lib().orc_gemm_w4a8_mxfp4(_p(qa), _p(sa), M, K, _p(codes), _p(E), N, _p(y), _p(out))
+    return y, out

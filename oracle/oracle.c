@@ -270,3 +270,83 @@ void orc_gemm_w4a8_q4k(const int8_t* qa, const float* sa, int64_t M, int64_t K,
     }
   }
 }
+
+/* ---------------------------------------------------------------------- */
+/* MXFP4 weights converted from Q8_0 (the README's "Blackwell MXFP4":    */
+/* the MLP's projections in MXFP4 from a Q8_0 file, lower precision)     */
+/* ---------------------------------------------------------------------- */
+/* E2M1 element: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0. */
+double orc_e2m1_value(int code) {
+  int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+/* nearest E2M1 code to v, ties to the even mantissa, magnitudes beyond 6
+ * saturate to 6; a zero magnitude is code 0 */
+static int e2m1_round(double v) {
+  double a = fabs(v);
+  int best = 0;
+  double best_err = a;  /* code 0: magnitude 0 */
+  for (int c = 1; c < 8; ++c) {
+    double err = fabs(a - orc_e2m1_value(c));
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  if (best == 0) return 0;
+  return (v < 0) ? (best | 8) : best;
+}
+
+void orc_mxfp4_from_q8_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* codes,
+                         uint8_t* E) {
+  int64_t B = K / QBLK;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < B; ++b) {
+      const uint8_t* blk = q8_0_block(blocks, B, n, b);
+      float d = q8_0_scale(blk);
+      double w[QBLK], amax = 0.0;
+      for (int j = 0; j < QBLK; ++j) {
+        w[j] = (double)d * (double)(int8_t)blk[2 + j];  /* exact */
+        if (fabs(w[j]) > amax) amax = fabs(w[j]);
+      }
+      int e = 127;  /* an all-zero block: X = 1 */
+      if (amax > 0.0) {
+        int p;
+        frexp(amax, &p);         /* amax = f * 2^p, f in [0.5, 1) */
+        e = (p - 1) - 2 + 127;   /* floor(log2(amax)) - emax(E2M1) + bias */
+        if (e < 0) e = 0;
+        if (e > 254) e = 254;
+      }
+      E[n * B + b] = (uint8_t)e;
+      double X = ldexp(1.0, e - 127);
+      for (int j = 0; j < QBLK; ++j) codes[n * K + b * QBLK + j] = (uint8_t)e2m1_round(w[j] / X);
+    }
+}
+
+void orc_gemm_w4a8_mxfp4(const int8_t* qa, const float* sa, int64_t M, int64_t K,
+                         const uint8_t* codes, const uint8_t* E, int64_t N, float* y,
+                         uint16_t* out) {
+  int64_t B = K / QBLK;
+  for (int64_t m = 0; m < M; ++m) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+      float acc = 0.0f;
+      for (int64_t b = 0; b < B; ++b) {  /* ascending K blocks */
+        int32_t is = 0;                    /* exact: |2v| <= 12 */
+        for (int j = 0; j < QBLK; ++j) {
+          int c2 = (int)lrint(2.0 * orc_e2m1_value(codes[n * K + b * QBLK + j]));
+          is += (int32_t)qa[m * K + b * QBLK + j] * c2;
+        }
+        /* weight = (2v) * X / 2: the block scale as an exact fp32 power of two */
+        acc = fmaf((float)is, ldexpf(1.0f, (int)E[n * B + b] - 128), acc);
+      }
+      float v = acc * sa[m];
+      if (y) y[m * N + n] = v;
+      if (out) out[m * N + n] = orc_f32_to_bf16(v);
+    }
+  }
+}

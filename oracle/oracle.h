@@ -97,6 +97,29 @@ void orc_block_sums_q4k(const int8_t* qa, int64_t M, int64_t K,
 /* Number of OpenMP threads the GEMM loops use (1 without OpenMP). */
 int orc_num_threads(void);
 
+/* MXFP4 weights from Q8_0 (README, "Supported models and GPUs" and "Blackwell
+ * MXFP4": --precision mxfp4 runs the MLP's projections in MXFP4 from a Q8_0
+ * file, at lower precision). The pages give no conversion rule; the reading
+ * taken (the OCP microscaling format): 32-element blocks along K share an
+ * 8-bit exponent E, scale X = 2^(E-127); elements are E2M1 codes (sign bit 3,
+ * exponent bits 2..1 with bias 1, mantissa bit 0: magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6). For a block of Q8_0 values w = d*q: E = floor(log2(max|w|)) -
+ * 2 + 127 (clamped to [0, 254]; an all-zero block takes E = 127), and each
+ * w/X goes to the nearest E2M1 value, ties to the even mantissa, magnitudes
+ * above 6 saturating at 6.
+ * codes: [N][K] one code per weight (0..15); E: [N][K/32]. */
+void orc_mxfp4_from_q8_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* codes,
+                         uint8_t* E);
+/* The value of an E2M1 code. */
+double orc_e2m1_value(int code);
+/* W4A8 with MXFP4 weights: per K block the exact sum isum = sum q_a * (2v)
+ * (2v in -12..12, an integer), then acc = fmaf((float)isum, 2^(E-128), acc)
+ * in ascending blocks, y = acc * s_a, bf16 round-to-nearest-even: the W8A8
+ * chain with integer weights 2v and block scales X/2. */
+void orc_gemm_w4a8_mxfp4(const int8_t* qa, const float* sa, int64_t M, int64_t K,
+                         const uint8_t* codes, const uint8_t* E, int64_t N, float* y,
+                         uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -133,3 +133,33 @@ def q4k_case_arrays(case):
         for i, v in bytes_.items():
             sb[n, i] = v
     return x, sb.reshape(N, K // 256, 144)
+
+
+def mxfp4_cases(name="mxfp4_small.txt"):
+    """Cases of mxfp4_small.txt: dicts with d (fp16 bits), q, qa, E, codes, y (bf16 bits)."""
+    cases, cur = [], None
+    for line in _lines(name):
+        key, _, rest = line.partition(" ")
+        if key == "case":
+            cur = {"name": rest}
+            cases.append(cur)
+        elif key in ("d", "y"):
+            cur[key] = int(rest, 16)
+        elif key == "E":
+            cur[key] = int(rest)
+        else:
+            cur[key] = [int(v) for v in rest.split()]
+    return cases
+
+
+def mxfp4_case_arrays(case, K=32):
+    """One Q8_0 block row (uint8 [1, K/32, 34]) and an int8 activation row [1, K] of a case."""
+    import numpy as np
+    blocks = np.zeros((1, K // 32, 34), np.uint8)
+    blocks[0, 0, 0] = case["d"] & 0xFF
+    blocks[0, 0, 1] = case["d"] >> 8
+    for j, v in enumerate(case["q"]):
+        blocks[0, 0, 2 + j] = np.uint8(v & 0xFF)
+    qa = np.zeros((1, K), np.int8)
+    qa[0, :len(case["qa"])] = case["qa"]
+    return blocks, qa
