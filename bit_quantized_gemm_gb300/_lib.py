@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SO_PATH = os.path.join(HERE, "libqgemm.so")
 HEADER = os.path.join(HERE, "..", "include", "qgemm.h")
 
-QG_OK, QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA, QG_ETIMEOUT = range(6)
+QG_OK, QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA, QG_ETIMEOUT, QG_ERANGE = range(7)
 QG_BF16, QG_F32 = 0, 1
 QG_PATH_AUTO, QG_PATH_SMALL, QG_PATH_LARGE = 0, 1, 2
 PATHS = {"auto": QG_PATH_AUTO, "small": QG_PATH_SMALL, "large": QG_PATH_LARGE}
@@ -63,6 +63,10 @@ def load():
         "qg_linear_w8a8_q8_0": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w4a8_q4k": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w8a8_q8_0_noalloc": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P], I),
+        "qg_mxfp4_packed_bytes": ([I64, I64], SZ),
+        "qg_pack_mxfp4_q8_0": ([P, I64, I64, P, P], I),
+        "qg_gemm_w4a8_mxfp4": ([P, P, P, I64, I64, P, I64, P, I, I64, P], I),
+        "qg_linear_w4a8_mxfp4": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
     }
     for name, (args, res) in sigs.items():
         f = getattr(L, name)
@@ -224,7 +228,7 @@ def linear_workspace_bytes(kind, M, K):
     return int(load().qg_linear_workspace_bytes(0 if kind == "q8_0" else 1, M, K))
 
 
-def _linear(kind, x, packed, N, out, out_dtype, scale_out, workspace, stream):
+def _linear(kind, x, packed, N, out, out_dtype, scale_out, workspace, stream, fn=None):
     assert x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     if out is None:
@@ -233,7 +237,8 @@ def _linear(kind, x, packed, N, out, out_dtype, scale_out, workspace, stream):
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    fn = load().qg_linear_w8a8_q8_0 if kind == "q8_0" else load().qg_linear_w4a8_q4k
+    if fn is None:
+        fn = load().qg_linear_w8a8_q8_0 if kind == "q8_0" else load().qg_linear_w4a8_q4k
     _check(fn(_ptr(x), _dtype_code(x.dtype), M, K, x.stride(0), _ptr(packed), N, _ptr(out),
               _dtype_code(out.dtype), out.stride(0), _ptr(scale_out), _ptr(workspace), nbytes,
               _stream(stream)))
@@ -253,6 +258,36 @@ def linear_w4a8_q4k(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=
                     workspace=None, stream=None):
     """As linear_w8a8_q8_0, with Q4_K weights."""
     return _linear("q4k", x, packed, N, out, out_dtype, scale_out, workspace, stream)
+
+
+def pack_mxfp4_q8_0(blocks, N, K, stream=None):
+    """Q8_0 blocks (cuda uint8, N*K/32 x 34 bytes) converted to MXFP4 and packed
+    (lossy: see include/qgemm.h). check_device_error() raises QG_ERANGE when a
+    block scale does not fit the decode kernels' fp16 scales."""
+    nbytes = int(load().qg_mxfp4_packed_bytes(N, K))
+    if nbytes == 0:
+        raise QGError(QG_EINVAL, "bad N/K for MXFP4")
+    packed = torch.empty((nbytes,), dtype=torch.uint8, device=blocks.device)
+    _check(load().qg_pack_mxfp4_q8_0(_ptr(blocks), N, K, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def gemm_w4a8_mxfp4(q, q16, scale, packed, N, out=None, out_dtype=torch.bfloat16, stream=None):
+    """As gemm_w8a8_q8_0 (AUTO path), on weights from pack_mxfp4_q8_0."""
+    M, K = (q if q is not None else q16).shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=(q if q is not None else q16).device)
+    _check(load().qg_gemm_w4a8_mxfp4(_ptr(q), _ptr(q16), _ptr(scale), M, K, _ptr(packed), N,
+                                     _ptr(out), _dtype_code(out.dtype), out.stride(0),
+                                     _stream(stream)))
+    return out
+
+
+def linear_w4a8_mxfp4(x, packed, N, out=None, out_dtype=torch.bfloat16, scale_out=None,
+                      workspace=None, stream=None):
+    """As linear_w8a8_q8_0, on weights from pack_mxfp4_q8_0."""
+    return _linear("q8_0", x, packed, N, out, out_dtype, scale_out, workspace, stream,
+                   fn=load().qg_linear_w4a8_mxfp4)
 
 
 def linear_noalloc_scratch_bytes():

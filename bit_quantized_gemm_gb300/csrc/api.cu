@@ -20,6 +20,8 @@ cudaError_t launch_pack_q8_0(const void* blocks, int64_t N, int64_t K, void* pac
                              cudaStream_t st);
 cudaError_t launch_pack_q4k(const void* sblocks, int64_t N, int64_t K, void* packed,
                             cudaStream_t st);
+cudaError_t launch_pack_mxfp4_q8_0(const void* blocks, int64_t N, int64_t K, void* packed,
+                                   uint32_t* err, cudaStream_t st);
 // pdl: launch with programmatic stream serialization (the kernel may start
 // while the previous kernel on the stream, the quantize kernel, still runs)
 cudaError_t launch_decode_q8_0(const int8_t* qa, const float* sa, int64_t M, int64_t K,
@@ -281,7 +283,11 @@ qg_status qg_check_device_error(void* stream) {
   if (v) {
     const uint32_t zero = 0;
     cudaMemcpyToSymbol(g_error_word_dev, &zero, sizeof(zero));
-    return fail(QG_ETIMEOUT, "device error word 0x%x: a bounded barrier wait gave up", v);
+    if (v & kErrTimeout)
+      return fail(QG_ETIMEOUT, "device error word 0x%x: a bounded barrier wait gave up", v);
+    return fail(QG_ERANGE,
+                "device error word 0x%x: a packed MXFP4 block scale is outside fp16's range "
+                "(the decode kernels' scales)", v);
   }
   return QG_OK;
 }
@@ -450,6 +456,37 @@ qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t
                              int64_t ldo, float* scale_out, void* workspace,
                              size_t workspace_bytes, void* stream) {
   return linear(true, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out,
+                workspace, workspace_bytes, stream);
+}
+
+size_t qg_mxfp4_packed_bytes(int64_t N, int64_t K) { return qg_q8_0_packed_bytes(N, K); }
+
+qg_status qg_pack_mxfp4_q8_0(const void* blocks, int64_t N, int64_t K, void* packed,
+                             void* stream) {
+  if (!blocks || !packed) return fail(QG_EINVAL, "null pointer argument");
+  if (N < 1 || N > kMaxN) return fail(QG_EINVAL, "N=%lld out of range [1, 2^24]", (long long)N);
+  qg_status s = check_k(K, kBlk);
+  if (s != QG_OK) return s;
+  if (!aligned(packed, 256)) return fail(QG_EALIGN, "packed needs 256-byte alignment");
+  return from_cuda(launch_pack_mxfp4_q8_0(blocks, N, K, packed, error_word(),
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                   "pack launch");
+}
+
+// The converted weights are integers 2v with scales 2^(E-128) in the Q8_0
+// packed layout: the W8A8 GEMM and layer call run them unchanged.
+qg_status qg_gemm_w4a8_mxfp4(const int8_t* q, const uint16_t* q16, const float* scale,
+                             int64_t M, int64_t K, const void* w_packed, int64_t N, void* out,
+                             qg_dtype out_dtype, int64_t ldo, void* stream) {
+  return gemm_q8_0(q, q16, scale, M, K, w_packed, N, out, out_dtype, ldo, QG_PATH_AUTO, nullptr,
+                   stream);
+}
+
+qg_status qg_linear_w4a8_mxfp4(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                               int64_t ldx, const void* w_packed, int64_t N, void* out,
+                               qg_dtype out_dtype, int64_t ldo, float* scale_out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return linear(false, x, x_dtype, M, K, ldx, w_packed, N, out, out_dtype, ldo, scale_out,
                 workspace, workspace_bytes, stream);
 }
 

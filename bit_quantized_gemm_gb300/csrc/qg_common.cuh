@@ -28,6 +28,7 @@ constexpr int kMaxK = 65536;
 
 // Error word codes (device-side, read by qg_check_device_error).
 constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrRange = 2u;  // a packed value outside its format's range
 
 __host__ __device__ constexpr int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -61,7 +61,8 @@ typedef enum {
   QG_EALIGN = 2,        /* pointer or leading dimension not aligned         */
   QG_EUNSUPPORTED = 3,  /* valid request that no kernel here implements     */
   QG_ECUDA = 4,         /* CUDA runtime/launch error                        */
-  QG_ETIMEOUT = 5       /* a bounded device-side wait gave up               */
+  QG_ETIMEOUT = 5,      /* a bounded device-side wait gave up               */
+  QG_ERANGE = 6         /* a packed value outside its format's range        */
 } qg_status;
 
 typedef enum { QG_BF16 = 0, QG_F32 = 1 } qg_dtype;
@@ -191,10 +192,11 @@ qg_status qg_gemm_w4a8_q4k_ex(const int8_t* q, const uint16_t* q16, const float*
 /* The whole layer in one call: x in, y out. qg_quantize_act (the dynamic    */
 /* per-token scales) into the caller's workspace, then the GEMM (AUTO), with */
 /* the bits of those two calls made separately.                              */
-/*   M <= qg_small_m_max(): the decode GEMM is launched as a programmatic    */
-/*     dependent of the quantize kernel: its CTAs start while the rows are   */
-/*     quantized, request their first weight stages, and copy activations   */
-/*     only after the quantize grid has completed.                           */
+/*   The GEMM's first launch (decode kernel for M <= qg_small_m_max(),      */
+/*     prefill or 16-row kernel above) is a programmatic dependent of the    */
+/*     quantize kernel: its CTAs start while the rows are quantized, request */
+/*     their first weight stages, and read activations and scales only after */
+/*     the quantize grid has completed.                                      */
 /*   x          [M][ldx] of x_dtype, 16-byte aligned, ldx >= K,              */
 /*              ldx*elem_size % 16 == 0.                                      */
 /*   w_packed   from qg_pack_q8_0 / qg_pack_q4k with the same N, K.          */
@@ -220,6 +222,41 @@ qg_status qg_linear_w4a8_q4k(const void* x, qg_dtype x_dtype, int64_t M, int64_t
                              const void* w_packed, int64_t N, void* out, qg_dtype out_dtype,
                              int64_t ldo, float* scale_out, void* workspace,
                              size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* MXFP4 weights from Q8_0 (StartLux-Prism README, "Supported models and     */
+/* GPUs" and "Blackwell MXFP4": --precision mxfp4 runs the MLP's projections */
+/* in MXFP4, from a Q8_0 file, at lower precision). Lossy in the conversion  */
+/* only: qg_pack_mxfp4_q8_0 rounds each Q8_0 block to MXFP4 -- 32 values     */
+/* sharing X = 2^(E-127), E = floor(log2 max|w|) - 2 + 127 (an all-zero       */
+/* block: 127), each w/X to the nearest E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4, */
+/* 6, signed; ties to the even mantissa; saturating at 6). Twice an E2M1     */
+/* value is an integer in [-12, 12], so the GEMM is the W8A8 one on integer  */
+/* weights 2v with block scales X/2 = 2^(E-128): exact int32 block sums and  */
+/* the same fixed-order fp32 epilogue, bit-reproducible like W8A8.           */
+/*   qg_mxfp4_packed_bytes / qg_pack_mxfp4_q8_0: as qg_q8_0_packed_bytes /   */
+/*     qg_pack_q8_0 (the same layout and buffer rules); the packed values    */
+/*     are the converted ones. A block whose X/2 lies outside fp16's range   */
+/*     (2^-24 .. 2^15; the decode kernels hold block scales in fp16) makes   */
+/*     the next qg_check_device_error() return QG_ERANGE; such a buffer must */
+/*     not be used by the decode kernel (M <= qg_small_m_max()).             */
+/*   qg_gemm_w4a8_mxfp4, qg_linear_w4a8_mxfp4: as qg_gemm_w8a8_q8_0 and       */
+/*     qg_linear_w8a8_q8_0 (workspace kind 0), on a buffer from               */
+/*     qg_pack_mxfp4_q8_0.                                                    */
+/* The pages ran this on Blackwell's block-scaled tensor cores; here the     */
+/* integer sums run on the int8 paths and the power-of-two block scale is     */
+/* applied in the fixed-order fp32 epilogue, so the bits stay reproducible.   */
+/* ------------------------------------------------------------------------ */
+size_t qg_mxfp4_packed_bytes(int64_t N, int64_t K);
+qg_status qg_pack_mxfp4_q8_0(const void* blocks, int64_t N, int64_t K, void* packed,
+                             void* stream);
+qg_status qg_gemm_w4a8_mxfp4(const int8_t* q, const uint16_t* q16, const float* scale,
+                             int64_t M, int64_t K, const void* w_packed, int64_t N, void* out,
+                             qg_dtype out_dtype, int64_t ldo, void* stream);
+qg_status qg_linear_w4a8_mxfp4(const void* x, qg_dtype x_dtype, int64_t M, int64_t K,
+                               int64_t ldx, const void* w_packed, int64_t N, void* out,
+                               qg_dtype out_dtype, int64_t ldo, float* scale_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* The W8A8 layer call without a workspace argument and without allocating   */

@@ -136,30 +136,42 @@ def q4k_case_arrays(case):
 
 
 def mxfp4_cases(name="mxfp4_small.txt"):
-    """Cases of mxfp4_small.txt: dicts with d (fp16 bits), q, qa, E, codes, y (bf16 bits)."""
+    """Cases of mxfp4_small.txt: dicts with d (fp16 bits per block), q, qa,
+    codes (index -> value; a plain list means indices 0, 1, ...), E (per
+    block), y (bf16 bits) and optionally y32 (fp32 bits)."""
     cases, cur = [], None
     for line in _lines(name):
         key, _, rest = line.partition(" ")
         if key == "case":
             cur = {"name": rest}
             cases.append(cur)
-        elif key in ("d", "y"):
+        elif key == "d":
+            cur[key] = [int(v, 16) for v in rest.split()]
+        elif key in ("y", "y32"):
             cur[key] = int(rest, 16)
         elif key == "E":
-            cur[key] = int(rest)
-        else:
             cur[key] = [int(v) for v in rest.split()]
+        else:  # q, qa, codes: dense values, or sparse index=value tokens
+            toks = rest.split()
+            if "=" in toks[0]:
+                cur[key] = {int(k): int(v) for k, v in (t.split("=") for t in toks)}
+            else:
+                cur[key] = {i: int(v) for i, v in enumerate(toks)}
     return cases
 
 
-def mxfp4_case_arrays(case, K=32):
-    """One Q8_0 block row (uint8 [1, K/32, 34]) and an int8 activation row [1, K] of a case."""
+def mxfp4_case_arrays(case):
+    """The case's Q8_0 row (uint8 [1, K/32, 34]) and int8 activation row [1, K], K = 32 x blocks."""
     import numpy as np
-    blocks = np.zeros((1, K // 32, 34), np.uint8)
-    blocks[0, 0, 0] = case["d"] & 0xFF
-    blocks[0, 0, 1] = case["d"] >> 8
-    for j, v in enumerate(case["q"]):
-        blocks[0, 0, 2 + j] = np.uint8(v & 0xFF)
+    nb = len(case["d"])
+    K = 32 * nb
+    blocks = np.zeros((1, nb, 34), np.uint8)
+    for b, d in enumerate(case["d"]):
+        blocks[0, b, 0] = d & 0xFF
+        blocks[0, b, 1] = d >> 8
+    for k, v in case["q"].items():
+        blocks[0, k // 32, 2 + k % 32] = np.uint8(v & 0xFF)
     qa = np.zeros((1, K), np.int8)
-    qa[0, :len(case["qa"])] = case["qa"]
+    for k, v in case["qa"].items():
+        qa[0, k] = v
     return blocks, qa
