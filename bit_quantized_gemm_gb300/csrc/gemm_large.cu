@@ -80,6 +80,9 @@ namespace qg {
 #ifndef QG_CHUNK
 #define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
 #endif
+#ifndef QG_W4_BM32
+#define QG_W4_BM32 1  // W4A8 GEMMs of at most 64 tokens may run 32-token tiles
+#endif
 #ifndef QG_PAIR_WAIT
 #define QG_PAIR_WAIT 1  // W4A8 (stage mode): one accumulator wait per stage of two blocks
 #endif
@@ -924,8 +927,15 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.pdl = (pdl && !dbg) ? 1 : 0;
   constexpr int BM = QG_BM_W4A8;
   if (dbg) return launch_prefill_t<true, true, BM>(ta, q16, a, st);
-  // a GEMM of at most 64 tokens fills half of a 128-token tile: 64-token tiles
-  if (M <= 64) return launch_prefill_t<true, false, 64>(ta, q16, a, st);
+  // a GEMM of at most 64 tokens fills half of a 128-token tile: 64-token
+  // tiles, or 32-token tiles when there are too few weight-row tiles to fill
+  // half the SMs (each tile walks all of K alone, so tile count sets the pace)
+  if (M <= 64) {
+    const int64_t NT = ceil_div(N, (int64_t)kBN);
+    if (QG_W4_BM32 && (M <= 32 || 2 * NT <= num_sms()))
+      return launch_prefill_t<true, false, 32>(ta, q16, a, st);
+    return launch_prefill_t<true, false, 64>(ta, q16, a, st);
+  }
   return launch_prefill_t<true, false, BM>(ta, q16, a, st);
 }
 

@@ -132,6 +132,21 @@ def test_w4a8_q4k():
             check_sampled(out, oq, os_, sblocks, "w4a8", n_rows=128, n_cols=128, seed=M)
 
 
+def test_w4a8_q4k_narrow_down_projection():
+    # 17408 -> 5120 at 32 and 64 tokens: 40 weight-row tiles, so these run as
+    # 32-token tiles, each walking all 544 sub-blocks; every output compared
+    K, N = 17408, 5120
+    sblocks = synth.config_weights("w4a8_q4k", N, K)
+    packed = qg.pack_q4k(to_dev(sblocks), N, K)
+    for M in (32, 64):
+        (q, s, bs, h), oq, os_ = quant_full("w4a8_q4k", M, K, bsum=True)
+        out = qg.gemm_w4a8_q4k(q, h, s, bs, packed, N)
+        torch.cuda.synchronize()
+        qg.check_device_error()
+        _, ob = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+        assert np.array_equal(bits_of(out), ob), M
+
+
 def test_tiny_config():
     M, K, N = synth.CONFIGS["tiny_w8a8"]["shapes"][0]
     x, _ = synth.config_activations("tiny_w8a8", M, K)
