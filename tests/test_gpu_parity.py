@@ -128,6 +128,27 @@ def test_w8a8_matches_oracle(M, K, N, path):
     assert np.array_equal(out_bits(out32), y.view(np.uint32))
 
 
+@pytest.mark.parametrize("M", [1, 3, 9, 20, 200])
+def test_longest_k_both_formats(M):
+    """K at its upper limit (65536: 2048 blocks, 256 Q4_K super-blocks) on
+    every kernel the row count selects (integer decode, int8-MMA decode,
+    narrow and 16-row tiles, tensor-memory tiles); W8A8 and W4A8 outputs and
+    the layer call against the oracle, every element."""
+    K, N = 65536, 40
+    x, bits = synth.activations(M + 3, M, K, dtype="bf16", outlier_frac=0.01)
+    oq, os_, _ = oracle.quantize_act(bits, bsum=True)
+    blocks = synth.q8_0_weights(M + 11, N, K)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    out, (q, h, s, packed) = gpu_w8a8(x, bits, blocks, N, "auto")
+    assert np.array_equal(out_bits(out), ob)
+    lay = qg.linear_w8a8_q8_0(bf16_dev(bits), packed, N)
+    assert np.array_equal(out_bits(lay), ob)
+    sblocks = synth.q4k_weights(M + 13, N, K)
+    _, ob4 = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+    out4, _ = gpu_w4a8(bits, sblocks, N, "auto")
+    assert np.array_equal(out_bits(out4), ob4)
+
+
 def test_w8a8_tiny_config_both_paths():
     M, K, N = synth.CONFIGS["tiny_w8a8"]["shapes"][0]
     x, _ = synth.config_activations("tiny_w8a8", M, K)
