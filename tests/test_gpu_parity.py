@@ -149,6 +149,24 @@ def test_longest_k_both_formats(M):
     assert np.array_equal(out_bits(out4), ob4)
 
 
+@pytest.mark.parametrize("M,K,N,tb", [(32, 9728, 128, 32), (2048, 9728, 128, 64),
+                                      (4096, 2560, 128, 128)])
+def test_skinny_tiles_every_token_width(M, K, N, tb):
+    """The 16-row kernel at each of its token-tile widths (the wave plan
+    sends these whole GEMMs to it on 152 SMs), on the 2048 x 9728 x 128 shape
+    among them; every output against the oracle."""
+    from bit_quantized_gemm_gb300 import _lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert _lib.prefill_plan(M, N, sms) == (0, "16-row", tb)
+    x, bits, blocks = make_w8a8(M, K, N, seed=M + 5 * tb, outl=0.02)
+    out, _ = gpu_w8a8(x, bits, blocks, N, "auto")
+    oq, os_ = oracle.quantize_act(bits)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    bad = np.argwhere(out_bits(out) != ob)
+    assert bad.size == 0, "first mismatches %s" % bad[:5].tolist()
+
+
 def test_w8a8_tiny_config_both_paths():
     M, K, N = synth.CONFIGS["tiny_w8a8"]["shapes"][0]
     x, _ = synth.config_activations("tiny_w8a8", M, K)
