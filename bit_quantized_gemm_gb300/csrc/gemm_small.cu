@@ -49,9 +49,11 @@ constexpr int kCompWarps = 8;      // compute warps per CTA
 // K blocks per pipeline stage. MMA tiles: 16 for both formats (8 KB of Q8_0
 // weights, 4 KB of Q4_K nibbles per 16-row group); Q4_K once took 32, but
 // its stash then left room for two stages in flight (16 measured 43 %
-// faster at 16 rows, equal at 1 and 8). Integer dot products: 16 for Q8_0,
-// 32 for Q4_K, whose 4 KB stages are otherwise too short for the fixed
-// per-stage work (barrier waits, hand-over) of every warp.
+// faster at 16 rows, equal at 1 and 8). Integer dot products: 32 for both
+// (16 KB of Q8_0, 8 KB of Q4_K nibbles per stage): shorter stages are too
+// short for the fixed per-stage work (barrier waits, hand-over) of every
+// warp (Q8_0 at 16: 17408 -> 5120 M = 1 20.7 against 19.0 us), longer ones
+// leave too few stages in flight (Q4_K at 48 or 64: 18.7 against 16.6 us).
 #ifndef QG_DEC_SBLK_Q8
 #define QG_DEC_SBLK_Q8 16
 #endif
@@ -59,7 +61,7 @@ constexpr int kCompWarps = 8;      // compute warps per CTA
 #define QG_DEC_SBLK_Q4K 16
 #endif
 #ifndef QG_DEC_SBLK_DP4A_Q8
-#define QG_DEC_SBLK_DP4A_Q8 16
+#define QG_DEC_SBLK_DP4A_Q8 32
 #endif
 #ifndef QG_DEC_SBLK_DP4A_Q4K
 #define QG_DEC_SBLK_DP4A_Q4K 32
