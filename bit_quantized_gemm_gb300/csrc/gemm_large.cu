@@ -126,7 +126,15 @@ __host__ __device__ constexpr int stages_for() {
                          (kQ4K ? kAsumRing : 1) * BM * 4 +
                          kEpiWarps * kCols * 4 + 2048;  // + barriers and alignment slack
   constexpr int kPer = (int)kStageABytes + BM * kBK * 2;
-  constexpr int n = (226 * 1024 - kFixed) / kPer;
+  constexpr int n0 = (226 * 1024 - kFixed) / kPer;
+  // Tiles with at least four accumulators alternate whole stages between the
+  // two MMA issuers, each waiting only on its own stages' barriers. With an
+  // even depth every ring slot belongs to one issuer, which then sees every
+  // phase of it; with an odd depth a slot alternates between the issuers, so
+  // each would see every other phase, and a parity wait could take a phase
+  // two loads old for the one it needs.
+  constexpr bool kAlternating = kTmemCols / BM >= 4;
+  constexpr int n = kAlternating ? n0 & ~1 : n0;
   // (W4A8 keeps 4: a deeper ring measured ~25 % slower there)
   constexpr int cap = kQ4K ? 4 : 12;
   return QG_STAGES ? QG_STAGES : (n > cap ? cap : n);
@@ -196,6 +204,7 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
   constexpr int kEpiWarps = C::kEpiWarps;
   constexpr int kStages = stages_for<kQ4K, BM>();
   constexpr bool kStageMode = C::kTBufs % 4 == 0;
+  static_assert(!kStageMode || kStages % 2 == 0, "alternating issuers need an even ring");
   constexpr int kBM = C::kBM;
   constexpr int kTBufs = C::kTBufs;
   constexpr uint32_t kStageBBytes = C::kStageBBytes;
