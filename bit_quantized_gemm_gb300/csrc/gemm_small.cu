@@ -110,6 +110,9 @@ static_assert(QG_DEC_DP4A_MAX_Q8 <= kDp4aMaxM && QG_DEC_DP4A_MAX_Q4K <= kDp4aMax
 #ifndef QG_DEC_BUDGET_TT2_KB
 #define QG_DEC_BUDGET_TT2_KB 70
 #endif
+#ifndef QG_DEC_EARLY
+#define QG_DEC_EARLY 1  // int8-MMA kernel: the compute warps release each stage
+#endif
 #ifndef QG_DEC_CHAIN_UNROLL
 #define QG_DEC_CHAIN_UNROLL 1  // chain warp: a full stage's block quads unrolled
 #endif
@@ -138,7 +141,13 @@ struct DecodeSmem {
       kDp4a ? kSBlk * kPairs * 16 * (kQ4K ? 16 : 8) : kSBlk * TT * 32 * 16;
   static constexpr int kScBytes = (kQ4K && !kDp4a) ? kSBlk * 16 * 8 : 0;
   static constexpr int kAsBytes = (kQ4K && kDp4a) ? kSBlk * kDp4aMaxM * 4 : 0;
-  static constexpr int kSlotBytes = kXBytes + kScBytes + kAsBytes;
+  // MMA tiles: the chain warp's inputs that arrive with the stage (Q8_0
+  // scales; Q4_K activation block sums of up to TT*8 rows), copied into the
+  // stash by the compute warps so that they, not the chain, release the stage
+  static constexpr bool kEarly = !kDp4a && QG_DEC_EARLY != 0;
+  static constexpr int kCdBytes = kEarly ? (kQ4K ? TT * 8 * kSBlk * 4 : kSBytes) : 0;
+  static constexpr int kCdOff = kXBytes + kScBytes + kAsBytes;
+  static constexpr int kSlotBytes = kXBytes + kScBytes + kAsBytes + kCdBytes;
   static constexpr int kMaxNw = 8;
   static __host__ __device__ int stage_bytes(int mrows) {
     return (int)align_up(kWBytes + kSBytes + mrows * kARow + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
@@ -338,7 +347,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   const int SBY = L::stage_bytes(mrows);
   float* stash_base = reinterpret_cast<float*>(smem + NW * SBY);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kSlotBytes);
-  uint64_t* empty = full + NW;    // weight stage consumed by the chain warp
+  uint64_t* empty = full + NW;    // weight stage consumed (compute warps, or the chain warp)
   uint64_t* xfull = empty + NW;   // stash slot written (count: compute warps)
   uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -350,7 +359,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], L::kEarly ? kCompWarps : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&xfull[i], kCompWarps);
@@ -510,8 +519,19 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
           scw[j * 16 + r] = q4k_scales(H, j & 7);
         }
       }
+      if constexpr (L::kEarly) {
+        // the chain's inputs from the stage into the stash, 16 bytes a lane
+        const int nchunk = (kQ4K ? mrows * kSBlk * 4 : L::kSBytes) / 16;
+        const uint8_t* src = base + (kQ4K ? L::bsum_off(mrows) : L::kWBytes);
+        uint8_t* dst = reinterpret_cast<uint8_t*>(stash) + L::kCdOff;
+        for (int i = cw * 32 + lane; i < nchunk; i += kCompWarps * 32)
+          *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(src + 16 * i);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&xfull[xs]);
+      if (lane == 0) {
+        mbar_arrive(&xfull[xs]);
+        if (L::kEarly) mbar_arrive(&empty[st]);  // this warp's reads of the stage are done
+      }
       if (++st == NW) { st = 0; ph ^= 1; }
       if (++xs == 2) { xs = 0; xph ^= 1; }
     }
@@ -534,9 +554,10 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     ok = mbar_wait(&xfull[xs], xph, a.err);
     if (!ok) break;
     const uint8_t* base = smem + st * SBY;
-    const uint8_t* sb = base + L::kWBytes;
-    const int32_t* bb = reinterpret_cast<const int32_t*>(base + L::bsum_off(mrows));
     const float* stash = stash_base + xs * (L::kSlotBytes / 4);
+    const uint8_t* cd = reinterpret_cast<const uint8_t*>(stash) + L::kCdOff;
+    const uint8_t* sb = L::kEarly ? cd : base + L::kWBytes;
+    const int32_t* bb = reinterpret_cast<const int32_t*>(L::kEarly ? cd : base + L::bsum_off(mrows));
     const float2* scs = reinterpret_cast<const float2*>(stash + L::kXBytes / 4);  // [block][row]
     // blocks in groups of kG (a quad of Q8_0 scales); a full stage's quads
     // are unrolled so that later quads' shared loads overlap earlier FMAs
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&xempty[xs]);
-      mbar_arrive(&empty[st]);
+      if (!L::kEarly) mbar_arrive(&empty[st]);
     }
     if (++st == NW) { st = 0; ph ^= 1; }
     if (++xs == 2) { xs = 0; xph ^= 1; }
