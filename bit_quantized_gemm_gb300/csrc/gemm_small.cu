@@ -46,10 +46,11 @@ constexpr int kCompWarps = 8;      // compute warps per CTA
 #define QG_DEC_IMMA 1
 #endif
 
-// K blocks per pipeline stage. MMA tiles: 16 for both formats (8 KB of Q8_0
-// weights, 4 KB of Q4_K nibbles per 16-row group); Q4_K once took 32, but
-// its stash then left room for two stages in flight (16 measured 43 %
-// faster at 16 rows, equal at 1 and 8). Integer dot products: 32 for both
+// K blocks per pipeline stage. MMA tiles: 16 for Q8_0 (8 KB of weights per
+// 16-row group; 32 measured 8-35 % slower at 4-16 rows); Q4_K 32 with one
+// 8-token tile (8 KB of nibbles: 5-8 rows 6-21 % faster than 16) and 16
+// with two, whose larger stash would leave too few stages in flight (32
+// measured 35 % slower at 12 and 16 rows). Integer dot products: 32 for both
 // (16 KB of Q8_0, 8 KB of Q4_K nibbles per stage): shorter stages are too
 // short for the fixed per-stage work (barrier waits, hand-over) of every
 // warp (Q8_0 at 16: 17408 -> 5120 M = 1 20.7 against 19.0 us), longer ones
@@ -60,16 +61,19 @@ constexpr int kCompWarps = 8;      // compute warps per CTA
 #ifndef QG_DEC_SBLK_Q4K
 #define QG_DEC_SBLK_Q4K 16
 #endif
+#ifndef QG_DEC_SBLK_Q4K_TT1
+#define QG_DEC_SBLK_Q4K_TT1 32
+#endif
 #ifndef QG_DEC_SBLK_DP4A_Q8
 #define QG_DEC_SBLK_DP4A_Q8 32
 #endif
 #ifndef QG_DEC_SBLK_DP4A_Q4K
 #define QG_DEC_SBLK_DP4A_Q4K 32
 #endif
-template <bool kQ4K, bool kDp4a>
+template <int TT, bool kQ4K, bool kDp4a>
 __host__ __device__ constexpr int sblk() {
   return kDp4a ? (kQ4K ? QG_DEC_SBLK_DP4A_Q4K : QG_DEC_SBLK_DP4A_Q8)
-               : (kQ4K ? QG_DEC_SBLK_Q4K : QG_DEC_SBLK_Q8);
+               : (kQ4K ? (TT == 1 ? QG_DEC_SBLK_Q4K_TT1 : QG_DEC_SBLK_Q4K) : QG_DEC_SBLK_Q8);
 }
 // CTAs of 320 threads resident per SM (registers and shared memory are
 // budgeted for it)
@@ -131,7 +135,7 @@ static_assert(QG_DEC_DP4A_MAX_Q8 <= kDp4aMaxM && QG_DEC_DP4A_MAX_Q4K <= kDp4aMax
 // for the chain), and for W4A8 -asum per block and token.
 template <int TT, bool kQ4K, bool kDp4a, int kPairs = 2>
 struct DecodeSmem {
-  static constexpr int kSBlk = sblk<kQ4K, kDp4a>();
+  static constexpr int kSBlk = sblk<TT, kQ4K, kDp4a>();
   // bytes per activation row in a stage: 32 per block + 32 of padding, so the
   // eight rows one 8-byte load touches fall in distinct banks
   static constexpr int kARow = kSBlk * 32 + 32;
@@ -339,8 +343,9 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
   constexpr int kBlkPerWarp = kSBlk / kCompWarps;
-  // (W4A8: each half-warp decodes the scales of one of the warp's blocks)
-  static_assert(!kQ4K || kBlkPerWarp == 2, "two blocks per compute warp and stage");
+  // (W4A8: each half-warp decodes the scales of every other one of the
+  // warp's blocks)
+  static_assert(!kQ4K || kBlkPerWarp % 2 == 0, "an even number of blocks per compute warp");
   extern __shared__ __align__(128) uint8_t smem[];
   const int NW = a.nw;
   const int mrows = min(a.M, TT * 8);
@@ -511,12 +516,17 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
         }
       }
       if (kQ4K) {
-        // lane (r, hh): row r's d*sc and dmin*m of block 2cw + hh
-        const int r = lane & 15, j = cw * kBlkPerWarp + (lane >> 4);
-        if (j < nb) {
-          const uint4 H = *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
-          float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
-          scw[j * 16 + r] = q4k_scales(H, j & 7);
+        // lane (r, hh): row r's d*sc and dmin*m of the warp's blocks hh, hh + 2, ...
+        const int r = lane & 15;
+#pragma unroll
+        for (int v = 0; v < kBlkPerWarp / 2; ++v) {
+          const int j = cw * kBlkPerWarp + 2 * v + (lane >> 4);
+          if (j < nb) {
+            const uint4 H =
+                *reinterpret_cast<const uint4*>(base + L::kWBytes + (j >> 3) * 256 + r * 16);
+            float2* scw = reinterpret_cast<float2*>(stash + L::kXBytes / 4);
+            scw[j * 16 + r] = q4k_scales(H, j & 7);
+          }
         }
       }
       if constexpr (L::kEarly) {
