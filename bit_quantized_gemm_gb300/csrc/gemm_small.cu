@@ -115,7 +115,7 @@ static_assert(QG_DEC_DP4A_MAX_Q8 <= kDp4aMaxM && QG_DEC_DP4A_MAX_Q4K <= kDp4aMax
 #define QG_DEC_BUDGET_TT2_KB 70
 #endif
 #ifndef QG_DEC_EARLY
-#define QG_DEC_EARLY 1  // int8-MMA kernel: the compute warps release each stage
+#define QG_DEC_EARLY 1  // the compute warps, not the chain warp, release each stage
 #endif
 #ifndef QG_DEC_CHAIN_UNROLL
 #define QG_DEC_CHAIN_UNROLL 1  // chain warp: a full stage's block quads unrolled
@@ -145,11 +145,13 @@ struct DecodeSmem {
       kDp4a ? kSBlk * kPairs * 16 * (kQ4K ? 16 : 8) : kSBlk * TT * 32 * 16;
   static constexpr int kScBytes = (kQ4K && !kDp4a) ? kSBlk * 16 * 8 : 0;
   static constexpr int kAsBytes = (kQ4K && kDp4a) ? kSBlk * kDp4aMaxM * 4 : 0;
-  // MMA tiles: the chain warp's inputs that arrive with the stage (Q8_0
-  // scales; Q4_K activation block sums of up to TT*8 rows), copied into the
+  // The chain warp's inputs that arrive with the stage (Q8_0 scales; MMA
+  // tiles' Q4_K activation block sums of up to TT*8 rows), copied into the
   // stash by the compute warps so that they, not the chain, release the stage
-  static constexpr bool kEarly = !kDp4a && QG_DEC_EARLY != 0;
-  static constexpr int kCdBytes = kEarly ? (kQ4K ? TT * 8 * kSBlk * 4 : kSBytes) : 0;
+  static constexpr bool kEarly = QG_DEC_EARLY != 0;
+  // (the integer kernel's Q4_K chain reads its stash alone)
+  static constexpr int kCdBytes =
+      kEarly ? (kQ4K ? (kDp4a ? 0 : TT * 8 * kSBlk * 4) : kSBytes) : 0;
   static constexpr int kCdOff = kXBytes + kScBytes + kAsBytes;
   static constexpr int kSlotBytes = kXBytes + kScBytes + kAsBytes + kCdBytes;
   static constexpr int kMaxNw = 8;
@@ -709,7 +711,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], L::kEarly ? kCompWarps : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&xfull[i], kCompWarps);
@@ -811,8 +813,18 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
             }
           }
         }
+        if constexpr (L::kEarly && !kQ4K) {
+          // the stage's scales into the stash for the chain, 16 bytes a lane
+          const uint8_t* src = base + L::kWBytes;
+          uint8_t* dst = reinterpret_cast<uint8_t*>(xsum) + L::kCdOff;
+          for (int i = cw * 32 + lane; i < L::kSBytes / 16; i += kCompWarps * 32)
+            *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(src + 16 * i);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xfull[xs]);
+        if (lane == 0) {
+          mbar_arrive(&xfull[xs]);
+          if (L::kEarly) mbar_arrive(&empty[st]);  // this warp's reads of the stage are done
+        }
         if (++st == NW) { st = 0; ph ^= 1; }
         if (++xs == 2) { xs = 0; xph ^= 1; }
       }
@@ -837,6 +849,8 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       const uint8_t* base = smem + st * SBY;
       const float* xsum = stash_base + xs * (L::kSlotBytes / 4);
       const float* asn = xsum + L::kXBytes / 4;
+      const uint8_t* sbase =
+          L::kEarly ? reinterpret_cast<const uint8_t*>(xsum) + L::kCdOff : base + L::kWBytes;
       // four blocks at a time: their operands are loaded before their FMAs
       auto quad = [&](const int j0) {
         if (!kQ4K) {
@@ -845,7 +859,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
           for (int u = 0; u < 4; ++u)
             x[u] = *reinterpret_cast<const float2*>(xsum + (((j0 + u) * kPairs + tpc) * 16 + r) * 2);
           // fp16 scales of rows r&7 and (r&7)+8 for blocks j0..j0+3
-          const uint2 dq = *reinterpret_cast<const uint2*>(base + L::kWBytes + (j0 >> 2) * 128 +
+          const uint2 dq = *reinterpret_cast<const uint2*>(sbase + (j0 >> 2) * 128 +
                                                            (r & 7) * 16 + (r >> 3) * 8);
           const float2 d01 = __half22float2(*reinterpret_cast<const __half2*>(&dq.x));
           const float2 d23 = __half22float2(*reinterpret_cast<const __half2*>(&dq.y));
@@ -879,7 +893,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&xempty[xs]);
-        mbar_arrive(&empty[st]);
+        if (!L::kEarly) mbar_arrive(&empty[st]);
       }
       if (++st == NW) { st = 0; ph ^= 1; }
       if (++xs == 2) { xs = 0; xph ^= 1; }
