@@ -14,7 +14,7 @@
 //     sums) -- into a shared-memory ring with 1-D bulk copies
 //     (cp.async.bulk + mbarrier transaction counts);
 //   * warps 1..8 compute the stage's exact block sums into a shared stash:
-//     - up to 3 (W8A8) or 4 (W4A8) rows, decode_dp4a_kernel: one lane per
+//     - up to 4 rows, decode_dp4a_kernel: one lane per
 //       weight row and block, eight dp4a per token on the row's 32 int8
 //       values (W4A8: its 32 nibbles masked into low and high bytes), no
 //       widening; the W4A8 lane also decodes its row's d*sc and dmin*m;
@@ -25,10 +25,13 @@
 //       nothing is widened (the fp16-MMA variant, which widens weights and
 //       activations in registers, is kept behind a build switch); every sum
 //       is below 2^20, exact in int32 and in fp32;
+//     and once a warp has read the stage (and copied into the stash what the
+//     chain needs from it: Q8_0 scales, MMA tiles' Q4_K block sums) it hands
+//     its part of the stage back to the producer;
 //   * warp 9 applies acc = fmaf(isum, d, acc) (Q4_K: then
 //     fmaf(-asum, dmin*m, acc)) over the stage's blocks in ascending order
 //     with packed f32x2 FMAs -- the same chain as the prefill kernel, so both
-//     paths give identical bits -- and hands the stage back to the producer.
+//     paths give identical bits -- reading the stash alone.
 // K-parallel compute with a sequential fp32 chain keeps ten warps busy per
 // 16-row group, which small N (few groups) needs to reach HBM rate.
 // As the GEMM of the layer call the kernel is a programmatic dependent of the
@@ -97,12 +100,13 @@ __host__ __device__ constexpr int dec_hbatch() { return kQ4K ? QG_DEC_HB_Q4K : 4
 // Rows up to which the integer dot-product kernel runs (one lane per weight
 // row; each token's 32 activation bytes of a block are loaded by every row's
 // lane) rather than MMA tiles (activations loaded once per 8-token tile); at
-// most kDp4aMaxM. Measured on GB300: W8A8 4 rows tie at 5120 -> 17408 and
-// favour the int8 MMA tiles at 17408 -> 5120 (24.9 vs 26.9 us); W4A8 4 rows
-// favour dp4a (23.0 vs 25.6 us).
+// most kDp4aMaxM. Measured on GB300 (both kernels releasing stages from
+// their compute warps): 4 rows tie at 5120 -> 17408 for both formats and
+// favour the integer kernel at 17408 -> 5120 for W8A8 (24.9 vs 25.7 us);
+// W4A8 ties there too (28.9 us).
 constexpr int kDp4aMaxM = 4;
 #ifndef QG_DEC_DP4A_MAX_Q8
-#define QG_DEC_DP4A_MAX_Q8 3
+#define QG_DEC_DP4A_MAX_Q8 4
 #endif
 #ifndef QG_DEC_DP4A_MAX_Q4K
 #define QG_DEC_DP4A_MAX_Q4K 4
