@@ -707,6 +707,23 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// rows of `row_bytes` bytes (a multiple of 16), read as 8-byte words:
+// box = box_words x box_rows, no swizzle, so the box lands row after row at a
+// pitch of 8 * box_words bytes; words past a row's end read as zero (used by
+// gemm_small.cu for the decode kernels' activation rows and block sums)
+bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                    uint32_t box_words, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15) || row_bytes % 16) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {box_words, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 output [M][ldo] as the TMA store's destination, box = 128 weight rows
 // x `rows` tokens; false when the base or the row pitch is not 16-byte
 // aligned (the kernel then stores element by element)

@@ -37,9 +37,17 @@
 // As the GEMM of the layer call the kernel is a programmatic dependent of the
 // quantize kernel: it starts while the rows are quantized, requests its first
 // weight stages, and copies activations only once the quantize grid is done.
+#include <cuda.h>
+
+#include <cstring>
+
 #include "qg_common.cuh"
 
 namespace qg {
+
+// from gemm_large.cu: rows of row_bytes bytes as 8-byte words, box_words x box_rows
+bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                    uint32_t box_words, uint32_t box_rows);
 
 constexpr int kCompWarps = 8;      // compute warps per CTA
 
@@ -159,11 +167,16 @@ struct DecodeSmem {
   static constexpr int kCdOff = kXBytes + kScBytes + kAsBytes;
   static constexpr int kSlotBytes = kXBytes + kScBytes + kAsBytes + kCdBytes;
   static constexpr int kMaxNw = 8;
+  // the activation rows and the block sums are TMA destinations: each starts
+  // on a 128-byte boundary of the stage (stages are 128-byte multiples)
+  static_assert((kWBytes + kSBytes) % 128 == 0, "activation rows 128-byte aligned");
   static __host__ __device__ int stage_bytes(int mrows) {
-    return (int)align_up(kWBytes + kSBytes + mrows * kARow + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
+    return (int)align_up(bsum_off(mrows) + (kQ4K ? mrows * kSBlk * 4 : 0), 128);
   }
   static __host__ __device__ int act_off() { return kWBytes + kSBytes; }
-  static __host__ __device__ int bsum_off(int mrows) { return kWBytes + kSBytes + mrows * kARow; }
+  static __host__ __device__ int bsum_off(int mrows) {
+    return (int)align_up(kWBytes + kSBytes + mrows * kARow, 128);
+  }
   // weight stages that fit in `budget` bytes next to the stash and barriers
   static int num_stages(int mrows, int budget) {
     const int fixed = 2 * kSlotBytes + 2 * (kMaxNw + 2) * 8;
@@ -257,7 +270,8 @@ struct DecodeArgs {
 // their block sums), and at the end waits until the chain warp has released
 // every stage.
 template <class L, bool kQ4K>
-__device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* smem, int SBY,
+__device__ __forceinline__ void decode_produce(const DecodeArgs& a, const CUtensorMap* tmX,
+                                               const CUtensorMap* tmS, uint8_t* smem, int SBY,
                                                int mrows, uint64_t* full, uint64_t* empty,
                                                int lane) {
   constexpr int kSBlk = L::kSBlk;
@@ -267,17 +281,15 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
   const int B4 = (B + 3) & ~3;
   const int J = B / 8;
   const int nstages = (B + kSBlk - 1) / kSBlk;
-  // The activation rows (and W4A8 block sums) of stage r into ring slot `slot`.
+  // The activation rows (and W4A8 block sums) of stage r into ring slot
+  // `slot`: one 2-D copy each, all rows at once, landing at the stage's row
+  // pitch (the box's rows carry the pitch's padding, read from the next
+  // stage or as zeros past K, never used)
   auto copy_acts = [&](int r, int slot) {
-    const int blk0 = r * kSBlk;
-    const int nb = min(kSBlk, B - blk0);
-    uint8_t* base = smem + slot * SBY;
-    for (int m = lane; m < mrows; m += 32) {
-      bulk_copy_g2s(base + L::act_off() + m * kARow,
-                a.qa + (int64_t)m * a.K + (int64_t)blk0 * kBlk, nb * 32, &full[slot]);
-      if (kQ4K)
-        bulk_copy_g2s(base + L::bsum_off(mrows) + m * (kSBlk * 4), a.bsum + (int64_t)m * B + blk0,
-                  nb * 4, &full[slot]);
+    if (lane == 0) {
+      uint8_t* base = smem + slot * SBY;
+      tma_load_2d(base + L::act_off(), tmX, &full[slot], r * kSBlk * (kBlk / 8), 0);
+      if (kQ4K) tma_load_2d(base + L::bsum_off(mrows), tmS, &full[slot], r * kSBlk / 2, 0);
     }
   };
   // Launched as a programmatic dependent, the weights and scales of the
@@ -302,8 +314,8 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
       const int nb = min(kSBlk, B - blk0);
       uint8_t* base = smem + st * SBY;
       uint32_t bytes = !kQ4K ? nb * 512 + ((nb + 3) / 4) * 128 : nb * 256 + (nb / 8) * 256;
-      bytes += mrows * nb * 32;
-      if (kQ4K) bytes += mrows * nb * 4;
+      bytes += mrows * kARow;                   // whole boxes (zero-filled past K)
+      if (kQ4K) bytes += mrows * kSBlk * 4;
       if (lane == 0) {
         ok = mbar_wait(&empty[st], ph ^ 1, a.err);
         if (ok) {
@@ -344,7 +356,8 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, uint8_t* sme
 // int8 m16n8k32 on the stored bytes, or (build switch) fp16 m16n8k16 on
 // values widened in registers.
 template <int TT, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+                       const DecodeArgs a) {
   using L = DecodeSmem<TT, kQ4K, false>;
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
@@ -381,7 +394,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   __syncthreads();
 
   if (warp == 0) {
-    decode_produce<L, kQ4K>(a, smem, SBY, mrows, full, empty, lane);
+    decode_produce<L, kQ4K>(a, &tmX, &tmS, smem, SBY, mrows, full, empty, lane);
     return;
   }
 
@@ -689,7 +702,8 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
 // fmaf(-asum, dmin*m, acc)): the same operations in the same order as the
 // MMA kernel and the prefill kernel.
 template <bool kQ4K, int kM, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_dp4a_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_dp4a_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+                       const DecodeArgs a) {
   constexpr int kPairs = (kM + 1) / 2;  // token pairs
   using L = DecodeSmem<1, kQ4K, true, kPairs>;
   constexpr int kSBlk = L::kSBlk;
@@ -726,7 +740,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   __syncthreads();
 
   if (warp == 0) {
-    decode_produce<L, kQ4K>(a, smem, SBY, M, full, empty, lane);
+    decode_produce<L, kQ4K>(a, &tmX, &tmS, smem, SBY, M, full, empty, lane);
     return;
   }
 
@@ -936,7 +950,15 @@ static cudaError_t launch_decode(Kern kern, std::atomic<uint64_t>& attr_set, con
   // with pdl, the CTAs may start while the previous kernel on the stream
   // (the quantize kernel) runs, streaming their first weight stages meanwhile
   const dim3 grid((unsigned)(a.G < slots ? a.G : slots)), block(32 * (kCompWarps + 2));
-  return launch_kernel(kern, grid, block, (size_t)L::total(mrows, b.nw), st, pdl, b);
+  // the activation rows and (W4A8) block sums of a stage, one box each
+  CUtensorMap tx, ts;
+  memset(&ts, 0, sizeof(ts));
+  if (!make_tmap_rows(&tx, a.qa, a.M, a.K, L::kARow / 8, (uint32_t)mrows))
+    return cudaErrorNotSupported;
+  if (kQ4K && !make_tmap_rows(&ts, a.bsum, a.M, (int64_t)(a.K / kBlk) * 4, L::kSBlk / 2,
+                              (uint32_t)mrows))
+    return cudaErrorNotSupported;
+  return launch_kernel(kern, grid, block, (size_t)L::total(mrows, b.nw), st, pdl, tx, ts, b);
 }
 
 template <int TT, bool kQ4K, bool kDebug>
