@@ -9,10 +9,11 @@
 // (1.0625 B/weight for Q8_0, 0.5625 B/weight for Q4_K). A CTA owns one group
 // of 16 weight rows and all of K; K is cut into stages of 16 or 32 blocks.
 // Two kernels share that frame:
-//   * warp 0 (one thread) streams each stage -- the group's contiguous
-//     weights and scales, the activation rows (and for W4A8 their block
-//     sums) -- into a shared-memory ring with 1-D bulk copies
-//     (cp.async.bulk + mbarrier transaction counts);
+//   * warp 0 (one thread) streams each stage into a shared-memory ring -- the
+//     group's contiguous weights and scales with 1-D bulk copies
+//     (cp.async.bulk), the stage's slice of every activation row (and for
+//     W4A8 of every block-sum row) as one 2-D TMA box -- with mbarrier
+//     transaction counts;
 //   * warps 1..8 compute the stage's exact block sums into a shared stash:
 //     - up to 4 rows, decode_dp4a_kernel: one lane per
 //       weight row and block, eight dp4a per token on the row's 32 int8
@@ -267,8 +268,8 @@ struct DecodeArgs {
 
 // Warp 0 of a decode CTA: streams stage after stage of the CTA's groups into
 // the ring (weights and scales, then the activation rows and, for W4A8,
-// their block sums), and at the end waits until the chain warp has released
-// every stage.
+// their block sums), and at the end waits until every stage has been handed
+// back.
 template <class L, bool kQ4K>
 __device__ __forceinline__ void decode_produce(const DecodeArgs& a, const CUtensorMap* tmX,
                                                const CUtensorMap* tmS, uint8_t* smem, int SBY,
@@ -356,8 +357,9 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, const CUtens
 // int8 m16n8k32 on the stored bytes, or (build switch) fp16 m16n8k16 on
 // values widened in registers.
 template <int TT, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
-                       const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmS, const DecodeArgs a) {
   using L = DecodeSmem<TT, kQ4K, false>;
   constexpr int kSBlk = L::kSBlk;
   constexpr int kARow = L::kARow;
@@ -702,8 +704,9 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
 // fmaf(-asum, dmin*m, acc)): the same operations in the same order as the
 // MMA kernel and the prefill kernel.
 template <bool kQ4K, int kM, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decode_dp4a_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
-                       const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
+    decode_dp4a_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmS, const DecodeArgs a) {
   constexpr int kPairs = (kM + 1) / 2;  // token pairs
   using L = DecodeSmem<1, kQ4K, true, kPairs>;
   constexpr int kSBlk = L::kSBlk;
@@ -718,7 +721,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>()) decod
   const int SBY = L::stage_bytes(M);
   float* stash_base = reinterpret_cast<float*>(smem + NW * SBY);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NW * SBY + 2 * L::kSlotBytes);
-  uint64_t* empty = full + NW;    // weight stage consumed by the chain warp
+  uint64_t* empty = full + NW;    // weight stage consumed (compute warps, or the chain warp)
   uint64_t* xfull = empty + NW;   // stash slot written (count: compute warps)
   uint64_t* xempty = xfull + 2;   // stash slot read by the chain warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
