@@ -132,6 +132,28 @@ def test_w4a8_q4k():
             check_sampled(out, oq, os_, sblocks, "w4a8", n_rows=128, n_cols=128, seed=M)
 
 
+@pytest.mark.parametrize("M,N,tb", [(24, 5120, 32), (64, 2560, 64)])
+def test_skinny_long_k_repeated(M, N, tb):
+    # 16-row tiles over K = 17408 (272 ring stages per CTA) with many CTAs per
+    # SM, three launches in a row: every output of every launch against the
+    # oracle (a race in the ring would show as a whole warp's tokens wrong in
+    # some CTAs, differently from launch to launch)
+    from bit_quantized_gemm_gb300 import _lib
+    K = 17408
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert _lib.prefill_plan(M, N, sms) == (0, "16-row", tb)
+    blocks = synth.config_weights("decode_w8a8", N, K, seed_offset=tb)
+    packed = qg.pack_q8_0(to_dev(blocks), N, K)
+    (q, s, _, h), oq, os_ = quant_full("decode_w8a8", M, K, seed_offset=tb)
+    _, ob = oracle.gemm_w8a8_q8_0(oq, os_, blocks)
+    for _ in range(3):
+        out = qg.gemm_w8a8_q8_0(q, h, s, packed, N)
+        torch.cuda.synchronize()
+        qg.check_device_error()
+        assert np.array_equal(bits_of(out), ob)
+
+
 def test_w4a8_q4k_narrow_down_projection():
     # 17408 -> 5120 at 32 and 64 tokens: 40 weight-row tiles, so these run as
     # 32-token tiles, each walking all 544 sub-blocks; every output compared
