@@ -44,6 +44,7 @@
 // Every output element still gets its whole K chain from one thread, so the
 // plan changes no bit.
 #include <cuda.h>
+#include <algorithm>
 #include <cstring>
 
 #include "qg_common.cuh"
@@ -783,12 +784,17 @@ static double tc_step_cycles(int bm) {
     default: return 420.0;  // 32
   }
 }
-static double skinny_step_cycles(int tb) { return tb == 32 ? 135.0 : (tb == 64 ? 260.0 : 300.0); }
-// Token-tile width of the 16-row tiles (two CTAs per SM): the one of the
-// smallest estimated time, waves x step cost.
+static double skinny_step_cycles(int tb, int64_t per_sm) {
+  return tb == 32 ? 135.0 : (tb == 64 ? (per_sm > 2 ? 332.0 : 260.0) : 300.0);
+}
+// Token-tile width of the 16-row tiles (64-token tiles three CTAs per SM,
+// the others two): the one of the smallest estimated time, waves x step cost
+// (64-token steps cost more when three CTAs share an SM).
 static double skinny_time(int64_t M, int64_t rows, int sms, int tb) {
   const int64_t ctas = ceil_div(rows, (int64_t)16) * ceil_div(M, (int64_t)tb);
-  return (double)ceil_div(ctas, 2 * (int64_t)sms) * skinny_step_cycles(tb);
+  const int64_t slots = (tb == 64 ? 3 : 2) * (int64_t)sms;
+  const int64_t per_sm = std::min<int64_t>(ceil_div(ctas, (int64_t)sms), tb == 64 ? 3 : 2);
+  return (double)ceil_div(ctas, slots) * skinny_step_cycles(tb, per_sm);
 }
 static int skinny_tb(int64_t M, int64_t rows, int sms) {
   int best = 32;

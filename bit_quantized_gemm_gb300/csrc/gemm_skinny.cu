@@ -49,7 +49,11 @@ struct SkinnyCfg {
   static constexpr uint32_t kABytes = kSkRows * kSkBK * 2;  // 2 KB
   static constexpr uint32_t kBBytes = TB * kSkBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // multiple of 1024 (swizzle atoms)
-  static constexpr int kStages = (96 * 1024) / (int)kStageBytes > 8 ? 8 : (96 * 1024) / (int)kStageBytes;
+  // resident CTAs per SM: three of 64 tokens (a shallower ring: 7 stages),
+  // else two; 17408 -> 5120 at 33-64 tokens (320 CTAs) then runs as one wave
+  static constexpr int kCtas = TB == 64 ? 3 : 2;
+  static constexpr int kBudget = kCtas == 3 ? 70 * 1024 : 96 * 1024;
+  static constexpr int kStages = kBudget / (int)kStageBytes > 8 ? 8 : kBudget / (int)kStageBytes;
   static constexpr size_t kSmem = kStages * kStageBytes + 2 * kStages * 8 + 1024;
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "1024-byte aligned tiles");
   static_assert(kStages >= 2, "ring depth");
@@ -79,7 +83,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int k) {
 }
 
 template <int TB>
-__global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, 2)
+__global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const SkinnyArgs args) {
   using C = SkinnyCfg<TB>;
@@ -121,6 +125,12 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, 2)
       for (int s = 0; s < NS && ok; ++s) {
         ok = mbar_wait(&empty[st], ph ^ 1, args.err);
         if (!ok) break;
+        // the compute warps read the slot through the generic proxy
+        // (ldmatrix); the TMA loads below rewrite it through the async proxy.
+        // Without this fence such a load could land before those reads
+        // (measured: wrong sums for a warp in a few CTAs when three CTAs
+        // shared an SM)
+        fence_proxy_async_smem();
         uint8_t* a_s = sm + st * C::kStageBytes;
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);  // whole boxes (zero-filled edges)
         tma_load_2d(a_s, &tmA, &full[st], s * kSkBK, n0);

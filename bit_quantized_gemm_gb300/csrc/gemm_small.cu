@@ -320,6 +320,10 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, const CUtens
       if (lane == 0) {
         ok = mbar_wait(&empty[st], ph ^ 1, a.err);
         if (ok) {
+          // the consumers read the slot through the generic proxy; the copies
+          // below rewrite it through the async proxy, ordered after those
+          // reads (which the wait made visible) only by this fence
+          fence_proxy_async_smem();
           mbar_arrive_expect_tx(&full[st], bytes);
           if (!kQ4K) {
             bulk_copy_g2s(base, a.wstream + (g * B + blk0) * 512, nb * 512, &full[st]);

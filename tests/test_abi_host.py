@@ -215,6 +215,7 @@ def test_prefill_wave_plan_on_152_sms(L):
     assert plan(8192, 17408, 152) == (17408, None, 0)      # 27B gate/up
     assert plan(32, 5120, 152) == (0, "16-row", 32)        # narrow prefill: 16-row tiles
     assert plan(64, 17408, 152) == (0, "tensor", 64)       # 64-token tensor-memory tiles
+    assert plan(64, 5120, 152) == (0, "16-row", 64)        # 40 row tiles: 16-row tiles, one wave
 
 
 def test_prefill_wave_plan_invariants(L):

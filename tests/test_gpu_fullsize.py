@@ -132,7 +132,7 @@ def test_w4a8_q4k():
             check_sampled(out, oq, os_, sblocks, "w4a8", n_rows=128, n_cols=128, seed=M)
 
 
-@pytest.mark.parametrize("M,N,tb", [(24, 5120, 32), (64, 2560, 64)])
+@pytest.mark.parametrize("M,N,tb", [(24, 5120, 32), (64, 2560, 64), (64, 5120, 64), (40, 5120, 64)])
 def test_skinny_long_k_repeated(M, N, tb):
     # 16-row tiles over K = 17408 (272 ring stages per CTA) with many CTAs per
     # SM, three launches in a row: every output of every launch against the
