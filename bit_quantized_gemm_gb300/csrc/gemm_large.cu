@@ -73,13 +73,16 @@ namespace qg {
 #define QG_FORCE_BM 0  // tuning: nonzero runs every W8A8 GEMM as one launch of this width
 #endif
 #ifndef QG_BM_W4A8
-#define QG_BM_W4A8 128
+#define QG_BM_W4A8 0  // W4A8 token-tile width above 64 tokens (0: chosen per shape)
 #endif
 #ifndef QG_EPI_BATCH
 #define QG_EPI_BATCH 0  // loads per wait; 0: all chunks of a block up to 64 columns, else 1
 #endif
 #ifndef QG_CHUNK
 #define QG_CHUNK 16  // tensor-memory columns per load (16 or 32)
+#endif
+#ifndef QG_W4_SCALAR_BM
+#define QG_W4_SCALAR_BM 256  // W4A8 tiles at least this wide load scalar scales one block ahead
 #endif
 #ifndef QG_W4_BM32
 #define QG_W4_BM32 1  // W4A8 GEMMs of at most 64 tokens may run 32-token tiles
@@ -97,11 +100,15 @@ __host__ __device__ constexpr int threads_for(int bm) { return 32 * (kFirstEpiWa
 constexpr uint32_t kStageABytes = kBN * kBK * 2;  // 16 KB
 constexpr int kCtasPerSm = QG_CTAS_PER_SM;  // CTAs sharing an SM (and its tensor memory)
 constexpr uint32_t kTmemCols = 512 / kCtasPerSm;
-constexpr int kAsumRing = 16;  // blocks of activation sums in flight (W4A8)
+// blocks of activation sums in flight (W4A8); 256-token tiles keep 8, which
+// leaves room for a third TMA stage
+__host__ __device__ constexpr int asum_ring(int bm) { return bm >= 256 ? 8 : 16; }
 
-// Tile width BM = tokens per tile (MMA N, tensor-memory columns). 256 suits
-// W8A8 (one FMA per element per block); W4A8's two FMAs per element need
-// the register room of BM = 128.
+// Tile width BM = tokens per tile (MMA N, tensor-memory columns). W8A8 runs
+// 256 (one FMA per element per block) with narrower tiles for leftovers;
+// W4A8 (two FMAs per element per block) 128 or 256, its 256-token tiles with
+// scalar scale loads and four-block activation-sum rounds to stay in the
+// registers of 11 warps.
 template <int BM>
 struct LargeCfg {
   static_assert(BM % 16 == 0 && BM >= 32 && BM <= 256 && kTmemCols % BM == 0, "tile width");
@@ -124,7 +131,7 @@ __host__ __device__ constexpr int stages_for() {
   constexpr int kCols = LargeCfg<BM>::kColsPerThread;
   constexpr int kEpiWarps = LargeCfg<BM>::kEpiWarps;
   constexpr int kFixed = (QG_TMA_OUT ? (kEpiWarps / 4) * kCols * kBN * 2 : 16) +
-                         (kQ4K ? kAsumRing : 1) * BM * 4 +
+                         (kQ4K ? asum_ring(BM) : 1) * BM * 4 +
                          kEpiWarps * kCols * 4 + 2048;  // + barriers and alignment slack
   constexpr int kPer = (int)kStageABytes + BM * kBK * 2;
   constexpr int n0 = (226 * 1024 - kFixed) / kPer;
@@ -152,11 +159,11 @@ struct LargeSmem {
   // warps (a column slice of the tile), kCols token rows x 128 weight rows
   // (row-major, the store's box)
   uint16_t ostage[QG_TMA_OUT ? kEpiWarps / 4 : 1][QG_TMA_OUT ? kCols * kBN : 8];
-  float asum[kQ4K ? kAsumRing : 1][BM];
+  float asum[kQ4K ? asum_ring(BM) : 1][BM];
   float sa_stage[kEpiWarps][kCols];  // per epilogue warp: its tile's activation scales
   uint64_t full[kStages], empty[kStages];
   uint64_t tfull[LargeCfg<BM>::kTBufs], tempty[LargeCfg<BM>::kTBufs];
-  uint64_t afull[kAsumRing], aempty[kAsumRing];
+  uint64_t afull[asum_ring(BM)], aempty[asum_ring(BM)];
   uint64_t mdrain[2];    // per MMA issuer: completion of its MMAs after a wait gave up
   uint32_t tmem_base;
   uint32_t tmem_busy;    // nonzero: an issuer's MMAs did not complete; tensor memory stays allocated
@@ -210,6 +217,7 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
   constexpr int kTBufs = C::kTBufs;
   constexpr uint32_t kStageBBytes = C::kStageBBytes;
   constexpr int kColsPerThread = C::kColsPerThread;
+  constexpr int kAsumRing = asum_ring(BM);
   extern __shared__ uint8_t smem_raw[];
   LargeSmem<kQ4K, BM>& S = *reinterpret_cast<LargeSmem<kQ4K, BM>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -259,19 +267,18 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
     uint32_t aphase = 0;
     bool ok = true;
     uint32_t loaded = 0, load_par = 0;  // per stage: a load was issued; parity of the last one
-    // W4A8: activation block sums of eight blocks for this lane's tokens
-    int4 bs_cur[kQ4K ? kBM / 32 : 1][2], bs_nxt[kQ4K ? kBM / 32 : 1][2];
-    auto load_bs8 = [&](int mt, int blk8, int4 (&dst)[kQ4K ? kBM / 32 : 1][2]) {
+    // W4A8: activation block sums of kBsR blocks (a quad per 16-byte load)
+    // for this lane's tokens; 256-token tiles take four blocks per round to
+    // keep the two rounds in registers
+    constexpr int kBsQ = kBM >= 256 ? 1 : 2, kBsR = 4 * kBsQ;
+    int4 bs_cur[kQ4K ? kBM / 32 : 1][kBsQ], bs_nxt[kQ4K ? kBM / 32 : 1][kBsQ];
+    auto load_bs = [&](int mt, int blk0, int4 (&dst)[kQ4K ? kBM / 32 : 1][kBsQ]) {
 #pragma unroll
       for (int i = 0; i < kBM / 32; ++i) {
         const int m = mt * kBM + i * 32 + lane;
-        if (m < M) {
-          const int4* p = reinterpret_cast<const int4*>(args.bsum + (int64_t)m * NB + blk8);
-          dst[i][0] = __ldg(p);
-          dst[i][1] = __ldg(p + 1);
-        } else {
-          dst[i][0] = dst[i][1] = make_int4(0, 0, 0, 0);
-        }
+        const int4* p = reinterpret_cast<const int4*>(args.bsum + (int64_t)(m < M ? m : 0) * NB + blk0);
+#pragma unroll
+        for (int j = 0; j < kBsQ; ++j) dst[i][j] = m < M ? __ldg(p + j) : make_int4(0, 0, 0, 0);
       }
     };
     // As a programmatic dependent of the quantize kernel (W8A8): the weight
@@ -308,24 +315,26 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           for (int j = 0; j < 2; ++j) {
             const int blk = 2 * s + j;
             if (blk >= NB) break;
-            // the tile's activation block sums come eight blocks per load
-            // round (two 16-byte loads per token: NB and the block index are
-            // multiples of 8), the next eight requested while these are used,
-            // so each round's latency is hidden behind eight blocks
-            if ((blk & 7) == 0) {
-              if (blk == 0) load_bs8(mt, 0, bs_cur);
+            // the tile's activation block sums come kBsR blocks per load
+            // round (NB and the block index are multiples of 8), the next
+            // round requested while this one is used, so each round's
+            // latency is hidden behind its blocks
+            if (blk % kBsR == 0) {
+              if (blk == 0) load_bs(mt, 0, bs_cur);
               else {
 #pragma unroll
-                for (int i = 0; i < kBM / 32; ++i) { bs_cur[i][0] = bs_nxt[i][0]; bs_cur[i][1] = bs_nxt[i][1]; }
+                for (int i = 0; i < kBM / 32; ++i)
+#pragma unroll
+                  for (int j = 0; j < kBsQ; ++j) bs_cur[i][j] = bs_nxt[i][j];
               }
-              if (blk + 8 < NB) load_bs8(mt, blk + 8, bs_nxt);
+              if (blk + kBsR < NB) load_bs(mt, blk + kBsR, bs_nxt);
             }
             ok = mbar_wait(&S.aempty[aslot], aphase ^ 1, args.err);
             if (!ok) break;
-            const int q = blk & 7;
+            const int q = blk % kBsR;
 #pragma unroll
             for (int i = 0; i < kBM / 32; ++i) {
-              const int4 w = (q < 4) ? bs_cur[i][0] : bs_cur[i][1];
+              const int4 w = bs_cur[i][q >> 2];
               const int v = (q & 3) == 0 ? w.x : (q & 3) == 1 ? w.y : (q & 3) == 2 ? w.z : w.w;
               S.asum[aslot][i * 32 + lane] = (float)v;  // exact: |v| <= 4064
             }
@@ -458,10 +467,12 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
       // ahead (quads of four blocks one to three quads ahead, or scalars two
       // blocks ahead, measured 3-55 % slower: the epilogue loop is tight on
       // registers). W4A8: four blocks per 16-byte load of d*sc and of dmin*m
-      // (rows are 16-byte aligned: whole quads), one quad ahead of its use.
-      constexpr int kQA = kQ4K ? 1 : 0;
+      // (rows are 16-byte aligned: whole quads), one quad ahead of its use;
+      // its 256-token tiles load both as scalars one block ahead (the quads
+      // spill there).
+      constexpr int kQA = (kQ4K && BM < QG_W4_SCALAR_BM) ? 1 : 0;
       constexpr int kQR = kQA > 0 ? kQA + 1 : 1;
-      float d_next = 0.0f;
+      float d_next = 0.0f, m_next = 0.0f;
       float4 dq[kQR], mq[kQR];
 #pragma unroll
       for (int i = 0; i < kQR; ++i) {
@@ -471,7 +482,10 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           if (kQ4K) mq[i] = ldg_f32x4_pinned(mrow + 4 * i);
         }
       }
-      if (kQA == 0 && nvalid) d_next = ldg_f32_pinned(drow);
+      if (kQA == 0 && nvalid) {
+        d_next = ldg_f32_pinned(drow);
+        if (kQ4K) m_next = ldg_f32_pinned(mrow);
+      }
       for (int blk = 0; blk < NB && ok; ++blk) {
         float dw, ndm = 0.0f;
         if (kQA > 0) {
@@ -492,7 +506,11 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           if (kQ4K) ndm = -(q == 0 ? mq[0].x : q == 1 ? mq[0].y : q == 2 ? mq[0].z : mq[0].w);
         } else {
           dw = d_next;
-          if (blk + 1 < NB && nvalid) d_next = ldg_f32_pinned(drow + blk + 1);
+          if (kQ4K) ndm = -m_next;
+          if (blk + 1 < NB && nvalid) {
+            d_next = ldg_f32_pinned(drow + blk + 1);
+            if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
+          }
         }
         const int tb = kStageMode ? (2 * (ti * NS + (blk >> 1)) + (blk & 1)) % kTBufs
                                   : blk % kTBufs;
@@ -936,6 +954,23 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   }
 }
 
+// Token-tile width of the W4A8 prefill kernel for an M x N GEMM on `sms` SMs.
+// A GEMM of at most 64 tokens fills half of a 128-token tile: 64-token tiles,
+// or 32-token tiles when there are too few weight-row tiles to fill half the
+// SMs (each tile walks all of K alone, so tile count sets the pace). Above,
+// 128- or 256-token tiles, whichever needs fewer whole waves of persistent
+// CTAs, a wave of 256-token tiles counted as 1.27 of 128-token ones (measured
+// on GB300: 1.22 to 1.29 per wave over 1024-4096 tokens, both shapes of a
+// 27B-class MLP; the wider tile halves the epilogue's fixed cost per element)
+int prefill_tile_q4k(int64_t M, int64_t N, int sms) {
+  const int64_t NT = ceil_div(N, (int64_t)kBN);
+  if (M <= 64) return (QG_W4_BM32 && (M <= 32 || 2 * NT <= sms)) ? 32 : 64;
+  if (QG_BM_W4A8) return QG_BM_W4A8;
+  const int64_t w128 = ceil_div(ceil_div(M, (int64_t)128) * NT, (int64_t)sms);
+  const int64_t w256 = ceil_div(ceil_div(M, (int64_t)256) * NT, (int64_t)sms);
+  return 127 * w256 < 100 * w128 ? 256 : 128;
+}
+
 cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
                                int64_t M, int64_t K, const void* packed, int64_t N, void* out,
                                bool out_f32, int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
@@ -957,18 +992,13 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.dbg = dbg;
   a.err = err;
   a.pdl = (pdl && !dbg) ? 1 : 0;
-  constexpr int BM = QG_BM_W4A8;
-  if (dbg) return launch_prefill_t<true, true, BM>(ta, q16, a, st);
-  // a GEMM of at most 64 tokens fills half of a 128-token tile: 64-token
-  // tiles, or 32-token tiles when there are too few weight-row tiles to fill
-  // half the SMs (each tile walks all of K alone, so tile count sets the pace)
-  if (M <= 64) {
-    const int64_t NT = ceil_div(N, (int64_t)kBN);
-    if (QG_W4_BM32 && (M <= 32 || 2 * NT <= num_sms()))
-      return launch_prefill_t<true, false, 32>(ta, q16, a, st);
-    return launch_prefill_t<true, false, 64>(ta, q16, a, st);
+  if (dbg) return launch_prefill_t<true, true, 128>(ta, q16, a, st);
+  switch (prefill_tile_q4k(M, N, num_sms())) {
+    case 32: return launch_prefill_t<true, false, 32>(ta, q16, a, st);
+    case 64: return launch_prefill_t<true, false, 64>(ta, q16, a, st);
+    case 256: return launch_prefill_t<true, false, 256>(ta, q16, a, st);
+    default: return launch_prefill_t<true, false, 128>(ta, q16, a, st);
   }
-  return launch_prefill_t<true, false, BM>(ta, q16, a, st);
 }
 
 }  // namespace qg

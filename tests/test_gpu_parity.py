@@ -330,6 +330,30 @@ def test_w4a8_block_sums_exact(path):
     assert np.array_equal(bs.cpu().numpy(), ra)
 
 
+def test_w4a8_256_token_tiles():
+    # 700 tokens x 5000 weight rows: on 152 SMs three 256-token tiles per
+    # weight-row tile (the last one ragged, and a ragged last weight-row tile),
+    # 120 tiles in one wave against 240 as 128-token tiles; every output
+    # compared in bf16 and fp32, and rows alone equal the batch's rows
+    from bit_quantized_gemm_gb300 import _lib
+    M, K, N = 700, 512, 5000
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _lib.prefill_tile_q4k(M, N, 152) == 256
+    x, bits = synth.activations(71, M, K, dtype="bf16", outlier_frac=0.01)
+    sblocks = synth.q4k_weights(171, N, K)
+    out, (q, h, s, bs, packed) = gpu_w4a8(bits, sblocks, N, "auto")
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+    got = out_bits(out)
+    bad = np.argwhere(got != ob)
+    assert bad.size == 0, "first mismatches %s" % bad[:5].tolist()
+    out32, _ = gpu_w4a8(bits, sblocks, N, "auto", out_dtype=torch.float32)
+    assert np.array_equal(out_bits(out32), y.view(np.uint32))
+    for r in (0, 255, 256, 699):
+        o = qg.gemm_w4a8_q4k(q[r:r + 1], h[r:r + 1], s[r:r + 1], bs[r:r + 1], packed, N)
+        assert np.array_equal(out_bits(o)[0], got[r])
+
+
 def test_w4a8_batch_invariance():
     K, N = 512, 96
     xs, bits = synth.activations(31, 150, K, dtype="bf16", outlier_frac=0.01)
