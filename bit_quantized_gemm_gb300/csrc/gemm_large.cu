@@ -84,6 +84,9 @@ namespace qg {
 #ifndef QG_W4_SCALAR_BM
 #define QG_W4_SCALAR_BM 256  // W4A8 tiles at least this wide load scalar scales one block ahead
 #endif
+#ifndef QG_W4_SCALAR_AHEAD
+#define QG_W4_SCALAR_AHEAD 1  // blocks ahead of their use that scalar W4A8 scales are loaded
+#endif
 #ifndef QG_W4_BM32
 #define QG_W4_BM32 1  // W4A8 GEMMs of at most 64 tokens may run 32-token tiles
 #endif
@@ -472,7 +475,8 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
       // spill there).
       constexpr int kQA = (kQ4K && BM < QG_W4_SCALAR_BM) ? 1 : 0;
       constexpr int kQR = kQA > 0 ? kQA + 1 : 1;
-      float d_next = 0.0f, m_next = 0.0f;
+      constexpr int kSA = kQ4K ? QG_W4_SCALAR_AHEAD : 1;  // scalar loads: blocks ahead
+      float d_next[kSA], m_next[kSA];
       float4 dq[kQR], mq[kQR];
 #pragma unroll
       for (int i = 0; i < kQR; ++i) {
@@ -482,9 +486,13 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           if (kQ4K) mq[i] = ldg_f32x4_pinned(mrow + 4 * i);
         }
       }
-      if (kQA == 0 && nvalid) {
-        d_next = ldg_f32_pinned(drow);
-        if (kQ4K) m_next = ldg_f32_pinned(mrow);
+#pragma unroll
+      for (int i = 0; i < kSA; ++i) {
+        d_next[i] = m_next[i] = 0.0f;
+        if (kQA == 0 && nvalid && i < NB) {
+          d_next[i] = ldg_f32_pinned(drow + i);
+          if (kQ4K) m_next[i] = ldg_f32_pinned(mrow + i);
+        }
       }
       for (int blk = 0; blk < NB && ok; ++blk) {
         float dw, ndm = 0.0f;
@@ -505,11 +513,16 @@ __global__ void __launch_bounds__(threads_for(BM), kCtasPerSm)
           dw = q == 0 ? dq[0].x : q == 1 ? dq[0].y : q == 2 ? dq[0].z : dq[0].w;
           if (kQ4K) ndm = -(q == 0 ? mq[0].x : q == 1 ? mq[0].y : q == 2 ? mq[0].z : mq[0].w);
         } else {
-          dw = d_next;
-          if (kQ4K) ndm = -m_next;
-          if (blk + 1 < NB && nvalid) {
-            d_next = ldg_f32_pinned(drow + blk + 1);
-            if (kQ4K) m_next = ldg_f32_pinned(mrow + blk + 1);
+          dw = d_next[0];
+          if (kQ4K) ndm = -m_next[0];
+#pragma unroll
+          for (int i = 0; i + 1 < kSA; ++i) {
+            d_next[i] = d_next[i + 1];
+            if (kQ4K) m_next[i] = m_next[i + 1];
+          }
+          if (blk + kSA < NB && nvalid) {
+            d_next[kSA - 1] = ldg_f32_pinned(drow + blk + kSA);
+            if (kQ4K) m_next[kSA - 1] = ldg_f32_pinned(mrow + blk + kSA);
           }
         }
         const int tb = kStageMode ? (2 * (ti * NS + (blk >> 1)) + (blk & 1)) % kTBufs
