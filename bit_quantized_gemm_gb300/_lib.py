@@ -60,7 +60,7 @@ def load():
         "qg_gemm_launch_count": ([I, I64, I64, I64, I], I),
         "qg_linear_workspace_bytes": ([I, I64, I64], SZ),
         "qg_debug_prefill_plan_q8_0": ([I64, I64, I, P, P, P], I),
-        "qg_debug_prefill_tile_q4k": ([I64, I64, I, P], I),
+        "qg_debug_prefill_tile_q4k": ([I64, I64, I, P, P], I),
         "qg_linear_w8a8_q8_0": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w4a8_q4k": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P, SZ, P], I),
         "qg_linear_w8a8_q8_0_noalloc": ([P, I, I64, I64, I64, P, I64, P, I, I64, P, P], I),
@@ -315,10 +315,11 @@ def linear_w8a8_q8_0_noalloc(x, packed, N, out=None, out_dtype=torch.bfloat16, s
 
 
 def prefill_tile_q4k(M, N, sms):
-    """The W4A8 prefill kernel's token-tile width for an M x N GEMM on `sms` SMs."""
+    """The W4A8 GEMM's tiles for M x N on `sms` SMs: ("tensor" / "16-row", token width)."""
+    kind = ctypes.c_int()
     tokens = ctypes.c_int()
-    _check(load().qg_debug_prefill_tile_q4k(M, N, sms, ctypes.byref(tokens)))
-    return tokens.value
+    _check(load().qg_debug_prefill_tile_q4k(M, N, sms, ctypes.byref(kind), ctypes.byref(tokens)))
+    return {1: "tensor", 2: "16-row"}[kind.value], tokens.value
 
 
 def prefill_plan(M, N, sms):

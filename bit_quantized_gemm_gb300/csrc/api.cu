@@ -37,7 +37,7 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
                                 int64_t ldo, int32_t* dbg, uint32_t* err, bool pdl,
                                 cudaStream_t st);
 int prefill_launches_q8_0(int64_t M, int64_t N);
-int prefill_tile_q4k(int64_t M, int64_t N, int sms);
+int prefill_tile_q4k(int64_t M, int64_t N, int sms, int* kind);
 void prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide, int* narrow_kind,
                        int* narrow_tokens);
 
@@ -275,12 +275,12 @@ qg_status qg_debug_prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* row
   return QG_OK;
 }
 
-qg_status qg_debug_prefill_tile_q4k(int64_t M, int64_t N, int sms, int* tokens) {
-  if (!tokens) return fail(QG_EINVAL, "null pointer argument");
+qg_status qg_debug_prefill_tile_q4k(int64_t M, int64_t N, int sms, int* kind, int* tokens) {
+  if (!kind || !tokens) return fail(QG_EINVAL, "null pointer argument");
   if (M < 1 || M > kMaxM || N < 1 || N > kMaxN)
     return fail(QG_EINVAL, "M, N out of range [1, 2^24]");
   if (sms < 1 || sms > 4096) return fail(QG_EINVAL, "sms=%d out of range [1, 4096]", sms);
-  *tokens = prefill_tile_q4k(M, N, sms);
+  *tokens = prefill_tile_q4k(M, N, sms, kind);
   return QG_OK;
 }
 

@@ -87,6 +87,9 @@ namespace qg {
 #ifndef QG_W4_SCALAR_AHEAD
 #define QG_W4_SCALAR_AHEAD 1  // blocks ahead of their use that scalar W4A8 scales are loaded
 #endif
+#ifndef QG_W4_SKINNY
+#define QG_W4_SKINNY 1  // W4A8 GEMMs of at most 64 tokens may run 16-row tiles
+#endif
 #ifndef QG_W4_BM32
 #define QG_W4_BM32 1  // W4A8 GEMMs of at most 64 tokens may run 32-token tiles
 #endif
@@ -882,6 +885,10 @@ static PrefillPlan plan_as_built(int64_t M, int64_t N, int sms) {
 }
 
 // gemm_skinny.cu: 16-weight-row tiles on legacy fp16 MMA
+cudaError_t launch_skinny_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
+                              int64_t M, int64_t K, const uint16_t* wq16, const float* ds32,
+                              const float* dm32, int64_t ldd, int64_t N, void* out, bool out_f32,
+                              int64_t ldo, int tb, uint32_t* err, bool pdl, cudaStream_t st);
 cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, int64_t K,
                                const uint16_t* wq16, const float* d32, int64_t ldd, int64_t N,
                                void* out, bool out_f32, int64_t ldo, int tb, uint32_t* err,
@@ -967,17 +974,27 @@ cudaError_t launch_prefill_q8_0(const uint16_t* q16, const float* sa, int64_t M,
   }
 }
 
-// Token-tile width of the W4A8 prefill kernel for an M x N GEMM on `sms` SMs.
-// A GEMM of at most 64 tokens fills half of a 128-token tile: 64-token tiles,
-// or 32-token tiles when there are too few weight-row tiles to fill half the
-// SMs (each tile walks all of K alone, so tile count sets the pace). Above,
-// 128- or 256-token tiles, whichever needs fewer whole waves of persistent
-// CTAs, a wave of 256-token tiles counted as 1.27 of 128-token ones (measured
-// on GB300: 1.22 to 1.29 per wave over 1024-4096 tokens, both shapes of a
+// Tiles of the W4A8 GEMM for M x N on `sms` SMs: kind 1 = tensor-memory tiles
+// of 128 weight rows, kind 2 = 16-row tiles of gemm_skinny.cu; and the token
+// width. A GEMM of at most 64 tokens whose 128-row tiles cannot fill half the
+// SMs runs as 16-row tiles of 32 or 64 tokens (each tile walks all of K
+// alone, so tile count sets the pace: 17408 -> 5120 at 64 tokens, 40 row
+// tiles, 215 us as 32-token tensor-memory tiles). Other GEMMs of at most 64
+// tokens: 64-token tensor-memory tiles (32 up to 32 tokens). Above, 128- or
+// 256-token tiles, whichever needs fewer whole waves of persistent CTAs, a
+// wave of 256-token tiles counted as 1.27 of 128-token ones (measured on
+// GB300: 1.22 to 1.29 per wave over 1024-4096 tokens, both shapes of a
 // 27B-class MLP; the wider tile halves the epilogue's fixed cost per element)
-int prefill_tile_q4k(int64_t M, int64_t N, int sms) {
+int prefill_tile_q4k(int64_t M, int64_t N, int sms, int* kind) {
   const int64_t NT = ceil_div(N, (int64_t)kBN);
-  if (M <= 64) return (QG_W4_BM32 && (M <= 32 || 2 * NT <= sms)) ? 32 : 64;
+  *kind = 1;
+  if (M <= 64) {
+    if (QG_W4_SKINNY && 2 * NT <= sms) {
+      *kind = 2;
+      return M <= 32 ? 32 : 64;
+    }
+    return (QG_W4_BM32 && (M <= 32 || 2 * NT <= sms)) ? 32 : 64;
+  }
   if (QG_BM_W4A8) return QG_BM_W4A8;
   const int64_t w128 = ceil_div(ceil_div(M, (int64_t)128) * NT, (int64_t)sms);
   const int64_t w256 = ceil_div(ceil_div(M, (int64_t)256) * NT, (int64_t)sms);
@@ -1006,7 +1023,12 @@ cudaError_t launch_prefill_q4k(const uint16_t* q16, const float* sa, const int32
   a.err = err;
   a.pdl = (pdl && !dbg) ? 1 : 0;
   if (dbg) return launch_prefill_t<true, true, 128>(ta, q16, a, st);
-  switch (prefill_tile_q4k(M, N, num_sms())) {
+  int kind = 1;
+  const int tb = prefill_tile_q4k(M, N, num_sms(), &kind);
+  if (kind == 2)
+    return launch_skinny_q4k(q16, sa, bsum, M, K, reinterpret_cast<const uint16_t*>(base + L.off_q16),
+                             a.d32, a.dm32, a.ldd, N, out, out_f32, ldo, tb, err, a.pdl != 0, st);
+  switch (tb) {
     case 32: return launch_prefill_t<true, false, 32>(ta, q16, a, st);
     case 64: return launch_prefill_t<true, false, 64>(ta, q16, a, st);
     case 256: return launch_prefill_t<true, false, 256>(ta, q16, a, st);

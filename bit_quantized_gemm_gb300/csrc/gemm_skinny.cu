@@ -1,10 +1,12 @@
-// gemm_skinny.cu -- W8A8 GEMM tiles of 16 weight rows on legacy fp16 MMA.
+// gemm_skinny.cu -- W8A8 and W4A8 GEMM tiles of 16 weight rows on legacy fp16 MMA.
 //
-// Operation: the W8A8 (Q8_0) product with exact int32 block sums and the
-// fixed ascending-block fp32 epilogue (StartLux-Prism README, "Why
-// StartLux-Prism": "Reproducible to the bit"; "How it works": int8 tensor
-// cores with exact int32 sums) -- the same chain as the other kernels, so all
-// give identical bits.
+// Operation: the W8A8 (Q8_0) and W4A8 (Q4_K) products with exact int32 block
+// sums and the fixed ascending-block fp32 epilogue (StartLux-Prism README,
+// "Why StartLux-Prism": "Reproducible to the bit"; "How it works": int8
+// tensor cores with exact int32 sums, W4A8 as 4-bit weights against 8-bit
+// activations) -- the same chain as the other kernels, so all give identical
+// bits: W8A8 one fma(isum, d, acc) per block, W4A8 fma(isum, d*sc, acc) then
+// fma(-asum, dmin*m, acc) per 32-wide sub-block.
 //
 // Use: work that the tensor-memory kernel can only cut into narrow tiles --
 // the weight rows left over after whole waves of 256-token tiles, and GEMMs
@@ -14,16 +16,17 @@
 // warp sums a block exactly with four m16n8k16 fp16 MMAs and applies that
 // block's FMAs at once, in registers: no accumulator hand-off at all.
 //   * operands: the fp16 copies of the weights ([N][K], from the packed
-//     buffer) and activations (q16 [M][K]) arrive by TMA, 64 K (two blocks)
-//     per stage, 128-byte swizzle; fragments come out with ldmatrix;
+//     buffer; Q4_K: the 4-bit values) and activations (q16 [M][K]) arrive by
+//     TMA, 64 K (two blocks) per stage, 128-byte swizzle; fragments come out
+//     with ldmatrix;
 //   * one producer warp (lane 0) runs the ring; the compute warps hand each
 //     stage back per thread (no warp-wide operation on the path);
-//   * weight scales: d[n][b] from the fp32 scale rows, a stage's two blocks
-//     per 8-byte load, fetched three stages ahead through a short register
-//     pipeline (one stage ahead left the loads' latency exposed).
+//   * per-block operands of the FMAs -- weight scales d[n][b] (W4A8: d*sc and
+//     dmin*m) from the fp32 scale rows and, for W4A8, the activation block
+//     sums of the lane's four tokens -- a stage's two blocks per 8-byte load,
+//     fetched several stages ahead into fixed register slots (one stage ahead
+//     left the loads' latency exposed).
 #include <cuda.h>
-
-#include <type_traits>
 
 #include "qg_common.cuh"
 
@@ -32,11 +35,11 @@ namespace qg {
 // from gemm_large.cu
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows);
 
-#ifndef QG_SK_SCALE_AHEAD
-#define QG_SK_SCALE_AHEAD 3  // trips whose scales are loaded ahead of their use
+#ifndef QG_SK_SCALE_AHEAD_Q4K
+#define QG_SK_SCALE_AHEAD_Q4K 2  // the same for W4A8 (four more loads per stage)
 #endif
-#ifndef QG_SK_STAGES_PER_TRIP
-#define QG_SK_STAGES_PER_TRIP 1  // stages whose blocks a compute warp sums before their FMAs
+#ifndef QG_SK_SCALE_AHEAD
+#define QG_SK_SCALE_AHEAD 4  // stages whose scales are loaded ahead of their use
 #endif
 constexpr int kSkRows = 16;  // weight rows per CTA (the MMA's M)
 constexpr int kSkBK = 64;    // K per stage: two blocks, one 128-byte swizzle row
@@ -60,7 +63,9 @@ struct SkinnyCfg {
 };
 
 struct SkinnyArgs {
-  const float* d32;  // [N][ldd] fp32 weight scales (rows padded to whole quads)
+  const float* d32;  // [N][ldd] fp32 weight scales (rows padded to whole quads); W4A8: d*sc
+  const float* dm32;     // W4A8: dmin*m [N][ldd]
+  const int32_t* bsum;   // W4A8: [M][K/32] activation block sums
   const float* sa;   // [M] activation scales
   void* out;
   int64_t ldo, ldd;
@@ -69,6 +74,14 @@ struct SkinnyArgs {
   int pdl;  // launched as a programmatic dependent of the quantize kernel
   uint32_t* err;
 };
+
+// 8-byte read-only load of two int32, volatile so the compiler keeps it
+// where it is written (p 8-byte aligned)
+__device__ __forceinline__ int2 ldg_s32x2_pinned(const int32_t* p) {
+  int2 v;
+  asm volatile("ld.global.nc.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -82,7 +95,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int k) {
   return (uint32_t)(r * 128 + ((((k >> 3) ^ r) & 7) << 4));
 }
 
-template <int TB>
+template <int TB, bool kQ4K>
 __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const SkinnyArgs args) {
@@ -152,6 +165,8 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
   }
 
   // ------------------------------------------------------------- compute
+  // W4A8: the activation block sums come from the quantize kernel
+  if (kQ4K && args.pdl) griddep_wait();
   const int g = lane >> 2, t = lane & 3;
   const int nA = n0 + g, nB = n0 + g + 8;  // this lane's two weight rows
   const float* drA = args.d32 + (int64_t)(nA < N ? nA : 0) * args.ldd;
@@ -165,62 +180,55 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
 #pragma unroll
   for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
 
-  // kU stages (2*kU blocks) per trip: their sums first, so the blocks' MMA
-  // chains overlap, then their FMAs in block order. The trip's scales are
-  // loaded one trip ahead (kU = 1: 8-byte loads, a stage's first block is
-  // even; kU = 2: 16-byte loads, a pair's first block is a multiple of 4;
-  // rows are padded to whole quads)
-  constexpr int kU = QG_SK_STAGES_PER_TRIP;
-  static_assert(kU == 1 || kU == 2, "stages per trip");
-  using ScaleV = typename std::conditional<kU == 2, float4, float2>::type;
-  auto load_scales = [&](const float* p) -> ScaleV {
-    if constexpr (kU == 2) return ldg_f32x4_pinned(p);
-    else return ldg_f32x2_pinned(p);
-  };
-  // scales of the next kP trips in flight (a shift register of loads)
-  constexpr int kP = QG_SK_SCALE_AHEAD;
-  ScaleV pA[kP], pB[kP];
+  // Per stage (two blocks): wait for the slot, sum each block exactly with
+  // four MMAs, hand the slot back, then the blocks' FMAs in block order. The
+  // weight scales of stage s (W4A8: d*sc, dmin*m and this lane's activation
+  // block sums) sit in register slot s % kP, loaded kP stages ahead; the stage
+  // loop is unrolled by kP so that each slot is a fixed set of registers and
+  // no register move waits on a load in flight.
+  constexpr int kP = kQ4K ? QG_SK_SCALE_AHEAD_Q4K : QG_SK_SCALE_AHEAD;
+  constexpr int kPQ = kQ4K ? kP : 1;
+  float2 pA[kP], pB[kP], qA[kPQ], qB[kPQ];
+  int2 pS[kPQ][2][2];  // [slot][token tile][token 2t + e]: sums of the stage's two blocks
+  const float* dmA = kQ4K ? args.dm32 + (int64_t)(nA < N ? nA : 0) * args.ldd : nullptr;
+  const float* dmB = kQ4K ? args.dm32 + (int64_t)(nB < N ? nB : 0) * args.ldd : nullptr;
+  const int mb = m0 + 16 * warp + 2 * t;  // this lane's first token (then +1, +8, +9)
+  // a stage's first block is even and rows are padded to whole quads (Q8_0)
+  // or hold a multiple of 8 blocks (Q4_K): 8-byte loads stay in the row
+  auto load_slot = [&](int j, int s) {
+    const int blk = 2 * s;
+    pA[j] = ldg_f32x2_pinned(drA + blk);
+    pB[j] = ldg_f32x2_pinned(drB + blk);
+    if constexpr (kQ4K) {
+      qA[j] = ldg_f32x2_pinned(dmA + blk);
+      qB[j] = ldg_f32x2_pinned(dmB + blk);
 #pragma unroll
-  for (int p = 0; p < kP; ++p) {
-    if (2 * kU * p < NB) {
-      pA[p] = load_scales(drA + 2 * kU * p);
-      pB[p] = load_scales(drB + 2 * kU * p);
+      for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int m = min(mb + 8 * tt + e, M - 1);  // rows past M: any valid row, unused
+          pS[j][tt][e] = ldg_s32x2_pinned(args.bsum + (int64_t)m * NB + blk);
+        }
     }
-  }
+  };
+#pragma unroll
+  for (int j = 0; j < kP; ++j)
+    if (j < NS) load_slot(j, j);
   int st = 0;
   uint32_t ph = 0;
   bool ok = true;
-  for (int s = 0; s < NS && ok; s += kU) {
-    const ScaleV cA = pA[0], cB = pB[0];
+  for (int s0 = 0; s0 < NS && ok; s0 += kP) {
 #pragma unroll
-    for (int p = 0; p + 1 < kP; ++p) {
-      pA[p] = pA[p + 1];
-      pB[p] = pB[p + 1];
-    }
-    if (2 * (s + kU * kP) < NB) {
-      pA[kP - 1] = load_scales(drA + 2 * (s + kU * kP));
-      pB[kP - 1] = load_scales(drB + 2 * (s + kU * kP));
-    }
-    const int nst = (s + kU <= NS) ? kU : NS - s;  // stages in this trip
-    int sts[kU];
-    uint32_t phs[kU];
-#pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      sts[q] = st;
-      phs[q] = ph;
-      if (q < nst && ++st == kS) { st = 0; ph ^= 1; }
-    }
-#pragma unroll
-    for (int q = 0; q < kU; ++q)
-      if (q < nst && ok) ok = mbar_wait(&full[sts[q]], phs[q], args.err);
-    if (!ok) break;
-    // every block's sums first (a missing second block of a K tail reads the
-    // zero-filled box and is never used; a missing stage is not read)
-    float d[2 * kU][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
-#pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      if (q < nst) {
-        const uint32_t a_s = smem_u32(sm + sts[q] * C::kStageBytes);
+    for (int j = 0; j < kP; ++j) {
+      const int s = s0 + j;
+      if (s >= NS) break;
+      ok = mbar_wait(&full[st], ph, args.err);
+      if (!ok) break;
+      // both blocks' sums first (a missing second block of a K tail reads the
+      // zero-filled box and is never used)
+      float d[2][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
+      {
+        const uint32_t a_s = smem_u32(sm + st * C::kStageBytes);
         const uint32_t b_s = a_s + C::kABytes;
 #pragma unroll
         for (int jb = 0; jb < 2; ++jb) {
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
             ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
             ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
             // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
-            float(&dd)[2][4] = d[2 * q + jb];
+            float(&dd)[2][4] = d[jb];
             if (kh == 0) {
               mma_f16_16816(dd[0], af, bfr[0], bfr[1], zero4);
               mma_f16_16816(dd[1], af, bfr[2], bfr[3], zero4);
@@ -242,23 +250,33 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
           }
         }
       }
-    }
+      mbar_arrive(&empty[st]);  // this thread's reads of the stage are done
+      if (++st == kS) { st = 0; ph ^= 1; }
 #pragma unroll
-    for (int q = 0; q < kU; ++q)
-      if (q < nst) mbar_arrive(&empty[sts[q]]);  // this thread's reads of the stage are done
+      for (int jb = 0; jb < 2; ++jb) {
+        if (2 * s + jb < NB) {
+          const float dA = jb ? pA[j].y : pA[j].x, dB = jb ? pB[j].y : pB[j].x;
+          const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
 #pragma unroll
-    for (int jb = 0; jb < 2 * kU; ++jb) {
-      if (2 * s + jb < NB) {
-        const float* fa = reinterpret_cast<const float*>(&cA);
-        const float* fb = reinterpret_cast<const float*>(&cB);
-        const float dA = fa[jb], dB = fb[jb];
-        const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
+          for (int tt = 0; tt < 2; ++tt) {
+            acc[tt][0] = __ffma2_rn(make_float2(d[jb][tt][0], d[jb][tt][1]), dA2, acc[tt][0]);
+            acc[tt][1] = __ffma2_rn(make_float2(d[jb][tt][2], d[jb][tt][3]), dB2, acc[tt][1]);
+          }
+          if constexpr (kQ4K) {
+            // then the min term of the same sub-block: fma(-asum, dmin*m, acc)
+            const float mA = jb ? qA[j].y : qA[j].x, mB = jb ? qB[j].y : qB[j].x;
+            const float2 nmA2 = make_float2(-mA, -mA), nmB2 = make_float2(-mB, -mB);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-          acc[tt][0] = __ffma2_rn(make_float2(d[jb][tt][0], d[jb][tt][1]), dA2, acc[tt][0]);
-          acc[tt][1] = __ffma2_rn(make_float2(d[jb][tt][2], d[jb][tt][3]), dB2, acc[tt][1]);
+            for (int tt = 0; tt < 2; ++tt) {
+              const float2 as = jb ? make_float2((float)pS[j][tt][0].y, (float)pS[j][tt][1].y)
+                                   : make_float2((float)pS[j][tt][0].x, (float)pS[j][tt][1].x);
+              acc[tt][0] = __ffma2_rn(as, nmA2, acc[tt][0]);
+              acc[tt][1] = __ffma2_rn(as, nmB2, acc[tt][1]);
+            }
+          }
         }
       }
+      if (s + kP < NS) load_slot(j, s + kP);
     }
   }
   if (!ok) return;
@@ -282,14 +300,14 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
   }
 }
 
-template <int TB>
+template <int TB, bool kQ4K>
 static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, const SkinnyArgs& a,
                                    cudaStream_t st) {
   using C = SkinnyCfg<TB>;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, wq16, a.N, a.K, kSkRows) || !make_tmap(&tb, q16, a.M, a.K, TB))
     return cudaErrorNotSupported;
-  auto kern = skinny_gemm_kernel<TB>;
+  auto kern = skinny_gemm_kernel<TB, kQ4K>;
   static std::atomic<uint64_t> attr_set{0};
   {
     const cudaError_t e = smem_attr_once_per_device(kern, (int)C::kSmem, attr_set);
@@ -316,9 +334,33 @@ cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, 
   a.M = (int)M; a.N = (int)N; a.K = (int)K;
   a.out_f32 = out_f32 ? 1 : 0;
   a.err = err;
-  if (tb == 32) return launch_skinny_t<32>(wq16, q16, a, st);
-  if (tb == 64) return launch_skinny_t<64>(wq16, q16, a, st);
-  return launch_skinny_t<128>(wq16, q16, a, st);
+  if (tb == 32) return launch_skinny_t<32, false>(wq16, q16, a, st);
+  if (tb == 64) return launch_skinny_t<64, false>(wq16, q16, a, st);
+  return launch_skinny_t<128, false>(wq16, q16, a, st);
+}
+
+// W4A8 (Q4_K): the same tiles over the fp16 copy of the 4-bit values, with the
+// sub-block scales d*sc and dmin*m (rows of ldd floats) and the activation
+// block sums [M][K/32]; each block's two FMAs in the order of the other W4A8
+// kernels (isum term, then min term). 32 or 64 tokens.
+cudaError_t launch_skinny_q4k(const uint16_t* q16, const float* sa, const int32_t* bsum,
+                              int64_t M, int64_t K, const uint16_t* wq16, const float* ds32,
+                              const float* dm32, int64_t ldd, int64_t N, void* out, bool out_f32,
+                              int64_t ldo, int tb, uint32_t* err, bool pdl, cudaStream_t st) {
+  SkinnyArgs a{};
+  a.pdl = pdl ? 1 : 0;
+  a.d32 = ds32;
+  a.dm32 = dm32;
+  a.bsum = bsum;
+  a.ldd = ldd;
+  a.sa = sa;
+  a.out = out;
+  a.ldo = ldo;
+  a.M = (int)M; a.N = (int)N; a.K = (int)K;
+  a.out_f32 = out_f32 ? 1 : 0;
+  a.err = err;
+  if (tb == 32) return launch_skinny_t<32, true>(wq16, q16, a, st);
+  return launch_skinny_t<64, true>(wq16, q16, a, st);
 }
 
 }  // namespace qg

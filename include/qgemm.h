@@ -315,12 +315,13 @@ qg_status qg_debug_block_sums_q4k(const int8_t* q, const uint16_t* q16, int64_t 
 qg_status qg_debug_prefill_plan_q8_0(int64_t M, int64_t N, int sms, int64_t* rows_wide,
                                      int* narrow_kind, int* narrow_tokens);
 
-/* Test support: the token-tile width (32, 64, 128 or 256) of the W4A8
- * prefill kernel for an M x N GEMM on a GPU of `sms` SMs, as
- * qg_gemm_w4a8_q4k carries it out there (M above qg_small_m_max(), AUTO; one
- * launch). Host-only; launches nothing. The width never changes a bit of the
- * result. */
-qg_status qg_debug_prefill_tile_q4k(int64_t M, int64_t N, int sms, int* tokens);
+/* Test support: the tiles of the W4A8 GEMM for M x N on a GPU of `sms` SMs,
+ * as qg_gemm_w4a8_q4k carries it out there (M above qg_small_m_max(), AUTO;
+ * one launch): *kind 1 = tensor-memory tiles of 128 weight rows, 2 = tiles of
+ * 16 weight rows (legacy fp16 MMA); *tokens = the token-tile width (32, 64,
+ * 128 or 256). Host-only; launches nothing. The tiles never change a bit of
+ * the result. */
+qg_status qg_debug_prefill_tile_q4k(int64_t M, int64_t N, int sms, int* kind, int* tokens);
 
 /* Test support for failure detection: launches one bounded wait on a
  * barrier that nothing completes; after `polls` polls (1 .. 2^20) it records

@@ -218,26 +218,36 @@ def test_prefill_wave_plan_on_152_sms(L):
     assert plan(64, 5120, 152) == (0, "16-row", 64)        # 40 row tiles: 16-row tiles, one wave
 
 
-def test_w4a8_tile_width_on_152_sms(L):
-    # 256-token tiles where their whole waves, at 1.27 each, beat 128-token ones
+def test_w4a8_tiles_on_152_sms(L):
+    # 256-token tiles where their whole waves, at 1.27 each, beat 128-token
+    # ones; 16-row tiles for at most 64 tokens when 128-row tiles fill at most
+    # half the SMs
     tile = _lib.prefill_tile_q4k
-    assert tile(4096, 17408, 152) == 256   # 15 waves against 29
-    assert tile(4096, 5120, 152) == 256    # 5 against 9
-    assert tile(1024, 5120, 152) == 256    # 2 against 3
-    assert tile(256, 17408, 152) == 256    # 1 against 2
-    assert tile(256, 5120, 152) == 128     # 40 or 80 tiles: one wave either way
-    assert tile(128, 17408, 152) == 128    # one token tile either way
-    assert tile(65, 129, 152) == 128
-    assert tile(700, 5000, 152) == 256     # the GPU parity case of 256-token tiles
-    assert tile(64, 17408, 152) == 64      # 136 row tiles fill more than half the SMs
-    assert tile(64, 5120, 152) == 32       # 40 row tiles: 32-token tiles
-    assert tile(32, 17408, 152) == 32
-    for M in (65, 100, 300, 1000, 2048, 8192):
+    assert tile(4096, 17408, 152) == ("tensor", 256)   # 15 waves against 29
+    assert tile(4096, 5120, 152) == ("tensor", 256)    # 5 against 9
+    assert tile(1024, 5120, 152) == ("tensor", 256)    # 2 against 3
+    assert tile(256, 17408, 152) == ("tensor", 256)    # 1 against 2
+    assert tile(256, 5120, 152) == ("tensor", 128)     # 40 or 80 tiles: one wave either way
+    assert tile(128, 17408, 152) == ("tensor", 128)    # one token tile either way
+    assert tile(65, 129, 152) == ("tensor", 128)
+    assert tile(700, 5000, 152) == ("tensor", 256)     # the GPU parity case of 256-token tiles
+    assert tile(64, 17408, 152) == ("tensor", 64)      # 136 row tiles fill more than half the SMs
+    assert tile(32, 17408, 152) == ("tensor", 32)
+    assert tile(64, 5120, 152) == ("16-row", 64)       # 40 row tiles
+    assert tile(33, 5120, 152) == ("16-row", 64)
+    assert tile(32, 5120, 152) == ("16-row", 32)
+    assert tile(17, 9728, 152) == ("16-row", 32)       # 76 row tiles: half the SMs
+    assert tile(17, 9856, 152) == ("tensor", 32)       # 77
+    for M in (17, 40, 64, 65, 100, 300, 1000, 2048, 8192):
         for N in (16, 130, 5120, 17408):
             for sms in (1, 8, 148, 152):
-                t = tile(M, N, sms)
-                assert t in (128, 256)
+                kind, t = tile(M, N, sms)
                 nt = -(-N // 128)
+                if M <= 64:
+                    assert (kind == "16-row") == (2 * nt <= sms)
+                    assert t == (32 if M <= 32 else 64)
+                    continue
+                assert kind == "tensor" and t in (128, 256)
                 w128, w256 = -(-(-(-M // 128) * nt) // sms), -(-(-(-M // 256) * nt) // sms)
                 assert (t == 256) == (127 * w256 < 100 * w128)
     with pytest.raises(qg.QGError):

@@ -155,9 +155,14 @@ def test_skinny_long_k_repeated(M, N, tb):
 
 
 def test_w4a8_q4k_narrow_down_projection():
-    # 17408 -> 5120 at 32 and 64 tokens: 40 weight-row tiles, so these run as
-    # 32-token tiles, each walking all 544 sub-blocks; every output compared
+    # 17408 -> 5120 at 32 and 64 tokens: 40 weight-row tiles of 128, so these
+    # run as 16-row tiles (320 per token tile), each walking all 544 sub-blocks;
+    # every output compared
+    from bit_quantized_gemm_gb300 import _lib
     K, N = 17408, 5120
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _lib.prefill_tile_q4k(32, N, 152) == ("16-row", 32)
+        assert _lib.prefill_tile_q4k(64, N, 152) == ("16-row", 64)
     sblocks = synth.config_weights("w4a8_q4k", N, K)
     packed = qg.pack_q4k(to_dev(sblocks), N, K)
     for M in (32, 64):

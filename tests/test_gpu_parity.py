@@ -338,7 +338,7 @@ def test_w4a8_256_token_tiles():
     from bit_quantized_gemm_gb300 import _lib
     M, K, N = 700, 512, 5000
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert _lib.prefill_tile_q4k(M, N, 152) == 256
+        assert _lib.prefill_tile_q4k(M, N, 152) == ("tensor", 256)
     x, bits = synth.activations(71, M, K, dtype="bf16", outlier_frac=0.01)
     sblocks = synth.q4k_weights(171, N, K)
     out, (q, h, s, bs, packed) = gpu_w4a8(bits, sblocks, N, "auto")
@@ -350,6 +350,29 @@ def test_w4a8_256_token_tiles():
     out32, _ = gpu_w4a8(bits, sblocks, N, "auto", out_dtype=torch.float32)
     assert np.array_equal(out_bits(out32), y.view(np.uint32))
     for r in (0, 255, 256, 699):
+        o = qg.gemm_w4a8_q4k(q[r:r + 1], h[r:r + 1], s[r:r + 1], bs[r:r + 1], packed, N)
+        assert np.array_equal(out_bits(o)[0], got[r])
+
+
+@pytest.mark.parametrize("M,K,N,tb", [(50, 2048, 1000, 64), (24, 1024, 520, 32), (64, 256, 16, 64)])
+def test_w4a8_16_row_tiles(M, K, N, tb):
+    # W4A8 GEMMs of at most 64 tokens whose 128-row tiles would fill at most
+    # half the SMs run as 16-row tiles (ragged last row tile and token tile);
+    # every output against the oracle, and rows alone equal the batch's rows
+    from bit_quantized_gemm_gb300 import _lib
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert _lib.prefill_tile_q4k(M, N, 152) == ("16-row", tb)
+    x, bits = synth.activations(M + 3 * K, M, K, dtype="bf16", outlier_frac=0.02)
+    sblocks = synth.q4k_weights(N + K, N, K)
+    out, (q, h, s, bs, packed) = gpu_w4a8(bits, sblocks, N, "auto")
+    oq, os_ = oracle.quantize_act(bits)
+    y, ob = oracle.gemm_w4a8_q4k(oq, os_, sblocks)
+    got = out_bits(out)
+    bad = np.argwhere(got != ob)
+    assert bad.size == 0, "first mismatches %s" % bad[:5].tolist()
+    out32, _ = gpu_w4a8(bits, sblocks, N, "auto", out_dtype=torch.float32)
+    assert np.array_equal(out_bits(out32), y.view(np.uint32))
+    for r in (0, M - 1):
         o = qg.gemm_w4a8_q4k(q[r:r + 1], h[r:r + 1], s[r:r + 1], bs[r:r + 1], packed, N)
         assert np.array_equal(out_bits(o)[0], got[r])
 
