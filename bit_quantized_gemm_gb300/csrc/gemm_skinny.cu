@@ -28,30 +28,37 @@
 //     left the loads' latency exposed).
 #include <cuda.h>
 
+#include <cstring>
+
 #include "qg_common.cuh"
 
 namespace qg {
 
 // from gemm_large.cu
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows);
+bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                    uint32_t box_words, uint32_t box_rows);
 
-#ifndef QG_SK_SCALE_AHEAD_Q4K
-#define QG_SK_SCALE_AHEAD_Q4K 2  // the same for W4A8 (four more loads per stage)
-#endif
-#ifndef QG_SK_SCALE_AHEAD
-#define QG_SK_SCALE_AHEAD 4  // stages whose scales are loaded ahead of their use
-#endif
 constexpr int kSkRows = 16;  // weight rows per CTA (the MMA's M)
 constexpr int kSkBK = 64;    // K per stage: two blocks, one 128-byte swizzle row
 
-template <int TB>
+template <int TB, bool kQ4K>
 struct SkinnyCfg {
   static_assert(TB % 16 == 0 && TB >= 16 && TB <= 256, "token tile");
   static constexpr int kWarps = TB / 16;  // compute warps, 16 tokens each
   static constexpr int kThreads = 32 * (kWarps + 1);
   static constexpr uint32_t kABytes = kSkRows * kSkBK * 2;  // 2 KB
   static constexpr uint32_t kBBytes = TB * kSkBK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // multiple of 1024 (swizzle atoms)
+  // every even stage also brings the per-block FMA operands of four blocks
+  // (its own two and the next stage's), 16 bytes per row: the 16 weight rows'
+  // scales d (W4A8: d*sc, and dmin*m) and, W4A8, the TB tokens' activation
+  // block sums; each box 128-byte aligned
+  static constexpr uint32_t kSdOff = kABytes + kBBytes;
+  static constexpr uint32_t kSmOff = kSdOff + 256;
+  static constexpr uint32_t kSsOff = kSdOff + 512;
+  static constexpr uint32_t kSBytes = kQ4K ? 512 + TB * 16 : 256;
+  static constexpr uint32_t kStageBytes =
+      kABytes + kBBytes + (kSBytes + 1023) / 1024 * 1024;  // multiple of 1024 (swizzle atoms)
   // resident CTAs per SM: three of 64 tokens (a shallower ring: 7 stages),
   // else two; 17408 -> 5120 at 33-64 tokens (320 CTAs) then runs as one wave
   static constexpr int kCtas = TB == 64 ? 3 : 2;
@@ -75,14 +82,6 @@ struct SkinnyArgs {
   uint32_t* err;
 };
 
-// 8-byte read-only load of two int32, volatile so the compiler keeps it
-// where it is written (p 8-byte aligned)
-__device__ __forceinline__ int2 ldg_s32x2_pinned(const int32_t* p) {
-  int2 v;
-  asm volatile("ld.global.nc.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -96,10 +95,13 @@ __device__ __forceinline__ uint32_t sw128(int r, int k) {
 }
 
 template <int TB, bool kQ4K>
-__global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
+__global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, kQ4K>::kCtas)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const SkinnyArgs args) {
-  using C = SkinnyCfg<TB>;
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmD,
+                       const __grid_constant__ CUtensorMap tmM,
+                       const __grid_constant__ CUtensorMap tmS, const SkinnyArgs args) {
+  using C = SkinnyCfg<TB, kQ4K>;
   constexpr int kW = C::kWarps;
   constexpr int kS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -122,6 +124,11 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
   if (warp == kW && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+    if (kQ4K) {
+      tma_prefetch_desc(&tmM);
+      tma_prefetch_desc(&tmS);
+    }
   }
   __syncthreads();
 
@@ -133,8 +140,9 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
       bool ok = true;
       // as a programmatic dependent of the quantize kernel: the weight tiles
       // of the first P stages before the wait for its grid, their activation
-      // tiles after it
-      const int P = args.pdl ? min(min(NS, kS), 3) : 0;
+      // tiles after it (W4A8 stages carry activation block sums: wait first)
+      const int P = (args.pdl && !kQ4K) ? min(min(NS, kS), 3) : 0;
+      if (kQ4K && args.pdl) griddep_wait();
       for (int s = 0; s < NS && ok; ++s) {
         ok = mbar_wait(&empty[st], ph ^ 1, args.err);
         if (!ok) break;
@@ -145,8 +153,18 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
         // shared an SM)
         fence_proxy_async_smem();
         uint8_t* a_s = sm + st * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[st], C::kStageBytes);  // whole boxes (zero-filled edges)
+        const bool ops = (s & 1) == 0;  // this stage brings four blocks' FMA operands
+        // whole boxes (zero-filled edges)
+        mbar_arrive_expect_tx(&full[st], C::kABytes + C::kBBytes + (ops ? C::kSBytes : 0));
         tma_load_2d(a_s, &tmA, &full[st], s * kSkBK, n0);
+        if (ops) {
+          // x in 8-byte words: blocks 2s..2s+3 start at word s (even: 16-byte aligned)
+          tma_load_2d(a_s + C::kSdOff, &tmD, &full[st], s, n0);
+          if (kQ4K) {
+            tma_load_2d(a_s + C::kSmOff, &tmM, &full[st], s, n0);
+            tma_load_2d(a_s + C::kSsOff, &tmS, &full[st], s, m0);
+          }
+        }
         if (s >= P) tma_load_2d(a_s + C::kABytes, &tmB, &full[st], s * kSkBK, m0);
         if (s + 1 == P) {
           griddep_wait();
@@ -165,12 +183,8 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
   }
 
   // ------------------------------------------------------------- compute
-  // W4A8: the activation block sums come from the quantize kernel
-  if (kQ4K && args.pdl) griddep_wait();
   const int g = lane >> 2, t = lane & 3;
   const int nA = n0 + g, nB = n0 + g + 8;  // this lane's two weight rows
-  const float* drA = args.d32 + (int64_t)(nA < N ? nA : 0) * args.ldd;
-  const float* drB = args.d32 + (int64_t)(nB < N ? nB : 0) * args.ldd;
   // ldmatrix row addresses: lane l serves row l % 8 of matrix l / 8
   const int mi = lane >> 3, ri = lane & 7;
   const int a_row = ri + 8 * (mi & 1), a_k = 8 * (mi >> 1);      // A: rows 0-15, k 0-15
@@ -181,102 +195,88 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
   for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
 
   // Per stage (two blocks): wait for the slot, sum each block exactly with
-  // four MMAs, hand the slot back, then the blocks' FMAs in block order. The
-  // weight scales of stage s (W4A8: d*sc, dmin*m and this lane's activation
-  // block sums) sit in register slot s % kP, loaded kP stages ahead; the stage
-  // loop is unrolled by kP so that each slot is a fixed set of registers and
-  // no register move waits on a load in flight.
-  constexpr int kP = kQ4K ? QG_SK_SCALE_AHEAD_Q4K : QG_SK_SCALE_AHEAD;
-  constexpr int kPQ = kQ4K ? kP : 1;
-  float2 pA[kP], pB[kP], qA[kPQ], qB[kPQ];
-  int2 pS[kPQ][2][2];  // [slot][token tile][token 2t + e]: sums of the stage's two blocks
-  const float* dmA = kQ4K ? args.dm32 + (int64_t)(nA < N ? nA : 0) * args.ldd : nullptr;
-  const float* dmB = kQ4K ? args.dm32 + (int64_t)(nB < N ? nB : 0) * args.ldd : nullptr;
-  const int mb = m0 + 16 * warp + 2 * t;  // this lane's first token (then +1, +8, +9)
-  // a stage's first block is even and rows are padded to whole quads (Q8_0)
-  // or hold a multiple of 8 blocks (Q4_K): 8-byte loads stay in the row
-  auto load_slot = [&](int j, int s) {
-    const int blk = 2 * s;
-    pA[j] = ldg_f32x2_pinned(drA + blk);
-    pB[j] = ldg_f32x2_pinned(drB + blk);
-    if constexpr (kQ4K) {
-      qA[j] = ldg_f32x2_pinned(dmA + blk);
-      qB[j] = ldg_f32x2_pinned(dmB + blk);
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int m = min(mb + 8 * tt + e, M - 1);  // rows past M: any valid row, unused
-          pS[j][tt][e] = ldg_s32x2_pinned(args.bsum + (int64_t)m * NB + blk);
-        }
-    }
-  };
-#pragma unroll
-  for (int j = 0; j < kP; ++j)
-    if (j < NS) load_slot(j, j);
+  // four MMAs, read the FMA operands that came with an even stage (this
+  // lane's rows g, g+8 and tokens: four blocks, 16-byte loads, one wavefront
+  // each), hand the slot back, then the blocks' FMAs in block order.
+  float4 sdA = make_float4(0.f, 0.f, 0.f, 0.f), sdB = sdA, smA = sdA, smB = sdA;
+  int4 ssv[2][2];  // [token tile][token 2t + e]: activation block sums of four blocks
+  const int tl = 16 * warp + 2 * t;  // this lane's first token in the tile (then +1, +8, +9)
   int st = 0;
   uint32_t ph = 0;
   bool ok = true;
-  for (int s0 = 0; s0 < NS && ok; s0 += kP) {
-#pragma unroll
-    for (int j = 0; j < kP; ++j) {
-      const int s = s0 + j;
-      if (s >= NS) break;
-      ok = mbar_wait(&full[st], ph, args.err);
-      if (!ok) break;
-      // both blocks' sums first (a missing second block of a K tail reads the
-      // zero-filled box and is never used)
-      float d[2][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
-      {
-        const uint32_t a_s = smem_u32(sm + st * C::kStageBytes);
-        const uint32_t b_s = a_s + C::kABytes;
-#pragma unroll
-        for (int jb = 0; jb < 2; ++jb) {
-#pragma unroll
-          for (int kh = 0; kh < 2; ++kh) {
-            const int kc = jb * 32 + kh * 16;
-            uint32_t af[4], bfr[4];
-            ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
-            ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
-            // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
-            float(&dd)[2][4] = d[jb];
-            if (kh == 0) {
-              mma_f16_16816(dd[0], af, bfr[0], bfr[1], zero4);
-              mma_f16_16816(dd[1], af, bfr[2], bfr[3], zero4);
-            } else {
-              mma_f16_16816(dd[0], af, bfr[0], bfr[1], dd[0]);
-              mma_f16_16816(dd[1], af, bfr[2], bfr[3], dd[1]);
-            }
-          }
-        }
-      }
-      mbar_arrive(&empty[st]);  // this thread's reads of the stage are done
-      if (++st == kS) { st = 0; ph ^= 1; }
+  for (int s = 0; s < NS && ok; ++s) {
+    ok = mbar_wait(&full[st], ph, args.err);
+    if (!ok) break;
+    // both blocks' sums first (a missing second block of a K tail reads the
+    // zero-filled box and is never used)
+    float d[2][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
+    const uint8_t* sb = sm + st * C::kStageBytes;
+    {
+      const uint32_t a_s = smem_u32(sb);
+      const uint32_t b_s = a_s + C::kABytes;
 #pragma unroll
       for (int jb = 0; jb < 2; ++jb) {
-        if (2 * s + jb < NB) {
-          const float dA = jb ? pA[j].y : pA[j].x, dB = jb ? pB[j].y : pB[j].x;
-          const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
 #pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
-            acc[tt][0] = __ffma2_rn(make_float2(d[jb][tt][0], d[jb][tt][1]), dA2, acc[tt][0]);
-            acc[tt][1] = __ffma2_rn(make_float2(d[jb][tt][2], d[jb][tt][3]), dB2, acc[tt][1]);
-          }
-          if constexpr (kQ4K) {
-            // then the min term of the same sub-block: fma(-asum, dmin*m, acc)
-            const float mA = jb ? qA[j].y : qA[j].x, mB = jb ? qB[j].y : qB[j].x;
-            const float2 nmA2 = make_float2(-mA, -mA), nmB2 = make_float2(-mB, -mB);
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              const float2 as = jb ? make_float2((float)pS[j][tt][0].y, (float)pS[j][tt][1].y)
-                                   : make_float2((float)pS[j][tt][0].x, (float)pS[j][tt][1].x);
-              acc[tt][0] = __ffma2_rn(as, nmA2, acc[tt][0]);
-              acc[tt][1] = __ffma2_rn(as, nmB2, acc[tt][1]);
-            }
+        for (int kh = 0; kh < 2; ++kh) {
+          const int kc = jb * 32 + kh * 16;
+          uint32_t af[4], bfr[4];
+          ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
+          ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
+          // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
+          float(&dd)[2][4] = d[jb];
+          if (kh == 0) {
+            mma_f16_16816(dd[0], af, bfr[0], bfr[1], zero4);
+            mma_f16_16816(dd[1], af, bfr[2], bfr[3], zero4);
+          } else {
+            mma_f16_16816(dd[0], af, bfr[0], bfr[1], dd[0]);
+            mma_f16_16816(dd[1], af, bfr[2], bfr[3], dd[1]);
           }
         }
       }
-      if (s + kP < NS) load_slot(j, s + kP);
+    }
+    if ((s & 1) == 0) {
+      sdA = *reinterpret_cast<const float4*>(sb + C::kSdOff + g * 16);
+      sdB = *reinterpret_cast<const float4*>(sb + C::kSdOff + (g + 8) * 16);
+      if constexpr (kQ4K) {
+        smA = *reinterpret_cast<const float4*>(sb + C::kSmOff + g * 16);
+        smB = *reinterpret_cast<const float4*>(sb + C::kSmOff + (g + 8) * 16);
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            ssv[tt][e] = *reinterpret_cast<const int4*>(sb + C::kSsOff + (tl + 8 * tt + e) * 16);
+      }
+    }
+    mbar_arrive(&empty[st]);  // this thread's reads of the stage are done
+    if (++st == kS) { st = 0; ph ^= 1; }
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+      if (2 * s + jb < NB) {
+        // block 2s + jb is entry q of the four-block group
+        const bool hi = (s & 1) != 0;
+        const float dA = jb ? (hi ? sdA.w : sdA.y) : (hi ? sdA.z : sdA.x);
+        const float dB = jb ? (hi ? sdB.w : sdB.y) : (hi ? sdB.z : sdB.x);
+        const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          acc[tt][0] = __ffma2_rn(make_float2(d[jb][tt][0], d[jb][tt][1]), dA2, acc[tt][0]);
+          acc[tt][1] = __ffma2_rn(make_float2(d[jb][tt][2], d[jb][tt][3]), dB2, acc[tt][1]);
+        }
+        if constexpr (kQ4K) {
+          // then the min term of the same sub-block: fma(-asum, dmin*m, acc)
+          const float mA = jb ? (hi ? smA.w : smA.y) : (hi ? smA.z : smA.x);
+          const float mB = jb ? (hi ? smB.w : smB.y) : (hi ? smB.z : smB.x);
+          const float2 nmA2 = make_float2(-mA, -mA), nmB2 = make_float2(-mB, -mB);
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            const int a0 = jb ? (hi ? ssv[tt][0].w : ssv[tt][0].y) : (hi ? ssv[tt][0].z : ssv[tt][0].x);
+            const int a1 = jb ? (hi ? ssv[tt][1].w : ssv[tt][1].y) : (hi ? ssv[tt][1].z : ssv[tt][1].x);
+            const float2 as = make_float2((float)a0, (float)a1);  // exact: |v| <= 4064
+            acc[tt][0] = __ffma2_rn(as, nmA2, acc[tt][0]);
+            acc[tt][1] = __ffma2_rn(as, nmB2, acc[tt][1]);
+          }
+        }
+      }
     }
   }
   if (!ok) return;
@@ -303,9 +303,18 @@ __global__ void __launch_bounds__(SkinnyCfg<TB>::kThreads, SkinnyCfg<TB>::kCtas)
 template <int TB, bool kQ4K>
 static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, const SkinnyArgs& a,
                                    cudaStream_t st) {
-  using C = SkinnyCfg<TB>;
-  CUtensorMap ta, tb;
+  using C = SkinnyCfg<TB, kQ4K>;
+  CUtensorMap ta, tb, td, tm, ts;
   if (!make_tmap(&ta, wq16, a.N, a.K, kSkRows) || !make_tmap(&tb, q16, a.M, a.K, TB))
+    return cudaErrorNotSupported;
+  // per-block operands as rows of 8-byte words, boxes of 2 words (four
+  // blocks) x 16 weight rows or TB tokens; rows hold whole quads of blocks
+  const int64_t nb = a.K / kBlk;
+  if (!make_tmap_rows(&td, a.d32, a.N, a.ldd * 4, 2, kSkRows)) return cudaErrorNotSupported;
+  memset(&tm, 0, sizeof(tm));
+  memset(&ts, 0, sizeof(ts));
+  if (kQ4K && (!make_tmap_rows(&tm, a.dm32, a.N, a.ldd * 4, 2, kSkRows) ||
+               !make_tmap_rows(&ts, a.bsum, a.M, nb * 4, 2, TB)))
     return cudaErrorNotSupported;
   auto kern = skinny_gemm_kernel<TB, kQ4K>;
   static std::atomic<uint64_t> attr_set{0};
@@ -314,7 +323,8 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)ceil_div(a.N, kSkRows), (unsigned)ceil_div(a.M, TB));
-  return launch_kernel(kern, grid, dim3(C::kThreads), C::kSmem, st, a.pdl != 0, ta, tb, a);
+  return launch_kernel(kern, grid, dim3(C::kThreads), C::kSmem, st, a.pdl != 0, ta, tb, td, tm, ts,
+                       a);
 }
 
 // Weight rows [0, N) of the packed-layout views passed in (the caller offsets
