@@ -12,9 +12,10 @@
 // the weight rows left over after whole waves of 256-token tiles, and GEMMs
 // whose weight-row tiles cannot fill the SMs. There each 32-block step of a
 // narrow tile pays a fixed barrier round trip (~400 cycles). Here a CTA owns
-// 16 weight rows x TB tokens, and every compute warp owns 16 tokens. Each
-// warp sums a block exactly with four m16n8k16 fp16 MMAs and applies that
-// block's FMAs at once, in registers: no accumulator hand-off at all.
+// 16 weight rows x TB tokens, and every compute warp owns 16 tokens (32 in
+// 64-token tiles). Each warp sums a block exactly with two m16n8k16 fp16 MMAs
+// per 8 tokens and applies that block's FMAs at once, in registers: no
+// accumulator hand-off at all.
 //   * operands: the fp16 copies of the weights ([N][K], from the packed
 //     buffer; Q4_K: the 4-bit values) and activations (q16 [M][K]) arrive by
 //     TMA, 64 K (two blocks) per stage, 128-byte swizzle; fragments come out
@@ -41,11 +42,21 @@ bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
 
 constexpr int kSkRows = 16;  // weight rows per CTA (the MMA's M)
 constexpr int kSkBK = 64;    // K per stage: two blocks, one 128-byte swizzle row
+#ifndef QG_SK_TT64
+#define QG_SK_TT64 4  // n8 token tiles per compute warp of a 64-token tile (others: 2)
+#endif
 
 template <int TB, bool kQ4K>
 struct SkinnyCfg {
   static_assert(TB % 16 == 0 && TB >= 16 && TB <= 256, "token tile");
-  static constexpr int kWarps = TB / 16;  // compute warps, 16 tokens each
+  // n8 token tiles per compute warp: 32 tokens in 64-token tiles (each
+  // weight fragment feeds four MMAs: fewer fragment loads per token on the
+  // L1 data pipe that bounds these tiles; 82.5 -> 78.0 us for 17408 -> 5120
+  // at 64 tokens), else 16 (a 32-token tile with one warp, or 128 tokens with
+  // four, measured slower)
+  static constexpr int kTT = TB == 64 ? QG_SK_TT64 : 2;
+  static_assert(kTT == 2 || kTT == 4, "token tiles per warp");
+  static constexpr int kWarps = TB / (8 * kTT);  // compute warps, 8 * kTT tokens each
   static constexpr int kThreads = 32 * (kWarps + 1);
   static constexpr uint32_t kABytes = kSkRows * kSkBK * 2;  // 2 KB
   static constexpr uint32_t kBBytes = TB * kSkBK * 2;
@@ -103,6 +114,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
                        const __grid_constant__ CUtensorMap tmS, const SkinnyArgs args) {
   using C = SkinnyCfg<TB, kQ4K>;
   constexpr int kW = C::kWarps;
+  constexpr int kTT = C::kTT;
   constexpr int kS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -188,19 +200,20 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
   // ldmatrix row addresses: lane l serves row l % 8 of matrix l / 8
   const int mi = lane >> 3, ri = lane & 7;
   const int a_row = ri + 8 * (mi & 1), a_k = 8 * (mi >> 1);      // A: rows 0-15, k 0-15
-  const int b_row = 16 * warp + ri + 8 * (mi >> 1), b_k = 8 * (mi & 1);  // B: 16 tokens
+  // B: 16 tokens per x4 load (matrices 2, 3: tokens 8-15; 1, 3: k 8-15)
+  const int b_row = 8 * kTT * warp + ri + 8 * (mi >> 1), b_k = 8 * (mi & 1);
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-  float2 acc[2][2];  // [token tile][row nA / nB]: tokens 2t, 2t+1 of the tile
+  float2 acc[kTT][2];  // [token tile][row nA / nB]: tokens 2t, 2t+1 of the tile
 #pragma unroll
-  for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+  for (int i = 0; i < kTT; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
 
   // Per stage (two blocks): wait for the slot, sum each block exactly with
   // four MMAs, read the FMA operands that came with an even stage (this
   // lane's rows g, g+8 and tokens: four blocks, 16-byte loads, one wavefront
   // each), hand the slot back, then the blocks' FMAs in block order.
   float4 sdA = make_float4(0.f, 0.f, 0.f, 0.f), sdB = sdA, smA = sdA, smB = sdA;
-  int4 ssv[2][2];  // [token tile][token 2t + e]: activation block sums of four blocks
-  const int tl = 16 * warp + 2 * t;  // this lane's first token in the tile (then +1, +8, +9)
+  int4 ssv[kTT][2];  // [token tile][token 2t + e]: activation block sums of four blocks
+  const int tl = 8 * kTT * warp + 2 * t;  // this lane's first token in the tile (then +1, +8, ...)
   int st = 0;
   uint32_t ph = 0;
   bool ok = true;
@@ -209,7 +222,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
     if (!ok) break;
     // both blocks' sums first (a missing second block of a K tail reads the
     // zero-filled box and is never used)
-    float d[2][2][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
+    float d[2][kTT][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
     const uint8_t* sb = sm + st * C::kStageBytes;
     {
       const uint32_t a_s = smem_u32(sb);
@@ -219,17 +232,19 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
           const int kc = jb * 32 + kh * 16;
-          uint32_t af[4], bfr[4];
+          uint32_t af[4], bfr[kTT / 2][4];
           ldsm_x4(a_s + sw128(a_row, kc + a_k), af);
-          ldsm_x4(b_s + sw128(b_row, kc + b_k), bfr);
-          // bfr: tile 0 (k 0-7, 8-15), tile 1 (k 0-7, 8-15); a fresh sum per block
-          float(&dd)[2][4] = d[jb];
-          if (kh == 0) {
-            mma_f16_16816(dd[0], af, bfr[0], bfr[1], zero4);
-            mma_f16_16816(dd[1], af, bfr[2], bfr[3], zero4);
-          } else {
-            mma_f16_16816(dd[0], af, bfr[0], bfr[1], dd[0]);
-            mma_f16_16816(dd[1], af, bfr[2], bfr[3], dd[1]);
+#pragma unroll
+          for (int h = 0; h < kTT / 2; ++h) ldsm_x4(b_s + sw128(b_row + 16 * h, kc + b_k), bfr[h]);
+          // bfr[h]: tile 2h (k 0-7, 8-15), tile 2h+1 (k 0-7, 8-15); a fresh sum per block
+          float(&dd)[kTT][4] = d[jb];
+#pragma unroll
+          for (int tt = 0; tt < kTT; ++tt) {
+            const uint32_t* bp = &bfr[tt / 2][2 * (tt & 1)];
+            if (kh == 0)
+              mma_f16_16816(dd[tt], af, bp[0], bp[1], zero4);
+            else
+              mma_f16_16816(dd[tt], af, bp[0], bp[1], dd[tt]);
           }
         }
       }
@@ -241,7 +256,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
         smA = *reinterpret_cast<const float4*>(sb + C::kSmOff + g * 16);
         smB = *reinterpret_cast<const float4*>(sb + C::kSmOff + (g + 8) * 16);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt)
+        for (int tt = 0; tt < kTT; ++tt)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
             ssv[tt][e] = *reinterpret_cast<const int4*>(sb + C::kSsOff + (tl + 8 * tt + e) * 16);
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
         const float dB = jb ? (hi ? sdB.w : sdB.y) : (hi ? sdB.z : sdB.x);
         const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
+        for (int tt = 0; tt < kTT; ++tt) {
           acc[tt][0] = __ffma2_rn(make_float2(d[jb][tt][0], d[jb][tt][1]), dA2, acc[tt][0]);
           acc[tt][1] = __ffma2_rn(make_float2(d[jb][tt][2], d[jb][tt][3]), dB2, acc[tt][1]);
         }
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
           const float mB = jb ? (hi ? smB.w : smB.y) : (hi ? smB.z : smB.x);
           const float2 nmA2 = make_float2(-mA, -mA), nmB2 = make_float2(-mB, -mB);
 #pragma unroll
-          for (int tt = 0; tt < 2; ++tt) {
+          for (int tt = 0; tt < kTT; ++tt) {
             const int a0 = jb ? (hi ? ssv[tt][0].w : ssv[tt][0].y) : (hi ? ssv[tt][0].z : ssv[tt][0].x);
             const int a1 = jb ? (hi ? ssv[tt][1].w : ssv[tt][1].y) : (hi ? ssv[tt][1].z : ssv[tt][1].x);
             const float2 as = make_float2((float)a0, (float)a1);  // exact: |v| <= 4064
@@ -282,10 +297,10 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
   if (!ok) return;
   if (args.pdl) griddep_wait();  // the activation scales come from the quantize kernel
 #pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
+  for (int tt = 0; tt < kTT; ++tt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int m = m0 + 16 * warp + 8 * tt + 2 * t + (e & 1);
+      const int m = m0 + 8 * kTT * warp + 8 * tt + 2 * t + (e & 1);
       const int n = (e < 2) ? nA : nB;
       const float a = (e == 0) ? acc[tt][0].x : (e == 1) ? acc[tt][0].y
                     : (e == 2) ? acc[tt][1].x : acc[tt][1].y;
