@@ -42,19 +42,16 @@ bool make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
 
 constexpr int kSkRows = 16;  // weight rows per CTA (the MMA's M)
 constexpr int kSkBK = 64;    // K per stage: two blocks, one 128-byte swizzle row
-#ifndef QG_SK_TT64
-#define QG_SK_TT64 4  // n8 token tiles per compute warp of a 64-token tile (others: 2)
-#endif
 
-template <int TB, bool kQ4K>
+// kTT = n8 token tiles per compute warp: 4 (32 tokens) in the 64-token tile
+// of a GEMM of at most 64 tokens (each weight fragment feeds four MMAs: fewer
+// fragment loads per token on the L1 data pipe that bounds these tiles;
+// 17408 -> 5120 at 64 tokens 82.5 -> 78.0 us), else 2 (16 tokens: a 32-token
+// tile with one warp, 128-token tiles, and the 256 64-token CTAs of the 4B
+// down projection's tail all measured slower with 32-token warps)
+template <int TB, bool kQ4K, int kTT>
 struct SkinnyCfg {
   static_assert(TB % 16 == 0 && TB >= 16 && TB <= 256, "token tile");
-  // n8 token tiles per compute warp: 32 tokens in 64-token tiles (each
-  // weight fragment feeds four MMAs: fewer fragment loads per token on the
-  // L1 data pipe that bounds these tiles; 82.5 -> 78.0 us for 17408 -> 5120
-  // at 64 tokens), else 16 (a 32-token tile with one warp, or 128 tokens with
-  // four, measured slower)
-  static constexpr int kTT = TB == 64 ? QG_SK_TT64 : 2;
   static_assert(kTT == 2 || kTT == 4, "token tiles per warp");
   static constexpr int kWarps = TB / (8 * kTT);  // compute warps, 8 * kTT tokens each
   static constexpr int kThreads = 32 * (kWarps + 1);
@@ -105,16 +102,15 @@ __device__ __forceinline__ uint32_t sw128(int r, int k) {
   return (uint32_t)(r * 128 + ((((k >> 3) ^ r) & 7) << 4));
 }
 
-template <int TB, bool kQ4K>
-__global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, kQ4K>::kCtas)
+template <int TB, bool kQ4K, int kTT>
+__global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K, kTT>::kThreads, SkinnyCfg<TB, kQ4K, kTT>::kCtas)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmM,
                        const __grid_constant__ CUtensorMap tmS, const SkinnyArgs args) {
-  using C = SkinnyCfg<TB, kQ4K>;
+  using C = SkinnyCfg<TB, kQ4K, kTT>;
   constexpr int kW = C::kWarps;
-  constexpr int kTT = C::kTT;
   constexpr int kS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -315,10 +311,10 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K>::kThreads, SkinnyCfg<TB, k
   }
 }
 
-template <int TB, bool kQ4K>
+template <int TB, bool kQ4K, int kTT = 2>
 static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, const SkinnyArgs& a,
                                    cudaStream_t st) {
-  using C = SkinnyCfg<TB, kQ4K>;
+  using C = SkinnyCfg<TB, kQ4K, kTT>;
   CUtensorMap ta, tb, td, tm, ts;
   if (!make_tmap(&ta, wq16, a.N, a.K, kSkRows) || !make_tmap(&tb, q16, a.M, a.K, TB))
     return cudaErrorNotSupported;
@@ -331,7 +327,7 @@ static cudaError_t launch_skinny_t(const uint16_t* wq16, const uint16_t* q16, co
   if (kQ4K && (!make_tmap_rows(&tm, a.dm32, a.N, a.ldd * 4, 2, kSkRows) ||
                !make_tmap_rows(&ts, a.bsum, a.M, nb * 4, 2, TB)))
     return cudaErrorNotSupported;
-  auto kern = skinny_gemm_kernel<TB, kQ4K>;
+  auto kern = skinny_gemm_kernel<TB, kQ4K, kTT>;
   static std::atomic<uint64_t> attr_set{0};
   {
     const cudaError_t e = smem_attr_once_per_device(kern, (int)C::kSmem, attr_set);
@@ -360,7 +356,9 @@ cudaError_t launch_skinny_q8_0(const uint16_t* q16, const float* sa, int64_t M, 
   a.out_f32 = out_f32 ? 1 : 0;
   a.err = err;
   if (tb == 32) return launch_skinny_t<32, false>(wq16, q16, a, st);
-  if (tb == 64) return launch_skinny_t<64, false>(wq16, q16, a, st);
+  if (tb == 64)
+    return M <= 64 ? launch_skinny_t<64, false, 4>(wq16, q16, a, st)
+                   : launch_skinny_t<64, false, 2>(wq16, q16, a, st);
   return launch_skinny_t<128, false>(wq16, q16, a, st);
 }
 
@@ -385,7 +383,7 @@ cudaError_t launch_skinny_q4k(const uint16_t* q16, const float* sa, const int32_
   a.out_f32 = out_f32 ? 1 : 0;
   a.err = err;
   if (tb == 32) return launch_skinny_t<32, true>(wq16, q16, a, st);
-  return launch_skinny_t<64, true>(wq16, q16, a, st);
+  return launch_skinny_t<64, true, 4>(wq16, q16, a, st);  // at most 64 tokens
 }
 
 }  // namespace qg
