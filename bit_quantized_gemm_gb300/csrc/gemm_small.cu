@@ -89,16 +89,26 @@ __host__ __device__ constexpr int sblk() {
 }
 // CTAs of 320 threads resident per SM (registers and shared memory are
 // budgeted for it)
+// (kKind: 0 the dp4a kernel, 1 / 2 the MMA kernel with one / two token
+// tiles). W4A8 on one MMA token tile (5-8 rows) runs two per SM with a deeper
+// ring: at 8 rows 5120 -> 17408 29.1 -> 25.0 us and 17408 -> 5120 37.6 ->
+// 33.2 us (at 5-6 rows 1-4 % slower); the dp4a kernel with two per SM
+// measured slower (17408 -> 5120 at 1 row 19.0 -> 21.1 us)
 #ifndef QG_DEC_CTAS_Q4K
 #define QG_DEC_CTAS_Q4K 3
+#endif
+#ifndef QG_DEC_CTAS_Q4K_TT1
+#define QG_DEC_CTAS_Q4K_TT1 2
 #endif
 #ifndef QG_DEC_CTAS_Q8
 #define QG_DEC_CTAS_Q8 3
 #endif
-template <bool kQ4K>
-__host__ __device__ constexpr int dec_ctas() { return kQ4K ? QG_DEC_CTAS_Q4K : QG_DEC_CTAS_Q8; }
-template <bool kQ4K>
-constexpr int dec_smem_budget() { return dec_ctas<kQ4K>() == 2 ? 110 * 1024 : 70 * 1024; }
+template <bool kQ4K, int kKind>
+__host__ __device__ constexpr int dec_ctas() {
+  return kQ4K ? (kKind == 1 ? QG_DEC_CTAS_Q4K_TT1 : QG_DEC_CTAS_Q4K) : QG_DEC_CTAS_Q8;
+}
+template <bool kQ4K, int kKind>
+constexpr int dec_smem_budget() { return dec_ctas<kQ4K, kKind>() == 2 ? 110 * 1024 : 70 * 1024; }
 // MMA tiles: blocks whose sums the chain warp loads before their FMAs: 4 for
 // Q8_0, one at a time for Q4_K (whose sub-block terms need the registers).
 #ifndef QG_DEC_HB_Q4K
@@ -361,7 +371,7 @@ __device__ __forceinline__ void decode_produce(const DecodeArgs& a, const CUtens
 // int8 m16n8k32 on the stored bytes, or (build switch) fp16 m16n8k16 on
 // values widened in registers.
 template <int TT, bool kQ4K, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K, TT>())
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmS, const DecodeArgs a) {
   using L = DecodeSmem<TT, kQ4K, false>;
@@ -708,7 +718,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
 // fmaf(-asum, dmin*m, acc)): the same operations in the same order as the
 // MMA kernel and the prefill kernel.
 template <bool kQ4K, int kM, bool kDebug>
-__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
+__global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K, 0>())
     decode_dp4a_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmS, const DecodeArgs a) {
   constexpr int kPairs = (kM + 1) / 2;  // token pairs
@@ -942,7 +952,7 @@ __global__ void __launch_bounds__(32 * (kCompWarps + 2), dec_ctas<kQ4K>())
 // Launch of either decode kernel with layout L over `mrows` activation rows.
 template <class L, bool kQ4K, class Kern>
 static cudaError_t launch_decode(Kern kern, std::atomic<uint64_t>& attr_set, const DecodeArgs& a,
-                                 int mrows, int budget, bool pdl, cudaStream_t st) {
+                                 int mrows, int budget, int ctas, bool pdl, cudaStream_t st) {
   // the attribute only caps the launch size; occupancy follows the size passed at launch
   {
     const cudaError_t e = smem_attr_once_per_device(kern, 200 * 1024, attr_set);
@@ -953,7 +963,7 @@ static cudaError_t launch_decode(Kern kern, std::atomic<uint64_t>& attr_set, con
   b.pdl = pdl ? 1 : 0;
   // persistent: at most the CTAs that are resident at once; each walks
   // groups blockIdx.x, + gridDim.x, ...
-  const int64_t slots = (int64_t)num_sms() * dec_ctas<kQ4K>();
+  const int64_t slots = (int64_t)num_sms() * ctas;
   // with pdl, the CTAs may start while the previous kernel on the stream
   // (the quantize kernel) runs, streaming their first weight stages meanwhile
   const dim3 grid((unsigned)(a.G < slots ? a.G : slots)), block(32 * (kCompWarps + 2));
@@ -972,10 +982,11 @@ template <int TT, bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_mma(const DecodeArgs& a, bool pdl, cudaStream_t st) {
   using L = DecodeSmem<TT, kQ4K, false>;
   // two-tile kernels (9..16 rows) carry twice the activation rows and stash
-  constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K>();
+  constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K, TT>();
   static std::atomic<uint64_t> attr_set{0};
   return launch_decode<L, kQ4K>(decode_gemm_kernel<TT, kQ4K, kDebug>, attr_set, a,
-                                a.M < TT * 8 ? a.M : TT * 8, kBudget, pdl, st);
+                                a.M < TT * 8 ? a.M : TT * 8, kBudget, dec_ctas<kQ4K, TT>(), pdl,
+                                st);
 }
 
 template <bool kQ4K, int kM, bool kDebug>
@@ -983,7 +994,7 @@ static cudaError_t launch_decode_dp4a_m(const DecodeArgs& a, bool pdl, cudaStrea
   using L = DecodeSmem<1, kQ4K, true, (kM + 1) / 2>;
   static std::atomic<uint64_t> attr_set{0};
   return launch_decode<L, kQ4K>(decode_dp4a_kernel<kQ4K, kM, kDebug>, attr_set, a, kM,
-                                dec_smem_budget<kQ4K>(), pdl, st);
+                                dec_smem_budget<kQ4K, 0>(), dec_ctas<kQ4K, 0>(), pdl, st);
 }
 
 template <bool kQ4K, bool kDebug>
