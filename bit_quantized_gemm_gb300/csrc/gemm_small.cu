@@ -103,9 +103,13 @@ __host__ __device__ constexpr int sblk() {
 #ifndef QG_DEC_CTAS_Q8
 #define QG_DEC_CTAS_Q8 3
 #endif
+#ifndef QG_DEC_CTAS_Q8_TT1
+#define QG_DEC_CTAS_Q8_TT1 3
+#endif
 template <bool kQ4K, int kKind>
 __host__ __device__ constexpr int dec_ctas() {
-  return kQ4K ? (kKind == 1 ? QG_DEC_CTAS_Q4K_TT1 : QG_DEC_CTAS_Q4K) : QG_DEC_CTAS_Q8;
+  return kQ4K ? (kKind == 1 ? QG_DEC_CTAS_Q4K_TT1 : QG_DEC_CTAS_Q4K)
+              : (kKind == 1 ? QG_DEC_CTAS_Q8_TT1 : QG_DEC_CTAS_Q8);
 }
 template <bool kQ4K, int kKind>
 constexpr int dec_smem_budget() { return dec_ctas<kQ4K, kKind>() == 2 ? 110 * 1024 : 70 * 1024; }
