@@ -57,22 +57,24 @@ struct SkinnyCfg {
   static constexpr int kThreads = 32 * (kWarps + 1);
   static constexpr uint32_t kABytes = kSkRows * kSkBK * 2;  // 2 KB
   static constexpr uint32_t kBBytes = TB * kSkBK * 2;
+  static constexpr uint32_t kTileBytes = kABytes + kBBytes;  // multiple of 1024 (swizzle atoms)
   // every even stage also brings the per-block FMA operands of four blocks
   // (its own two and the next stage's), 16 bytes per row: the 16 weight rows'
   // scales d (W4A8: d*sc, and dmin*m) and, W4A8, the TB tokens' activation
-  // block sums; each box 128-byte aligned
-  static constexpr uint32_t kSdOff = kABytes + kBBytes;
-  static constexpr uint32_t kSmOff = kSdOff + 256;
-  static constexpr uint32_t kSsOff = kSdOff + 512;
+  // block sums; they land in the stage's operand slot, kept apart from the
+  // tiles (slots 128-byte aligned, each box 128-byte aligned in its slot)
+  static constexpr uint32_t kSdOff = 0;
+  static constexpr uint32_t kSmOff = 256;
+  static constexpr uint32_t kSsOff = 512;
   static constexpr uint32_t kSBytes = kQ4K ? 512 + TB * 16 : 256;
-  static constexpr uint32_t kStageBytes =
-      kABytes + kBBytes + (kSBytes + 1023) / 1024 * 1024;  // multiple of 1024 (swizzle atoms)
+  static constexpr uint32_t kSSlot = (kSBytes + 127) / 128 * 128;
+  static constexpr uint32_t kPerStage = kTileBytes + kSSlot;
   // resident CTAs per SM: three of 64 tokens (a shallower ring: 7 stages),
   // else two; 17408 -> 5120 at 33-64 tokens (320 CTAs) then runs as one wave
   static constexpr int kCtas = TB == 64 ? 3 : 2;
-  static constexpr int kBudget = kCtas == 3 ? 70 * 1024 : 96 * 1024;
-  static constexpr int kStages = kBudget / (int)kStageBytes > 8 ? 8 : kBudget / (int)kStageBytes;
-  static constexpr size_t kSmem = kStages * kStageBytes + 2 * kStages * 8 + 1024;
+  static constexpr int kBudget = kCtas == 3 ? 74 * 1024 : 96 * 1024;
+  static constexpr int kStages = kBudget / (int)kPerStage > 8 ? 8 : kBudget / (int)kPerStage;
+  static constexpr size_t kSmem = kStages * kPerStage + 2 * kStages * 8 + 1024;
   static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "1024-byte aligned tiles");
   static_assert(kStages >= 2, "ring depth");
 };
@@ -115,7 +117,8 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K, kTT>::kThreads, SkinnyCfg<
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kS * C::kStageBytes);
+  uint8_t* const sops = sm + kS * C::kTileBytes;  // the stages' operand slots
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kS * C::kPerStage);
   uint64_t* empty = full + kS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = args.M, N = args.N, K = args.K;
@@ -160,24 +163,25 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K, kTT>::kThreads, SkinnyCfg<
         // (measured: wrong sums for a warp in a few CTAs when three CTAs
         // shared an SM)
         fence_proxy_async_smem();
-        uint8_t* a_s = sm + st * C::kStageBytes;
+        uint8_t* a_s = sm + st * C::kTileBytes;
+        uint8_t* o_s = sops + st * C::kSSlot;
         const bool ops = (s & 1) == 0;  // this stage brings four blocks' FMA operands
         // whole boxes (zero-filled edges)
         mbar_arrive_expect_tx(&full[st], C::kABytes + C::kBBytes + (ops ? C::kSBytes : 0));
         tma_load_2d(a_s, &tmA, &full[st], s * kSkBK, n0);
         if (ops) {
           // x in 8-byte words: blocks 2s..2s+3 start at word s (even: 16-byte aligned)
-          tma_load_2d(a_s + C::kSdOff, &tmD, &full[st], s, n0);
+          tma_load_2d(o_s + C::kSdOff, &tmD, &full[st], s, n0);
           if (kQ4K) {
-            tma_load_2d(a_s + C::kSmOff, &tmM, &full[st], s, n0);
-            tma_load_2d(a_s + C::kSsOff, &tmS, &full[st], s, m0);
+            tma_load_2d(o_s + C::kSmOff, &tmM, &full[st], s, n0);
+            tma_load_2d(o_s + C::kSsOff, &tmS, &full[st], s, m0);
           }
         }
         if (s >= P) tma_load_2d(a_s + C::kABytes, &tmB, &full[st], s * kSkBK, m0);
         if (s + 1 == P) {
           griddep_wait();
           for (int r = 0; r < P; ++r)
-            tma_load_2d(sm + r * C::kStageBytes + C::kABytes, &tmB, &full[r], r * kSkBK, m0);
+            tma_load_2d(sm + r * C::kTileBytes + C::kABytes, &tmB, &full[r], r * kSkBK, m0);
         }
         if (++st == kS) { st = 0; ph ^= 1; }
       }
@@ -219,7 +223,8 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K, kTT>::kThreads, SkinnyCfg<
     // both blocks' sums first (a missing second block of a K tail reads the
     // zero-filled box and is never used)
     float d[2][kTT][4];  // [block][token tile]: (nA, 2t), (nA, 2t+1), (nB, 2t), (nB, 2t+1)
-    const uint8_t* sb = sm + st * C::kStageBytes;
+    const uint8_t* sb = sm + st * C::kTileBytes;
+    const uint8_t* ob = sops + st * C::kSSlot;
     {
       const uint32_t a_s = smem_u32(sb);
       const uint32_t b_s = a_s + C::kABytes;
@@ -246,16 +251,16 @@ __global__ void __launch_bounds__(SkinnyCfg<TB, kQ4K, kTT>::kThreads, SkinnyCfg<
       }
     }
     if ((s & 1) == 0) {
-      sdA = *reinterpret_cast<const float4*>(sb + C::kSdOff + g * 16);
-      sdB = *reinterpret_cast<const float4*>(sb + C::kSdOff + (g + 8) * 16);
+      sdA = *reinterpret_cast<const float4*>(ob + C::kSdOff + g * 16);
+      sdB = *reinterpret_cast<const float4*>(ob + C::kSdOff + (g + 8) * 16);
       if constexpr (kQ4K) {
-        smA = *reinterpret_cast<const float4*>(sb + C::kSmOff + g * 16);
-        smB = *reinterpret_cast<const float4*>(sb + C::kSmOff + (g + 8) * 16);
+        smA = *reinterpret_cast<const float4*>(ob + C::kSmOff + g * 16);
+        smB = *reinterpret_cast<const float4*>(ob + C::kSmOff + (g + 8) * 16);
 #pragma unroll
         for (int tt = 0; tt < kTT; ++tt)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            ssv[tt][e] = *reinterpret_cast<const int4*>(sb + C::kSsOff + (tl + 8 * tt + e) * 16);
+            ssv[tt][e] = *reinterpret_cast<const int4*>(ob + C::kSsOff + (tl + 8 * tt + e) * 16);
       }
     }
     mbar_arrive(&empty[st]);  // this thread's reads of the stage are done
