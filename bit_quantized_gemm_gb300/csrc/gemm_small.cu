@@ -100,6 +100,9 @@ __host__ __device__ constexpr int sblk() {
 #ifndef QG_DEC_CTAS_Q4K_TT1
 #define QG_DEC_CTAS_Q4K_TT1 2
 #endif
+#ifndef QG_DEC_CTAS_Q4K_TT2
+#define QG_DEC_CTAS_Q4K_TT2 3
+#endif
 #ifndef QG_DEC_CTAS_Q8
 #define QG_DEC_CTAS_Q8 3
 #endif
@@ -108,7 +111,7 @@ __host__ __device__ constexpr int sblk() {
 #endif
 template <bool kQ4K, int kKind>
 __host__ __device__ constexpr int dec_ctas() {
-  return kQ4K ? (kKind == 1 ? QG_DEC_CTAS_Q4K_TT1 : QG_DEC_CTAS_Q4K)
+  return kQ4K ? (kKind == 1 ? QG_DEC_CTAS_Q4K_TT1 : kKind == 2 ? QG_DEC_CTAS_Q4K_TT2 : QG_DEC_CTAS_Q4K)
               : (kKind == 1 ? QG_DEC_CTAS_Q8_TT1 : QG_DEC_CTAS_Q8);
 }
 template <bool kQ4K, int kKind>
@@ -986,7 +989,8 @@ template <int TT, bool kQ4K, bool kDebug>
 static cudaError_t launch_decode_mma(const DecodeArgs& a, bool pdl, cudaStream_t st) {
   using L = DecodeSmem<TT, kQ4K, false>;
   // two-tile kernels (9..16 rows) carry twice the activation rows and stash
-  constexpr int kBudget = TT == 2 ? QG_DEC_BUDGET_TT2_KB * 1024 : dec_smem_budget<kQ4K, TT>();
+  constexpr int kBudget = (TT == 2 && dec_ctas<kQ4K, TT>() != 2) ? QG_DEC_BUDGET_TT2_KB * 1024
+                                                                  : dec_smem_budget<kQ4K, TT>();
   static std::atomic<uint64_t> attr_set{0};
   return launch_decode<L, kQ4K>(decode_gemm_kernel<TT, kQ4K, kDebug>, attr_set, a,
                                 a.M < TT * 8 ? a.M : TT * 8, kBudget, dec_ctas<kQ4K, TT>(), pdl,
